@@ -1,0 +1,204 @@
+/*
+ * arfuse.h -- C ABI of libarfuse: the fused decode-layer boundary op for one
+ * GB300 (sm_103a) GPU.
+ *
+ * For every token row t (0 <= t < T) and column j (0 <= j < H) the library
+ * computes, accumulating in fp32:
+ *
+ *   y[t,j]   = sum_{r<R} ( sum_{k<K} w[t,k] * E_r[perm[t,k], j]  +  S_r[t,j] )
+ *   h[t,j]   = y[t,j] + residual[t,j]                       -> residual_out
+ *   out[t,j] = h[t,j] * rsqrt( (1/H) sum_j h[t,j]^2 + eps ) * (gamma[j] + weight_bias)
+ *
+ * i.e. the MoE finalize (weighted gather of the permuted expert-output rows
+ * back to token order), the shared-expert add, the arithmetic of the
+ * post-experts tensor-parallel all-reduce over R rank partials that all sit
+ * in this GPU's memory, the residual add and the next layer's input RMSNorm,
+ * in one launch.
+ *   - The fold of finalize + shared add + all-reduce into the next input norm:
+ *     sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and wire it
+ *     for DeepSeek-V3 / GLM-5.x", Motivation.
+ *   - The (gamma + weight_bias) scale, with weight_bias = 0 both for plain
+ *     RMSNorm weights and for Gemma-style weights stored as checkpoint + 1:
+ *     same page, Modifications section 1.
+ *   - S_r added without a gate, once per rank partial (a replicated shared
+ *     expert must not be passed as a partial): same page, Modifications
+ *     section 2.
+ *   - The K = 0 form (trailing all-reduce + residual RMSNorm), the mandatory
+ *     residual and the clean decline that lets the caller run its own split
+ *     path: sglang PR #37104 "perf(mtp): fuse trailing TP all-reduce with
+ *     final RMSNorm", Changes.
+ *   - One workspace per model, shared by its layers and fixed per
+ *     hidden / top_k / eps; calls capturable in a CUDA graph: sglang PR
+ *     #37196, Modifications section 2, and sglang PR #37104, Correctness.
+ *
+ * Conventions for every entry point below:
+ *   - "device" pointers point into memory of the workspace's GPU; "host"
+ *     pointers point into ordinary host memory and are read during the call
+ *     only (the library keeps no reference to them after it returns).
+ *   - The caller owns every tensor.  The library owns only the workspace.
+ *   - Layouts are dense row-major with no padding; bf16 is IEEE bfloat16.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = the legacy default stream).  They never allocate, free or
+ *     synchronise, so they can be captured in a CUDA graph.  The caller's
+ *     current device must be the workspace's device.
+ *   - The returned status covers host-side validation and the launch only.
+ *     Any status other than AR_OK means nothing was launched: the caller can
+ *     fall back to its own unfused path.
+ *   - Device-side problems (a perm value outside [0, rows_e); a pipeline wait
+ *     that ran past its time limit) never fault: the kernel clamps or gives
+ *     up, records a bit in the workspace's error word and still returns;
+ *     read it with ar_workspace_device_error() after synchronising.
+ */
+#ifndef ARFUSE_H
+#define ARFUSE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ARFUSE_API __attribute__((visibility("default")))
+#else
+#define ARFUSE_API
+#endif
+
+/* Limits of this build. */
+#define AR_MAX_RANKS 16      /* R: rank partials per call            */
+#define AR_MAX_TOP_K 16      /* K: routed experts per token          */
+#define AR_MAX_HIDDEN 16384  /* H: columns per row (multiple of 8)   */
+
+typedef enum ar_status {
+    AR_OK = 0,
+    AR_ERR_INVALID_ARG = 1,  /* NULL / inconsistent / overlapping arguments   */
+    AR_ERR_ALIGNMENT = 2,    /* a pointer not 16-byte aligned, or H % 8 != 0   */
+    AR_ERR_UNSUPPORTED = 3,  /* outside this build's limits                   */
+    AR_ERR_CAPACITY = 4,     /* T larger than the workspace's max_tokens       */
+    AR_ERR_CUDA = 5,         /* a CUDA runtime call or the launch failed      */
+    AR_ERR_DEVICE_CHECK = 6, /* a device-side check fired (see device_error)  */
+    AR_VALIDATED = 7         /* dry-run workspace: arguments valid, no launch */
+} ar_status;
+
+/* ar_workspace_create() flags. */
+#define AR_WS_DRY_RUN 0x1u   /* no GPU state: calls validate, then return AR_VALIDATED */
+
+/* Bits of the device error word (ar_workspace_device_error). */
+#define AR_DEVERR_PERM_RANGE 0x1   /* some perm value was outside [0, rows_e); clamped */
+#define AR_DEVERR_TIMEOUT 0x2      /* a pipeline wait gave up after its time limit     */
+
+/* Kernel regimes (ar_workspace_set_regime / ar_workspace_last_regime). */
+#define AR_REGIME_AUTO 0     /* pick by (T, R, K, H) and the tuned crossover      */
+#define AR_REGIME_CLUSTER 1  /* small T: one thread-block cluster per token row   */
+#define AR_REGIME_STREAM 2   /* large T: persistent CTAs, bulk-copy ring per row  */
+
+typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
+
+/*
+ * Create the workspace for one model: fixes ranks (R), top_k (K), hidden (H)
+ * and eps, as the model's MoE layers share them.  Allocates a small device
+ * block (the error word) on `device` and sets kernel attributes; call it once,
+ * outside any stream capture.
+ *   device      CUDA device ordinal (ignored with AR_WS_DRY_RUN)
+ *   ranks       1 .. AR_MAX_RANKS
+ *   top_k       0 .. AR_MAX_TOP_K (0: only ar_rmsnorm is meaningful)
+ *   hidden      8 .. AR_MAX_HIDDEN, a multiple of 8
+ *   max_tokens  largest T any call may pass (>= 1)
+ *   eps         RMSNorm epsilon every call must repeat
+ *   flags       0 or AR_WS_DRY_RUN
+ *   out         host pointer that receives the handle (set to NULL on error)
+ * Errors: AR_ERR_INVALID_ARG (out NULL, max_tokens < 1, eps < 0 or not
+ * finite), AR_ERR_ALIGNMENT (hidden % 8), AR_ERR_UNSUPPORTED (limits above,
+ * or a device older than sm_100), AR_ERR_CUDA.
+ */
+ARFUSE_API ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden,
+                                         int64_t max_tokens, float eps, unsigned flags,
+                                         ar_workspace** out);
+
+/* Free the workspace.  NULL is accepted.  Synchronises nothing: the caller
+ * must make sure no call using it is still running. */
+ARFUSE_API ar_status ar_workspace_destroy(ar_workspace* ws);
+
+/*
+ * The fused op (routed + shared + rank sum + residual + RMSNorm).
+ *   ws            workspace; R, K, H and eps must equal its values
+ *   expert_out    host array [R] of device pointers, each bf16 [rows_e, H]:
+ *                 rank r's expert outputs in permuted (expert-grouped) order
+ *   rows_e        rows of every expert_out[r] (>= 1 when K > 0)
+ *   perm          device int32 [T, K]: perm[t*K + k] is the row of every
+ *                 expert_out[r] that holds token t's k-th routed expert
+ *                 (a gather index; duplicates are allowed)
+ *   topk_w        device fp32 [T, K] routing weights (any routed scaling
+ *                 already folded in)
+ *   shared_out    host array [R] of device pointers, each bf16 [T, H]: rank
+ *                 r's shared-expert partial; or NULL for no shared term
+ *   residual      device bf16 [T, H], required (NULL is AR_ERR_INVALID_ARG)
+ *   gamma         device bf16 [H] norm weight
+ *   weight_bias   added to gamma in fp32 (0 for plain and for Gemma weights
+ *                 stored as checkpoint + 1)
+ *   eps           must equal the workspace's eps
+ *   T, R, K, H    tokens, rank partials, routed experts per token, hidden
+ *   out           device bf16 [T, H]
+ *   residual_out  device [T, H], bf16 or fp32 (see next); may be the same
+ *                 pointer as residual when bf16 (in-place update)
+ *   residual_out_is_fp32  0: bf16 residual_out, 1: fp32
+ *   stream        cudaStream_t
+ * K == 0 means no routed term; K == 0 with shared_out == NULL is
+ * AR_ERR_INVALID_ARG (nothing to reduce).  T == 0 returns AR_OK at once.
+ * Alignment: every data pointer 16-byte aligned, perm and topk_w 4-byte
+ * aligned (else AR_ERR_ALIGNMENT).  out and residual_out must not overlap
+ * each other or any input, except the exact in-place residual alias above
+ * (else AR_ERR_INVALID_ARG).  T > max_tokens is AR_ERR_CAPACITY.
+ */
+ARFUSE_API ar_status ar_finalize_rmsnorm(ar_workspace* ws,
+                                         const void* const* expert_out, int64_t rows_e,
+                                         const int32_t* perm, const float* topk_w,
+                                         const void* const* shared_out,
+                                         const void* residual, const void* gamma,
+                                         float weight_bias, float eps,
+                                         int64_t T, int R, int K, int H,
+                                         void* out, void* residual_out,
+                                         int residual_out_is_fp32, void* stream);
+
+/*
+ * Trailing all-reduce + residual RMSNorm without a MoE term (the K = 0 form):
+ * h = sum_r partials[r] + residual; out = RMSNorm(h).  `partials` is a host
+ * array [R] of device pointers, each bf16 [T, H].  R and H must equal the
+ * workspace's; its top_k is not used.  Everything else as for
+ * ar_finalize_rmsnorm.
+ */
+ARFUSE_API ar_status ar_rmsnorm(ar_workspace* ws, const void* const* partials, int R,
+                                const void* residual, const void* gamma,
+                                float weight_bias, float eps, int64_t T, int H,
+                                void* out, void* residual_out, int residual_out_is_fp32,
+                                void* stream);
+
+/*
+ * Read and clear the workspace's device error word (AR_DEVERR_* bits) into
+ * *code (host pointer).  Synchronises the workspace's device first.  Returns
+ * AR_ERR_DEVICE_CHECK when a bit was set, AR_OK when none, AR_ERR_INVALID_ARG
+ * for NULL arguments, AR_ERR_CUDA on a failed copy.
+ */
+ARFUSE_API ar_status ar_workspace_device_error(ar_workspace* ws, int* code);
+
+/*
+ * Force a kernel regime (AR_REGIME_*) for later calls on this workspace, e.g.
+ * to test both kernels at every T.  AR_REGIME_AUTO restores the tuned choice.
+ * A forced regime that cannot run a given call makes that call return
+ * AR_ERR_UNSUPPORTED.
+ */
+ARFUSE_API ar_status ar_workspace_set_regime(ar_workspace* ws, int regime);
+
+/* Regime (AR_REGIME_CLUSTER / AR_REGIME_STREAM) of the last launched call,
+ * 0 before the first one.  *cluster_ctas receives the CTAs per row (cluster
+ * regime) or the persistent grid size (stream regime); may be NULL. */
+ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* cluster_ctas);
+
+/* Static description of a status code; never NULL. */
+ARFUSE_API const char* ar_status_string(ar_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ARFUSE_H */

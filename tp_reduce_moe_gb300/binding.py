@@ -1,0 +1,272 @@
+"""Thin ctypes binding of libarfuse (include/arfuse.h): argument marshalling only.
+
+Every step of the operator runs in the CUDA library; this module turns torch
+tensors into device pointers and sizes, checks that their shapes agree with
+the sizes passed (the C ABI sees only pointers), and raises on any status
+other than AR_OK.  There is no CPU path: if the library is missing, loading it
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+import weakref
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libarfuse.so")
+
+AR_OK = 0
+AR_ERR_INVALID_ARG = 1
+AR_ERR_ALIGNMENT = 2
+AR_ERR_UNSUPPORTED = 3
+AR_ERR_CAPACITY = 4
+AR_ERR_CUDA = 5
+AR_ERR_DEVICE_CHECK = 6
+AR_VALIDATED = 7
+
+AR_WS_DRY_RUN = 0x1
+AR_DEVERR_PERM_RANGE = 0x1
+AR_DEVERR_TIMEOUT = 0x2
+AR_REGIME_AUTO = 0
+AR_REGIME_CLUSTER = 1
+AR_REGIME_STREAM = 2
+
+AR_MAX_RANKS = 16
+AR_MAX_TOP_K = 16
+AR_MAX_HIDDEN = 16384
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ArfuseError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {ar_status_string(status)} (status {status})")
+
+
+def load_library(path: str | None = None):
+    """Load libarfuse.so (built by ``tp_reduce_moe_gb300.build``).  Raises if
+    it is missing: there is no fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libarfuse.so not found at {p}; build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        P, I, I64, F, U = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                           ctypes.c_uint)
+        lib.ar_workspace_create.restype = I
+        lib.ar_workspace_create.argtypes = [I, I, I, I, I64, F, U, ctypes.POINTER(P)]
+        lib.ar_workspace_destroy.restype = I
+        lib.ar_workspace_destroy.argtypes = [P]
+        lib.ar_finalize_rmsnorm.restype = I
+        lib.ar_finalize_rmsnorm.argtypes = [P, P, I64, P, P, P, P, P, F, F, I64, I, I, I,
+                                            P, P, I, P]
+        lib.ar_rmsnorm.restype = I
+        lib.ar_rmsnorm.argtypes = [P, P, I, P, P, F, F, I64, I, P, P, I, P]
+        lib.ar_workspace_device_error.restype = I
+        lib.ar_workspace_device_error.argtypes = [P, ctypes.POINTER(I)]
+        lib.ar_workspace_set_regime.restype = I
+        lib.ar_workspace_set_regime.argtypes = [P, I]
+        lib.ar_workspace_last_regime.restype = I
+        lib.ar_workspace_last_regime.argtypes = [P, ctypes.POINTER(I)]
+        lib.ar_status_string.restype = ctypes.c_char_p
+        lib.ar_status_string.argtypes = [I]
+        _lib = lib
+        return lib
+
+
+def ar_status_string(status: int) -> str:
+    return load_library().ar_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str, ok=(AR_OK,)):
+    if status not in ok:
+        raise ArfuseError(status, where)
+    return status
+
+
+class Workspace:
+    """Owner of one ``ar_workspace*`` (fixed R, K, H, eps, max_tokens)."""
+
+    def __init__(self, handle: int, R: int, K: int, H: int, max_tokens: int, eps: float,
+                 device: int, dry_run: bool):
+        self.handle = handle
+        self.R, self.K, self.H = R, K, H
+        self.max_tokens, self.eps, self.device, self.dry_run = max_tokens, eps, device, dry_run
+        self._fin = weakref.finalize(self, _destroy_handle, handle)
+
+    def destroy(self):
+        self._fin()
+
+    @property
+    def alive(self) -> bool:
+        return self._fin.alive
+
+
+def _destroy_handle(handle):
+    if handle:
+        load_library().ar_workspace_destroy(ctypes.c_void_p(handle))
+
+
+def ar_workspace_create(ranks: int, top_k: int, hidden: int, max_tokens: int, eps: float,
+                        device: int | None = None, flags: int = 0) -> Workspace:
+    lib = load_library()
+    dry = bool(flags & AR_WS_DRY_RUN)
+    if device is None:
+        device = torch.cuda.current_device() if not dry else 0
+    h = ctypes.c_void_p()
+    _check(lib.ar_workspace_create(int(device), int(ranks), int(top_k), int(hidden),
+                                   int(max_tokens), float(eps), int(flags), ctypes.byref(h)),
+           "ar_workspace_create")
+    return Workspace(h.value, ranks, top_k, hidden, max_tokens, eps, device, dry)
+
+
+def ar_workspace_destroy(ws: Workspace) -> None:
+    ws.destroy()
+
+
+def ar_workspace_set_regime(ws: Workspace, regime: int) -> None:
+    _check(load_library().ar_workspace_set_regime(ctypes.c_void_p(ws.handle), int(regime)),
+           "ar_workspace_set_regime")
+
+
+def ar_workspace_last_regime(ws: Workspace):
+    n = ctypes.c_int(0)
+    r = load_library().ar_workspace_last_regime(ctypes.c_void_p(ws.handle), ctypes.byref(n))
+    return int(r), int(n.value)
+
+
+def ar_workspace_device_error(ws: Workspace) -> int:
+    """Synchronise, read and clear the device error word (AR_DEVERR_* bits)."""
+    code = ctypes.c_int(0)
+    st = load_library().ar_workspace_device_error(ctypes.c_void_p(ws.handle), ctypes.byref(code))
+    _check(st, "ar_workspace_device_error", ok=(AR_OK, AR_ERR_DEVICE_CHECK))
+    return int(code.value)
+
+
+# ------------------------------------------------------------------ marshalling
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _need(t, dtype, shape, name):
+    if isinstance(t, int):       # raw device address: the caller vouches for it
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _ptr_array(ts):
+    return (ctypes.c_void_p * len(ts))(*[_ptr(t) for t in ts])
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def ar_finalize_rmsnorm(ws: Workspace, expert_out, perm, topk_w, shared_out, residual, gamma,
+                        weight_bias: float, eps: float, out=None, residual_out=None,
+                        residual_out_fp32: bool = False, stream=None, rows_e: int | None = None,
+                        T: int | None = None):
+    """Fused MoE finalize + shared add + rank sum + residual + RMSNorm.
+
+    expert_out: list of R bf16 [rows_e, H] tensors; perm int32 [T, K]; topk_w
+    fp32 [T, K]; shared_out: list of R bf16 [T, H] or None; residual bf16
+    [T, H]; gamma bf16 [H].  Returns (out, residual_out); outputs are
+    allocated when not given.  ``residual_out`` may be ``residual`` (in place,
+    bf16 only).
+    """
+    R, K, H = ws.R, ws.K, ws.H
+    if T is None:
+        T = residual.shape[0]
+    if K == 0 and not expert_out:
+        expert_out = []
+    elif len(expert_out) != R:
+        raise ValueError(f"expert_out has {len(expert_out)} entries, workspace has R={R}")
+    if rows_e is None:
+        rows_e = expert_out[0].shape[0] if K > 0 else 0
+    for r, e in enumerate(expert_out):
+        _need(e, torch.bfloat16, (rows_e, H), f"expert_out[{r}]")
+    if K > 0:
+        _need(perm, torch.int32, (T, K), "perm")
+        _need(topk_w, torch.float32, (T, K), "topk_w")
+    if shared_out is not None:
+        if len(shared_out) != R:
+            raise ValueError("shared_out must have R entries")
+        for r, s in enumerate(shared_out):
+            _need(s, torch.bfloat16, (T, H), f"shared_out[{r}]")
+    _need(residual, torch.bfloat16, (T, H), "residual")
+    _need(gamma, torch.bfloat16, (H,), "gamma")
+    dev = residual.device if not isinstance(residual, int) else None
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if residual_out is None:
+        residual_out = torch.empty((T, H), dtype=torch.float32 if residual_out_fp32 else torch.bfloat16,
+                                   device=dev)
+    _need(out, torch.bfloat16, (T, H), "out")
+    _need(residual_out, torch.float32 if residual_out_fp32 else torch.bfloat16, (T, H),
+          "residual_out")
+    e_arr = _ptr_array(expert_out) if K > 0 else None
+    s_arr = _ptr_array(shared_out) if shared_out is not None else None
+    st = load_library().ar_finalize_rmsnorm(
+        ctypes.c_void_p(ws.handle), ctypes.cast(e_arr, ctypes.c_void_p) if e_arr is not None else None,
+        int(rows_e), _ptr(perm) if K > 0 else None, _ptr(topk_w) if K > 0 else None,
+        ctypes.cast(s_arr, ctypes.c_void_p) if s_arr is not None else None,
+        _ptr(residual), _ptr(gamma), float(weight_bias), float(eps), int(T), int(R), int(K), int(H),
+        _ptr(out), _ptr(residual_out), 1 if residual_out_fp32 else 0,
+        _stream_handle(stream, dev) if not ws.dry_run else None)
+    _check(st, "ar_finalize_rmsnorm", ok=(AR_OK, AR_VALIDATED) if ws.dry_run else (AR_OK,))
+    return out, residual_out
+
+
+def ar_rmsnorm(ws: Workspace, partials, residual, gamma, weight_bias: float, eps: float, out=None,
+               residual_out=None, residual_out_fp32: bool = False, stream=None,
+               T: int | None = None):
+    """Trailing all-reduce + residual RMSNorm (no MoE term): h = sum_r partials[r]
+    + residual, out = RMSNorm(h).  Returns (out, residual_out)."""
+    R, H = ws.R, ws.H
+    if T is None:
+        T = residual.shape[0]
+    if len(partials) != R:
+        raise ValueError(f"partials has {len(partials)} entries, workspace has R={R}")
+    for r, s in enumerate(partials):
+        _need(s, torch.bfloat16, (T, H), f"partials[{r}]")
+    _need(residual, torch.bfloat16, (T, H), "residual")
+    _need(gamma, torch.bfloat16, (H,), "gamma")
+    dev = residual.device if not isinstance(residual, int) else None
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if residual_out is None:
+        residual_out = torch.empty((T, H), dtype=torch.float32 if residual_out_fp32 else torch.bfloat16,
+                                   device=dev)
+    _need(out, torch.bfloat16, (T, H), "out")
+    _need(residual_out, torch.float32 if residual_out_fp32 else torch.bfloat16, (T, H),
+          "residual_out")
+    p_arr = _ptr_array(partials)
+    st = load_library().ar_rmsnorm(
+        ctypes.c_void_p(ws.handle), ctypes.cast(p_arr, ctypes.c_void_p), int(R), _ptr(residual),
+        _ptr(gamma), float(weight_bias), float(eps), int(T), int(H), _ptr(out), _ptr(residual_out),
+        1 if residual_out_fp32 else 0, _stream_handle(stream, dev) if not ws.dry_run else None)
+    _check(st, "ar_rmsnorm", ok=(AR_OK, AR_VALIDATED) if ws.dry_run else (AR_OK,))
+    return out, residual_out

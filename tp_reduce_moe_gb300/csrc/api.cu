@@ -1,0 +1,356 @@
+// api.cu -- the C ABI of libarfuse (declared in include/arfuse.h): argument
+// validation, the workspace, and the choice of kernel regime per call.
+//
+// Validation follows the pages' contract for the fused boundary: a residual is
+// required and any decline must leave the caller free to run its own split
+// path (sglang PR #37104 "perf(mtp): fuse trailing TP all-reduce with final
+// RMSNorm", Changes); one workspace serves all layers of a model and is fixed
+// per hidden / top_k / eps (sglang PR #37196 "[Comm] Share the CuTe DSL AR
+// fusion core and wire it for DeepSeek-V3 / GLM-5.x", Modifications section
+// 2).  Nothing here allocates or synchronises on the call path, so a call can
+// be captured in a CUDA graph.
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "arf_common.cuh"
+#include "arfuse.h"
+
+struct ar_workspace {
+    int device;
+    int R, K, H;
+    int64_t max_tokens;
+    float eps;
+    unsigned flags;
+    unsigned* d_err;  // device error word (AR_DEVERR_* bits)
+    int num_sms;
+    int smem_optin;
+    int max_cluster;  // largest co-schedulable cluster for the cluster kernel
+    int regime_force;
+    int last_regime;
+    int last_ctas;
+    bool stream_ok;
+    arf::StreamPlan splan;
+    int64_t stream_min_tokens;  // crossover: T >= this runs the stream kernel
+};
+
+namespace {
+
+constexpr int64_t kMaxTokensLimit = int64_t(1) << 26;
+constexpr int kDryRunSms = 152;          // GB300
+constexpr int kDryRunSmemOptin = 232448;  // 227 KB
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void* p, int64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+// Crossover between the cluster (small T) and stream (large T) kernels.
+int64_t default_stream_min_tokens(int R, int K, int H, int num_sms) {
+    (void)R;
+    (void)K;
+    (void)H;
+    return 2LL * num_sms;
+}
+
+ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int32_t* perm,
+              const float* w, const void* const* S, const void* residual, const void* gamma,
+              float weight_bias, float eps, int64_t T, int R, int K, int H, void* out,
+              void* residual_out, int res_f32, void* stream, bool routed_call) {
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (R != ws->R || H != ws->H) return AR_ERR_INVALID_ARG;
+    if (routed_call && K != ws->K) return AR_ERR_INVALID_ARG;
+    if (!(eps == ws->eps)) return AR_ERR_INVALID_ARG;
+    if (T < 0) return AR_ERR_INVALID_ARG;
+    if (T > ws->max_tokens) return AR_ERR_CAPACITY;
+    if (res_f32 != 0 && res_f32 != 1) return AR_ERR_INVALID_ARG;
+    if (T == 0) return AR_OK;
+    if (!residual || !gamma || !out || !residual_out) return AR_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!E || !perm || !w || rows_e < 1) return AR_ERR_INVALID_ARG;
+        if (rows_e > (INT64_MAX / 4) / H) return AR_ERR_INVALID_ARG;
+        for (int r = 0; r < R; ++r)
+            if (!E[r]) return AR_ERR_INVALID_ARG;
+    }
+    if (K == 0 && !S) return AR_ERR_INVALID_ARG;  // nothing to reduce
+    if (S)
+        for (int r = 0; r < R; ++r)
+            if (!S[r]) return AR_ERR_INVALID_ARG;
+
+    // Alignment: 16-byte vectors and bulk copies everywhere.
+    if (!aligned(residual, 16) || !aligned(gamma, 16) || !aligned(out, 16) ||
+        !aligned(residual_out, 16))
+        return AR_ERR_ALIGNMENT;
+    if (K > 0) {
+        if (!aligned(perm, 4) || !aligned(w, 4)) return AR_ERR_ALIGNMENT;
+        for (int r = 0; r < R; ++r)
+            if (!aligned(E[r], 16)) return AR_ERR_ALIGNMENT;
+    }
+    if (S)
+        for (int r = 0; r < R; ++r)
+            if (!aligned(S[r], 16)) return AR_ERR_ALIGNMENT;
+
+    // Outputs must not overlap each other or an input (the exact bf16 in-place
+    // residual alias excepted).
+    const int64_t row2 = T * H * 2;
+    const Range r_out = range_of(out, row2);
+    const Range r_rout = range_of(residual_out, res_f32 ? 2 * row2 : row2);
+    const bool inplace = (residual_out == residual) && !res_f32;
+    if (overlap(r_out, r_rout)) return AR_ERR_INVALID_ARG;
+    Range ins[2 * AR_MAX_RANKS + 4];
+    int n_in = 0;
+    ins[n_in++] = range_of(gamma, (int64_t)H * 2);
+    if (K > 0) {
+        ins[n_in++] = range_of(perm, T * K * 4);
+        ins[n_in++] = range_of(w, T * K * 4);
+        for (int r = 0; r < R; ++r) ins[n_in++] = range_of(E[r], rows_e * H * 2);
+    }
+    if (S)
+        for (int r = 0; r < R; ++r) ins[n_in++] = range_of(S[r], row2);
+    for (int i = 0; i < n_in; ++i)
+        if (overlap(r_out, ins[i]) || overlap(r_rout, ins[i])) return AR_ERR_INVALID_ARG;
+    const Range r_res = range_of(residual, row2);
+    if (overlap(r_out, r_res)) return AR_ERR_INVALID_ARG;
+    if (!inplace && overlap(r_rout, r_res)) return AR_ERR_INVALID_ARG;
+
+    // Regime.
+    int regime = ws->regime_force;
+    if (regime == AR_REGIME_AUTO)
+        regime = (T >= ws->stream_min_tokens && ws->stream_ok) ? AR_REGIME_STREAM : AR_REGIME_CLUSTER;
+    arf::ClusterPlan cplan{};
+    if (regime == AR_REGIME_CLUSTER) {
+        if (!arf::plan_cluster_rows(R, K, H, S != nullptr, ws->max_cluster, T, ws->num_sms, &cplan)) {
+            if (ws->regime_force == AR_REGIME_CLUSTER || !ws->stream_ok) return AR_ERR_UNSUPPORTED;
+            regime = AR_REGIME_STREAM;
+        }
+    }
+    if (regime == AR_REGIME_STREAM && !ws->stream_ok) return AR_ERR_UNSUPPORTED;
+
+    if (ws->flags & AR_WS_DRY_RUN) return AR_VALIDATED;
+
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return AR_ERR_CUDA;
+    if (cur != ws->device) return AR_ERR_INVALID_ARG;
+
+    arf::RowArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int r = 0; r < R; ++r) {
+        if (K > 0) a.E[r] = static_cast<const uint16_t*>(E[r]);
+        if (S) a.S[r] = static_cast<const uint16_t*>(S[r]);
+    }
+    a.perm = perm;
+    a.w = w;
+    a.residual = static_cast<const uint16_t*>(residual);
+    a.gamma = static_cast<const uint16_t*>(gamma);
+    a.out = out;
+    a.residual_out = residual_out;
+    a.err = ws->d_err;
+    a.T = T;
+    a.rows_e = K > 0 ? rows_e : 0;
+    a.R = R;
+    a.K = K;
+    a.H = H;
+    a.has_shared = S ? 1 : 0;
+    a.weight_bias = weight_bias;
+    a.eps = eps;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    int ctas;
+    if (regime == AR_REGIME_CLUSTER) {
+        e = arf::launch_cluster_rows(a, cplan, res_f32 != 0, s);
+        ctas = cplan.C;
+    } else {
+        const int64_t cap = (int64_t)ws->num_sms * ws->splan.ctas_per_sm;
+        const int grid = (int)(T < cap ? T : cap);
+        e = arf::launch_stream_rows(a, ws->splan, grid, res_f32 != 0, s);
+        ctas = grid;
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    ws->last_regime = regime;
+    ws->last_ctas = ctas;
+    return AR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int64_t max_tokens,
+                              float eps, unsigned flags, ar_workspace** out) {
+    if (!out) return AR_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (max_tokens < 1 || !(eps >= 0.0f) || eps > 3.0e38f) return AR_ERR_INVALID_ARG;
+    if ((flags & ~AR_WS_DRY_RUN) != 0) return AR_ERR_INVALID_ARG;
+    if (hidden < 8 || hidden % 8 != 0) return hidden < 8 ? AR_ERR_UNSUPPORTED : AR_ERR_ALIGNMENT;
+    if (ranks < 1 || ranks > AR_MAX_RANKS || top_k < 0 || top_k > AR_MAX_TOP_K ||
+        hidden > AR_MAX_HIDDEN || max_tokens > kMaxTokensLimit)
+        return AR_ERR_UNSUPPORTED;
+
+    ar_workspace* ws = new (std::nothrow) ar_workspace();
+    if (!ws) return AR_ERR_CUDA;
+    ws->device = device;
+    ws->R = ranks;
+    ws->K = top_k;
+    ws->H = hidden;
+    ws->max_tokens = max_tokens;
+    ws->eps = eps;
+    ws->flags = flags;
+    ws->d_err = nullptr;
+    ws->regime_force = AR_REGIME_AUTO;
+    ws->last_regime = 0;
+    ws->last_ctas = 0;
+
+    if (flags & AR_WS_DRY_RUN) {
+        ws->num_sms = kDryRunSms;
+        ws->smem_optin = kDryRunSmemOptin;
+        ws->max_cluster = 16;
+        ws->stream_ok = arf::plan_stream_rows(hidden, ws->smem_optin, &ws->splan);
+        ws->stream_min_tokens = default_stream_min_tokens(ranks, top_k, hidden, ws->num_sms);
+        *out = ws;
+        return AR_OK;
+    }
+
+    int prev = -1;
+    ar_status st = AR_OK;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess ||
+        cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+        st = AR_ERR_CUDA;
+        goto fail;
+    }
+    if (prop.major < 10) {
+        st = AR_ERR_UNSUPPORTED;
+        goto fail;
+    }
+    ws->num_sms = prop.multiProcessorCount;
+    ws->smem_optin = (int)prop.sharedMemPerBlockOptin;
+    ws->stream_ok = arf::plan_stream_rows(hidden, ws->smem_optin, &ws->splan);
+    if (ws->stream_ok && arf::stream_rows_set_attributes(ws->splan.smem) != cudaSuccess) {
+        st = AR_ERR_CUDA;
+        goto fail;
+    }
+    if (arf::cluster_rows_set_attributes() != cudaSuccess) {
+        st = AR_ERR_CUDA;
+        goto fail;
+    }
+    {
+        // Largest cluster the device co-schedules for this model's block shape.
+        arf::ClusterPlan p{};
+        ws->max_cluster = 16;
+        if (arf::plan_cluster_rows(ranks, top_k, hidden, true, 16, 1, ws->num_sms, &p))
+            ws->max_cluster = arf::cluster_rows_max_cluster(p.threads, p.smem, false);
+        if (ws->max_cluster < 1) ws->max_cluster = 1;
+    }
+    ws->stream_min_tokens = default_stream_min_tokens(ranks, top_k, hidden, ws->num_sms);
+    if (cudaMalloc(&ws->d_err, 256) != cudaSuccess || cudaMemset(ws->d_err, 0, 256) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        st = AR_ERR_CUDA;
+        goto fail;
+    }
+    (void)cudaSetDevice(prev);
+    *out = ws;
+    return AR_OK;
+
+fail:
+    (void)cudaGetLastError();
+    if (ws->d_err) (void)cudaFree(ws->d_err);
+    if (prev >= 0) (void)cudaSetDevice(prev);
+    delete ws;
+    return st;
+}
+
+ar_status ar_workspace_destroy(ar_workspace* ws) {
+    if (!ws) return AR_OK;
+    ar_status st = AR_OK;
+    if (ws->d_err) {
+        int prev = -1;
+        (void)cudaGetDevice(&prev);
+        if (cudaSetDevice(ws->device) != cudaSuccess || cudaFree(ws->d_err) != cudaSuccess)
+            st = AR_ERR_CUDA;
+        if (prev >= 0) (void)cudaSetDevice(prev);
+    }
+    delete ws;
+    return st;
+}
+
+ar_status ar_finalize_rmsnorm(ar_workspace* ws, const void* const* expert_out, int64_t rows_e,
+                              const int32_t* perm, const float* topk_w,
+                              const void* const* shared_out, const void* residual,
+                              const void* gamma, float weight_bias, float eps, int64_t T, int R,
+                              int K, int H, void* out, void* residual_out,
+                              int residual_out_is_fp32, void* stream) {
+    if (K < 0 || K > AR_MAX_TOP_K || R < 1 || R > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
+    return run(ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma, weight_bias, eps,
+               T, R, K, H, out, residual_out, residual_out_is_fp32, stream, true);
+}
+
+ar_status ar_rmsnorm(ar_workspace* ws, const void* const* partials, int R, const void* residual,
+                     const void* gamma, float weight_bias, float eps, int64_t T, int H, void* out,
+                     void* residual_out, int residual_out_is_fp32, void* stream) {
+    if (R < 1 || R > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
+    if (!partials) return AR_ERR_INVALID_ARG;
+    return run(ws, nullptr, 0, nullptr, nullptr, partials, residual, gamma, weight_bias, eps, T, R,
+               0, H, out, residual_out, residual_out_is_fp32, stream, false);
+}
+
+ar_status ar_workspace_device_error(ar_workspace* ws, int* code) {
+    if (!ws || !code) return AR_ERR_INVALID_ARG;
+    *code = 0;
+    if (ws->flags & AR_WS_DRY_RUN) return AR_OK;
+    int prev = -1;
+    (void)cudaGetDevice(&prev);
+    unsigned v = 0;
+    ar_status st = AR_OK;
+    if (cudaSetDevice(ws->device) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&v, ws->d_err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(ws->d_err, 0, sizeof v) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        (void)cudaGetLastError();
+        st = AR_ERR_CUDA;
+    }
+    if (prev >= 0) (void)cudaSetDevice(prev);
+    if (st != AR_OK) return st;
+    *code = (int)v;
+    return v ? AR_ERR_DEVICE_CHECK : AR_OK;
+}
+
+ar_status ar_workspace_set_regime(ar_workspace* ws, int regime) {
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (regime != AR_REGIME_AUTO && regime != AR_REGIME_CLUSTER && regime != AR_REGIME_STREAM)
+        return AR_ERR_INVALID_ARG;
+    ws->regime_force = regime;
+    return AR_OK;
+}
+
+int ar_workspace_last_regime(const ar_workspace* ws, int* cluster_ctas) {
+    if (!ws) return 0;
+    if (cluster_ctas) *cluster_ctas = ws->last_ctas;
+    return ws->last_regime;
+}
+
+const char* ar_status_string(ar_status s) {
+    switch (s) {
+        case AR_OK: return "ok";
+        case AR_ERR_INVALID_ARG: return "invalid argument";
+        case AR_ERR_ALIGNMENT: return "misaligned pointer or hidden size not a multiple of 8";
+        case AR_ERR_UNSUPPORTED: return "outside the limits of this build";
+        case AR_ERR_CAPACITY: return "more tokens than the workspace's max_tokens";
+        case AR_ERR_CUDA: return "CUDA runtime error";
+        case AR_ERR_DEVICE_CHECK: return "a device-side check fired";
+        case AR_VALIDATED: return "validated (dry-run workspace, nothing launched)";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,264 @@
+// arf_common.cuh -- shared device helpers of libarfuse (sm_103a only).
+//
+// The argument block every kernel receives, bf16 <-> fp32 helpers, and thin
+// inline-PTX wrappers for the Blackwell features the kernels use: mbarriers,
+// 1-D bulk async copies (cp.async.bulk, the TMA engine's untiled form),
+// thread-block-cluster barriers and distributed shared memory.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace arf {
+
+constexpr int kMaxRanks = 16;
+constexpr int kMaxTopK = 16;
+
+// Device error word bits (same values as AR_DEVERR_* in arfuse.h).
+constexpr unsigned kErrPermRange = 0x1u;
+constexpr unsigned kErrTimeout = 0x2u;
+
+// Time limit of every spin-wait on an mbarrier: past it the kernel records
+// kErrTimeout and stops waiting (it never hangs the GPU).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr unsigned kWaitMaxIters = 1u << 30;                // failsafe bound
+
+// Everything one launch needs.  Passed by value as a __grid_constant__ kernel
+// parameter: the pointer tables live in the parameter bank, no device table.
+struct RowArgs {
+    const uint16_t* E[kMaxRanks];  // bf16 [rows_e, H] per rank (K > 0)
+    const uint16_t* S[kMaxRanks];  // bf16 [T, H] per rank (has_shared)
+    const int32_t* perm;           // [T, K] gather rows into E
+    const float* w;                // [T, K] routing weights
+    const uint16_t* residual;      // bf16 [T, H]
+    const uint16_t* gamma;         // bf16 [H]
+    void* out;                     // bf16 [T, H]
+    void* residual_out;            // bf16 or fp32 [T, H]
+    unsigned* err;                 // device error word
+    int64_t T;
+    int64_t rows_e;
+    int R, K, H;
+    int has_shared;
+    float weight_bias;
+    float eps;
+};
+
+// ------------------------------------------------------------------ bf16 data
+// A bf16 value is the top half of an IEEE binary32 word, so widening is a
+// shift; eight of them travel as one 16-byte vector.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float f[8]) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(u[i] << 16);
+        f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16x8(const float f[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+
+// 16-byte streaming load of read-once data: non-coherent path, no L1 line.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_global16(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Store residual_out for 8 consecutive columns, bf16 (16 B) or fp32 (32 B).
+template <bool RES_F32>
+__device__ __forceinline__ void store_residual8(void* base, int64_t elem, const float h[8]) {
+    if (RES_F32) {
+        float* p = reinterpret_cast<float*>(base) + elem;
+        st_global16(p, make_uint4(__float_as_uint(h[0]), __float_as_uint(h[1]),
+                                  __float_as_uint(h[2]), __float_as_uint(h[3])));
+        st_global16(p + 4, make_uint4(__float_as_uint(h[4]), __float_as_uint(h[5]),
+                                      __float_as_uint(h[6]), __float_as_uint(h[7])));
+    } else {
+        st_global16(reinterpret_cast<uint16_t*>(base) + elem, f32x8_to_bf16x8(h));
+    }
+}
+
+// Routed row of slot (t, k), checked against rows_e.  An out-of-range value
+// is clamped into range (so no load ever leaves the buffer) and flagged.
+__device__ __forceinline__ int64_t checked_row(int32_t p, int64_t rows_e, unsigned* err) {
+    if ((uint64_t)(int64_t)p >= (uint64_t)rows_e) {
+        atomicOr(err, kErrPermRange);
+        return p < 0 ? 0 : rows_e - 1;
+    }
+    return p;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until the phase of `bar` with the given parity has completed.  Gives
+// up (returns false) when *abort becomes non-zero, after kWaitLimitNs, or
+// after kWaitMaxIters polls, whichever comes first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (unsigned it = 1; it < kWaitMaxIters; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0u) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+    return false;
+}
+
+// ------------------------------------------------------- bulk async copy (TMA)
+// L2 policy for data read exactly once: evict it first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global
+// memory into this CTA's shared memory; completion is signalled on `bar`
+// as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// ------------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Named barrier over a subset of the CTA's warps (id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------ host launchers
+struct ClusterPlan {
+    int C;    // CTAs per row (cluster size)
+    int nch;  // 16-byte column chunks per CTA
+    int G;    // thread groups splitting the term list
+    int threads;
+    int smem;  // dynamic shared memory bytes
+};
+
+// Kernel plan for the small-T regime; returns false if (R, K, H, shared) has
+// no launchable plan with a cluster of at most max_c CTAs.  T and the SM count
+// set how many CTAs per row are worth using.
+bool plan_cluster_rows(int R, int K, int H, bool shared, int max_c, int64_t T, int num_sms,
+                       ClusterPlan* p);
+int cluster_rows_max_cluster(int threads, int smem, bool res_f32);
+cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res_f32,
+                                cudaStream_t stream);
+cudaError_t cluster_rows_set_attributes();
+
+struct StreamPlan {
+    int cpt;       // 16-byte chunks per consumer thread
+    int threads;   // producer warp + consumer warps
+    int nstages;   // ring depth
+    int stage_bytes;
+    int smem;      // dynamic shared memory bytes
+    int ctas_per_sm;
+};
+
+bool plan_stream_rows(int H, int smem_optin, StreamPlan* p);
+cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, int grid, bool res_f32,
+                               cudaStream_t stream);
+cudaError_t stream_rows_set_attributes(int smem_bytes);
+
+}  // namespace arf

@@ -1,0 +1,246 @@
+// cluster_rows.cu -- small-T (decode) kernel: one thread-block cluster per
+// token row.
+//
+// At decode sizes (1..~128 tokens) one row carries ~1 MB of gathered expert
+// data (R*K rows of H bf16), so a row must be spread over many SMs to get
+// enough loads in flight.  The row's H columns are split over the C CTAs of
+// a cluster (C <= 16), and inside a CTA the R*(K+1) summands of each 16-byte
+// column chunk are split over G thread groups, each thread issuing all of
+// its (<= 8) 16-byte loads at once.  Group partials meet in shared memory,
+// the row's sum of squares meets across the cluster in distributed shared
+// memory, and every CTA normalises and stores its own columns.
+//
+// Operation: sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and
+// wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
+// 1-2 (finalize + shared add + all-reduce folded into the next input RMSNorm,
+// scale gamma + weight_bias); sglang PR #37104 "perf(mtp): fuse trailing TP
+// all-reduce with final RMSNorm", Changes (K = 0 form, residual required).
+#include "arf_common.cuh"
+
+namespace arf {
+
+constexpr int kClusterMaxTerms = 8;     // 16-byte loads in flight per thread
+constexpr int kClusterMaxThreads = 768;
+
+// Grid: T*C CTAs, clusters of C along x; CTA c of a cluster owns chunks
+// [c*nch, min((c+1)*nch, H/8)) of row t = blockIdx.x / C (the last CTA of a
+// row may be ragged).  blockDim.x = nch * G.  Term q of a thread group:
+// q < nS is shared partial S_q; otherwise e = q - nS selects slot k = e / R
+// of rank r = e % R.
+template <bool RES_F32>
+__global__ void __launch_bounds__(kClusterMaxThreads, 1)
+    cluster_rows_kernel(const __grid_constant__ RowArgs a, int C, int nch, int G) {
+    extern __shared__ __align__(16) uint8_t dyn_smem[];
+    float4* red = reinterpret_cast<float4*>(dyn_smem);  // [G-1][2][nch]
+    __shared__ int64_t s_row[kMaxTopK];
+    __shared__ float s_w[kMaxTopK];
+    __shared__ float s_warp[32];
+    __shared__ float s_part;   // this CTA's sum of squares, read by its peers
+    __shared__ float s_total;  // the row's sum of squares
+
+    const int tid = threadIdx.x;
+    const int64_t t = blockIdx.x / C;
+    const uint32_t c = (C > 1) ? cluster_ctarank() : 0u;
+    const int i = tid % nch;
+    const int g = tid / nch;
+    const int H = a.H;
+    const int chunk = (int)c * nch + i;
+    const bool active = chunk < H / 8;  // ragged last CTA of a row
+    const int64_t col = (int64_t)chunk * 8;
+    const int nS = a.has_shared ? a.R : 0;
+    const int NT = active ? nS + a.R * a.K : 0;
+    const int64_t rowoff = t * H + col;
+
+    for (int k = tid; k < a.K; k += blockDim.x) {
+        s_row[k] = checked_row(a.perm[t * a.K + k], a.rows_e, a.err);
+        s_w[k] = a.w[t * a.K + k];
+    }
+
+    // Pass 1: loads that do not depend on the routing metadata.
+    uint4 v[kClusterMaxTerms];
+    float coef[kClusterMaxTerms];
+#pragma unroll
+    for (int m = 0; m < kClusterMaxTerms; ++m) {
+        const int q = g + m * G;
+        if (q < nS && q < NT) {
+            v[m] = ld_stream16(a.S[q] + rowoff);
+            coef[m] = 1.0f;
+        }
+    }
+    uint4 res = make_uint4(0, 0, 0, 0);
+    if (g == 0 && active) res = ld_stream16(a.residual + rowoff);
+    __syncthreads();
+
+    // Pass 2: the routed (gathered) expert rows.
+#pragma unroll
+    for (int m = 0; m < kClusterMaxTerms; ++m) {
+        const int q = g + m * G;
+        if (q >= nS && q < NT) {
+            const int e = q - nS;
+            const int k = e / a.R;
+            const int r = e - k * a.R;
+            v[m] = ld_stream16(a.E[r] + s_row[k] * H + col);
+            coef[m] = s_w[k];
+        }
+    }
+
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+#pragma unroll
+    for (int m = 0; m < kClusterMaxTerms; ++m) {
+        if (g + m * G < NT) {
+            float f[8];
+            bf16x8_to_f32(v[m], f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(coef[m], f[j], acc[j]);
+        }
+    }
+
+    // Group partials meet in shared memory; group 0 finishes the columns.
+    if (g > 0) {
+        float4* dst = red + (size_t)(g - 1) * 2 * nch + i;
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[nch] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    __syncthreads();
+
+    float h[8];
+    float ss = 0.0f;
+    if (g == 0 && active) {
+        for (int gg = 1; gg < G; ++gg) {
+            const float4 x = red[(size_t)(gg - 1) * 2 * nch + i];
+            const float4 y = red[(size_t)(gg - 1) * 2 * nch + nch + i];
+            acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+            acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+        }
+        float rf[8];
+        bf16x8_to_f32(res, rf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            h[j] = acc[j] + rf[j];
+            ss = fmaf(h[j], h[j], ss);
+        }
+        store_residual8<RES_F32>(a.residual_out, rowoff, h);
+    }
+
+    // Row sum of squares: warps -> CTA -> cluster (fixed order everywhere,
+    // so every CTA of the row derives the same scale).
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) s_warp[tid >> 5] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float tot = 0.0f;
+        const int nw = (blockDim.x + 31) >> 5;
+        for (int w = 0; w < nw; ++w) tot += s_warp[w];
+        s_part = tot;
+        s_total = tot;
+    }
+    if (C > 1) {
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        if (tid == 0) {
+            const uint32_t mine = smem_addr(&s_part);
+            float tot = 0.0f;
+            for (int rk = 0; rk < C; ++rk) tot += ld_shared_cluster_f32(map_shared_rank(mine, rk));
+            s_total = tot;
+        }
+        __syncwarp();
+        cluster_arrive_release();  // this CTA is done reading its peers
+    }
+    __syncthreads();
+
+    if (g == 0 && active) {
+        const float inv = rsqrtf(s_total / (float)H + a.eps);
+        const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma + col);
+        float gf[8], o[8];
+        bf16x8_to_f32(gv, gf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = h[j] * inv * (gf[j] + a.weight_bias);
+        st_global16(reinterpret_cast<uint16_t*>(a.out) + rowoff, f32x8_to_bf16x8(o));
+    }
+    if (C > 1) cluster_wait_acquire();  // no CTA leaves while a peer may read it
+}
+
+static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+bool plan_cluster_rows(int R, int K, int H, bool shared, int max_c, int64_t T, int num_sms,
+                       ClusterPlan* p) {
+    const int chunks = H / 8;
+    const int NT = (shared ? R : 0) + R * K;
+    if (NT < 1 || chunks < 1) return false;
+    const int G = ceil_div(NT, kClusterMaxTerms);
+    if (G > kClusterMaxThreads) return false;
+    // Enough CTAs to cover the GPU about twice over.
+    int want = 1;
+    while (want < 16 && (int64_t)want * T < 2LL * num_sms) want <<= 1;
+    int best = 0, largest = 0;
+    for (int C = 1; C <= 16 && C <= max_c && C <= chunks; C <<= 1) {
+        const int nch = ceil_div(chunks, C);
+        if (nch * G > kClusterMaxThreads) continue;
+        largest = C;
+        if (!best && C >= want) best = C;
+    }
+    if (!best) best = largest;
+    if (!best) return false;
+    p->C = best;
+    p->nch = ceil_div(chunks, best);
+    p->G = G;
+    p->threads = p->nch * G;
+    p->smem = (G - 1) * 2 * p->nch * (int)sizeof(float4);
+    return true;
+}
+
+cudaError_t cluster_rows_set_attributes() {
+    cudaError_t e;
+    e = cudaFuncSetAttribute(cluster_rows_kernel<false>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(cluster_rows_kernel<true>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+static cudaLaunchConfig_t cluster_config(const ClusterPlan& p, int64_t T, cudaStream_t s,
+                                         cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(T * p.C), 1, 1);
+    cfg.blockDim = dim3((unsigned)p.threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)p.smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Largest cluster size (<= 16) the device can co-schedule for a block of
+// this shape, 0 if even a single CTA cannot run.
+int cluster_rows_max_cluster(int threads, int smem, bool res_f32) {
+    for (int C = 16; C >= 1; C >>= 1) {
+        cudaLaunchAttribute attr[1];
+        ClusterPlan p{C, 1, 1, threads, smem};
+        cudaLaunchConfig_t cfg = cluster_config(p, 1, nullptr, attr);
+        int n = 0;
+        cudaError_t e = res_f32
+                            ? cudaOccupancyMaxActiveClusters(&n, cluster_rows_kernel<true>, &cfg)
+                            : cudaOccupancyMaxActiveClusters(&n, cluster_rows_kernel<false>, &cfg);
+        if (e == cudaSuccess && n > 0) return C;
+        (void)cudaGetLastError();
+    }
+    return 0;
+}
+
+cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res_f32,
+                                cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster_config(p, a.T, stream, attr);
+    if (res_f32)
+        return cudaLaunchKernelEx(&cfg, cluster_rows_kernel<true>, a, p.C, p.nch, p.G);
+    return cudaLaunchKernelEx(&cfg, cluster_rows_kernel<false>, a, p.C, p.nch, p.G);
+}
+
+}  // namespace arf
