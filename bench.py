@@ -45,7 +45,15 @@ METRIC = "µs/call and achieved HBM GB/s (% of GB300 roofline) vs tokens T, 1 GP
 UNIT = "GB/s"
 HEADLINE = ("prefill", 8192)
 FALLBACK_HBM_GBS = 6800.0
-REGIMES = {"auto": 0, "cluster": 1, "stream": 2}
+REGIMES = {"auto": 0, "cluster": 1, "stream": 2, "oneshot": 3}
+REGIME_NAMES = {1: "cluster", 2: "stream", 3: "oneshot"}
+
+
+def parse_regime(tok: str):
+    """'auto' | 'cluster' | 'stream' | 'oneshot' | 'c<N>' (cluster regime, N CTAs per row)."""
+    if tok.startswith("c") and tok[1:].isdigit():
+        return REGIMES["cluster"], int(tok[1:])
+    return REGIMES[tok], 0
 CPU_SAMPLE_T = 512
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "stream_rows_prefill_traffic.json")
 
@@ -64,12 +72,19 @@ def parse():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=8)
-    p.add_argument("--regime", choices=["auto", "cluster", "stream"], default="auto",
-                   help="force a kernel regime for the timed call (tuning)")
+    p.add_argument("--regime", default="auto",
+                   help="force a kernel regime for the timed call: auto, cluster, stream, "
+                        "oneshot or c<N> (cluster regime with N CTAs per row)")
+    p.add_argument("--stage-bytes", type=int, default=0,
+                   help="target ring-slot bytes of the streaming kernels (0 = automatic)")
     p.add_argument("--sweep-regimes", default="auto",
-                   help="comma list of regimes timed in the sweep (auto,cluster,stream)")
+                   help="comma list of regimes timed in the sweep (same tokens as --regime)")
     p.add_argument("--sweep-only", default="",
                    help="comma list of workloads to sweep (default: all)")
+    p.add_argument("--sweep-mode", choices=["rotate", "scatter", "warm"], default="rotate",
+                   help="rotate: L2-cold, each call gathers within its own expert block; "
+                        "scatter: L2-cold, gathers spread over all sets' rows; "
+                        "warm: one input set replayed (L2-warm)")
     return p.parse_args()
 
 
@@ -290,7 +305,10 @@ def main_ours(args):
     # weak scaling: every rank draws and reduces its own T token rows
     d = make_inputs(cfg, T, seed=rank_seed(cfg.index, T, rank), device=dev)
     ws = arf.ar_workspace_create(R, K, H, T, cfg.eps, device=local)
-    arf.ar_workspace_set_regime(ws, REGIMES[args.regime])
+    force, csize = parse_regime(args.regime)
+    arf.ar_workspace_set_regime(ws, force)
+    arf.ar_workspace_set_cluster_size(ws, csize)
+    arf.ar_workspace_set_stage_bytes(ws, args.stage_bytes)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     r_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -351,7 +369,7 @@ def main_ours(args):
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "kernel": "stream_rows_kernel" if regime == arf.AR_REGIME_STREAM else "cluster_rows_kernel",
+                "kernel": "cluster_rows_kernel" if regime == arf.AR_REGIME_ONESHOT else "stream_rows_kernel",
                 "algorithmic_bytes_per_launch": bytes_step}
 
     # ---------------------------------------------- end to end (host buffers)
@@ -362,7 +380,7 @@ def main_ours(args):
     sweep = None
     if not args.no_sweep and rank == 0:
         sweep = run_sweep(arf, torch, dev, stream, peak, args.sweep_regimes.split(","),
-                          [w for w in args.sweep_only.split(",") if w])
+                          [w for w in args.sweep_only.split(",") if w], args.sweep_mode)
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
@@ -378,7 +396,7 @@ def main_ours(args):
                 "data": "synthetic",
                 "config": headline_config(args.workload, T, world),
                 "us_per_call": round(1e3 * ms_per_step, 3),
-                "regime": {1: "cluster", 2: "stream"}.get(regime, "?"), "ctas": ctas,
+                "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps, "clocks": clocks.summary(), "sweep": sweep}
         print(json.dumps(line), flush=True)
@@ -431,10 +449,11 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
             "steps": n, "api": "tp_reduce_moe_gb300.ar_finalize_rmsnorm"}
 
 
-def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=()):
+def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate"):
     """µs/call vs T for every workload: L2-cold by rotating through disjoint
-    input sets (>= 3x L2 in total), timed by replaying a CUDA graph of one call
-    per set."""
+    input sets (>= 3x L2 in total; each set gathers only within its own block
+    of expert rows, like successive layers), timed by replaying a CUDA graph
+    of one call per set."""
     from gen import CONFIGS, make_inputs, problem_bytes
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     res = []
@@ -447,18 +466,22 @@ def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=()):
                 continue
             for regime_name in regimes:
                 res.append(sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T,
-                                       REGIMES[regime_name]))
+                                       *parse_regime(regime_name), mode=mode))
     return res
 
 
-def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force):
+def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0, mode="rotate"):
     """One (workload, T, regime) point of the sweep."""
     from gen import make_inputs, problem_bytes
     b = problem_bytes(cfg.R, cfg.K, cfg.H, T)
     n_sets = int(min(8192, max(2, math.ceil(3 * l2 / b))))
-    big = make_inputs(cfg, T * n_sets, seed=11 + T, device=dev)
+    if mode == "warm":
+        n_sets = 1
+    big = make_inputs(cfg, T * n_sets, seed=11 + T, device=dev,
+                      perm_blocks=n_sets if mode == "rotate" else 1)
     ws = arf.ar_workspace_create(cfg.R, cfg.K, cfg.H, T, cfg.eps, device=dev.index)
     arf.ar_workspace_set_regime(ws, force)
+    arf.ar_workspace_set_cluster_size(ws, csize)
     outs = torch.empty((n_sets, T, cfg.H), dtype=torch.bfloat16, device=dev)
     routs = torch.empty((n_sets, T, cfg.H), dtype=torch.bfloat16, device=dev)
 
@@ -490,14 +513,16 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force):
     g.replay()
     torch.cuda.synchronize()
     per = []
+    reps = 200 if mode == "warm" else 1
     for _ in range(3):
         a = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        g.replay()
+        for _ in range(reps):
+            g.replay()
         e.record(stream)
         torch.cuda.synchronize()
-        per.append(a.elapsed_time(e) * 1e3 / n_sets)
+        per.append(a.elapsed_time(e) * 1e3 / (n_sets * reps))
     us = statistics.median(per)
     gbs = b / (us * 1e-6) / 1e9
     err = arf.ar_workspace_device_error(ws)
@@ -507,8 +532,8 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force):
     return {"workload": name, "R": cfg.R, "K": cfg.K, "H": cfg.H, "T": T,
             "us_per_call": round(us, 3), "GBps": round(gbs, 1),
             "frac_of_hbm_peak": round(gbs / peak, 4),
-            "regime": {1: "cluster", 2: "stream"}.get(regime, "?"), "ctas": ctas,
-            "forced": force != 0, "calls_per_graph": n_sets, "device_error": err}
+            "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas,
+            "forced": force != 0, "calls_per_graph": n_sets, "mode": mode, "device_error": err}
 
 
 def main():

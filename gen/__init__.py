@@ -126,12 +126,17 @@ def _routing(cfg: Config, T: int, g, device):
 
 
 def make_inputs(cfg, T: int, seed: int | None = None, device="cpu",
-                perm_kind: str = "random", shared: bool | None = None):
+                perm_kind: str = "random", shared: bool | None = None, perm_blocks: int = 1):
     """Draw one problem of config ``cfg`` (a Config or its name) with T tokens.
 
     Returns a dict: R, K, H, T, rows_e, eps, weight_bias, E (list of R bf16
     [T*K, H] or None), perm (int32 [T, K] or None), w (fp32 [T, K] or None),
     S (list of R bf16 [T, H] or None), residual (bf16 [T, H]), gamma (bf16 [H]).
+
+    perm_blocks = n > 1 (random perm only) draws the T rows as n equal blocks,
+    each gathering only from its own contiguous block of T*K/n expert rows --
+    n independent problems packed in one buffer, as n successive layers' expert
+    outputs would be.
     """
     if isinstance(cfg, str):
         cfg = CONFIGS[cfg]
@@ -150,7 +155,15 @@ def make_inputs(cfg, T: int, seed: int | None = None, device="cpu",
     perm = w = None
     if K > 0:
         w, ids = _routing(cfg, T, g, device)
-        if perm_kind == "random":
+        if perm_kind == "random" and perm_blocks > 1:
+            if T % perm_blocks:
+                raise ValueError("T must be a multiple of perm_blocks")
+            blk = rows_e // perm_blocks
+            keys = torch.rand((perm_blocks, blk), generator=g, device=device)
+            local = torch.argsort(keys, dim=1)
+            base = torch.arange(perm_blocks, device=device).view(-1, 1) * blk
+            perm = (local + base).to(torch.int32).view(T, K)
+        elif perm_kind == "random":
             perm = torch.randperm(rows_e, generator=g, device=device).to(torch.int32).view(T, K)
         elif perm_kind == "expert_sorted":
             # position of slot (t, k) after a stable sort of all slots by expert id

@@ -88,9 +88,13 @@ typedef enum ar_status {
 #define AR_DEVERR_TIMEOUT 0x2      /* a pipeline wait gave up after its time limit     */
 
 /* Kernel regimes (ar_workspace_set_regime / ar_workspace_last_regime). */
-#define AR_REGIME_AUTO 0     /* pick by (T, R, K, H) and the tuned crossover      */
-#define AR_REGIME_CLUSTER 1  /* small T: one thread-block cluster per token row   */
-#define AR_REGIME_STREAM 2   /* large T: persistent CTAs, bulk-copy ring per row  */
+#define AR_REGIME_AUTO 0     /* pick by (T, R, K, H) and the SM count                    */
+#define AR_REGIME_CLUSTER 1  /* small T: each row split into column tiles over a cluster  */
+                             /* of C CTAs, each streaming its tile through a bulk-copy    */
+                             /* ring; sum of squares exchanged in distributed smem        */
+#define AR_REGIME_STREAM 2   /* large T: persistent CTAs, whole rows through the ring     */
+#define AR_REGIME_ONESHOT 3  /* one cluster per row, every load in flight at once from    */
+                             /* registers, no pipeline (latency-optimal for tiny rows)    */
 
 typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
 
@@ -189,10 +193,28 @@ ARFUSE_API ar_status ar_workspace_device_error(ar_workspace* ws, int* code);
  */
 ARFUSE_API ar_status ar_workspace_set_regime(ar_workspace* ws, int regime);
 
-/* Regime (AR_REGIME_CLUSTER / AR_REGIME_STREAM) of the last launched call,
- * 0 before the first one.  *cluster_ctas receives the CTAs per row (cluster
- * regime) or the persistent grid size (stream regime); may be NULL. */
-ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* cluster_ctas);
+/*
+ * Force the number of CTAs per token row (the cluster size C, 2..16) that
+ * AR_REGIME_CLUSTER uses; 0 restores the automatic choice.  A size that
+ * cannot be launched for a call makes that call return AR_ERR_UNSUPPORTED.
+ */
+ARFUSE_API ar_status ar_workspace_set_cluster_size(ar_workspace* ws, int ctas_per_row);
+
+/*
+ * Set the target size in bytes of one ring slot of the streaming kernels (a
+ * slot holds as many whole row segments as fit, at least one, one bulk copy
+ * each, all signalled on one mbarrier); 0 restores the automatic size (32 KB
+ * for whole rows, 16 KB for column tiles).  Values outside 0 or
+ * [1024, 131072] are AR_ERR_INVALID_ARG.  A tuning control: results are
+ * identical for every value.
+ */
+ARFUSE_API ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes);
+
+/* Regime (AR_REGIME_CLUSTER / AR_REGIME_STREAM / AR_REGIME_ONESHOT) of the
+ * last launched call, 0 before the first one.  *ctas receives the CTAs per
+ * row (cluster and one-shot regimes) or the persistent grid size (stream
+ * regime); may be NULL. */
+ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
 
 /* Static description of a status code; never NULL. */
 ARFUSE_API const char* ar_status_string(ar_status s);

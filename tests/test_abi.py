@@ -231,12 +231,44 @@ def test_ar_rmsnorm_validation(lib):
 
 
 def test_regime_setter(lib, ws):
-    for r in (arf.AR_REGIME_AUTO, arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+    for r in (arf.AR_REGIME_AUTO, arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_ONESHOT):
         arf.ar_workspace_set_regime(ws, r)
         assert Fake().call(lib, ws) == arf.AR_VALIDATED
     with pytest.raises(arf.ArfuseError):
         arf.ar_workspace_set_regime(ws, 7)
     assert arf.ar_workspace_last_regime(ws) == (0, 0)     # nothing launched
+
+
+def test_cluster_size_setter(lib, ws):
+    arf.ar_workspace_set_regime(ws, arf.AR_REGIME_CLUSTER)
+    for c in (0, 2, 4, 8, 16):
+        arf.ar_workspace_set_cluster_size(ws, c)
+        assert Fake().call(lib, ws) == arf.AR_VALIDATED
+    for c in (1, -2, 17, 32):
+        with pytest.raises(arf.ArfuseError):
+            arf.ar_workspace_set_cluster_size(ws, c)
+
+
+def test_stage_bytes_setter(lib, ws):
+    for b in (0, 1024, 16384, 131072):
+        arf.ar_workspace_set_stage_bytes(ws, b)
+        assert Fake().call(lib, ws) == arf.AR_VALIDATED
+    for b in (-1, 1023, 131073):
+        with pytest.raises(arf.ArfuseError):
+            arf.ar_workspace_set_stage_bytes(ws, b)
+
+
+def test_cluster_regime_needs_two_chunks(lib):
+    """A row of one 16-byte chunk cannot be split over a cluster: a clean decline."""
+    w = arf.ar_workspace_create(1, 1, 8, 4, EPS, flags=arf.AR_WS_DRY_RUN)
+    try:
+        f = Fake()
+        arf.ar_workspace_set_regime(w, arf.AR_REGIME_CLUSTER)
+        assert f.call(lib, w, R=1, K=1, H=8, E=f.E[:1], S=f.S[:1]) == arf.AR_ERR_UNSUPPORTED
+        arf.ar_workspace_set_regime(w, arf.AR_REGIME_STREAM)
+        assert f.call(lib, w, R=1, K=1, H=8, E=f.E[:1], S=f.S[:1]) == arf.AR_VALIDATED
+    finally:
+        w.destroy()
 
 
 def test_dry_run_device_error_is_clear(lib, ws):

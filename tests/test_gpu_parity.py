@@ -19,7 +19,8 @@ from tests._util import check_bf16, check_f32, oracle_args, run_oracle
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-REGIMES = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_AUTO)
+REGIMES = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_ONESHOT, arf.AR_REGIME_AUTO)
+KERNELS = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_ONESHOT)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,6 +60,11 @@ def run_gpu(ws, d, fp32=False, regime=arf.AR_REGIME_AUTO, **kw):
 def check_all(ws, d, ref, what, regimes=REGIMES, fp32s=(False, True)):
     for regime in regimes:
         for fp32 in fp32s:
+            if regime == arf.AR_REGIME_CLUSTER and d["H"] // 8 < 2:
+                with pytest.raises(arf.ArfuseError) as e:   # one chunk cannot be split
+                    run_gpu(ws, d, fp32=fp32, regime=regime)
+                assert e.value.status == arf.AR_ERR_UNSUPPORTED
+                continue
             out, r_out = run_gpu(ws, d, fp32=fp32, regime=regime)
             torch.cuda.synchronize()
             tag = f"{what} regime={regime} fp32={fp32}"
@@ -148,7 +154,7 @@ def test_perm_decode_bit_exact(R, K, H, T):
             want = d["perm"][torch.arange(T, device=DEV), d["hot"]].long()
             cols = torch.arange(H, device=DEV)
             expect = (want.view(-1, 1) >> (4 * (cols % D)).view(1, -1)) & 15
-            for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+            for regime in KERNELS:
                 for fp32 in (False, True):
                     _, r_out = run_gpu(ws, d, fp32=fp32, regime=regime)
                     torch.cuda.synchronize()
@@ -233,7 +239,7 @@ def test_in_place_residual():
     ref = run_oracle(inp, want_abs=True)
     ws = make_ws(inp)
     try:
-        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+        for regime in KERNELS:
             d = to_dev(inp)
             out, r_out = run_gpu(ws, d, regime=regime, residual_out=d["residual"])
             torch.cuda.synchronize()
@@ -270,7 +276,7 @@ def test_perm_out_of_range_sets_error_and_never_faults():
     bad[3, 0] = -7
     ws = make_ws(inp)
     try:
-        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+        for regime in KERNELS:
             d = to_dev(dict(inp, perm=bad))
             out, _ = run_gpu(ws, d, regime=regime)
             code = arf.ar_workspace_device_error(ws)
@@ -289,7 +295,7 @@ def test_outputs_stay_in_bounds():
     ws = make_ws(inp)
     T, H = inp["T"], inp["H"]
     try:
-        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+        for regime in KERNELS:
             for fp32 in (False, True):
                 pad = 4096
                 dt = torch.float32 if fp32 else torch.bfloat16
@@ -309,7 +315,7 @@ def test_cuda_graph_replay_with_changing_inputs():
     """Capture once, then replay after overwriting the inputs in place."""
     ws = arf.ar_workspace_create(8, 8, 7168, 16, 1e-6, device=0)
     try:
-        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM):
+        for regime in KERNELS:
             d = to_dev(make_inputs("dsv3_decode", 16, seed=1))
             out = torch.empty(16, 7168, dtype=torch.bfloat16, device=DEV)
             r_out = torch.empty(16, 7168, dtype=torch.bfloat16, device=DEV)
@@ -349,7 +355,7 @@ def test_side_stream_and_back_to_back_calls():
         s = torch.cuda.Stream()
         outs = []
         with torch.cuda.stream(s):
-            for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM) * 3:
+            for regime in KERNELS * 3:
                 outs.append(run_gpu(ws, d, regime=regime, stream=s)[0])
         s.synchronize()
         for o in outs:
@@ -365,5 +371,27 @@ def test_wrong_device_or_mismatch_is_a_clean_decline():
         with pytest.raises(arf.ArfuseError) as e:
             run_gpu(ws, to_dev(inp))          # T=4 > max_tokens=2
         assert e.value.status == arf.AR_ERR_CAPACITY
+    finally:
+        ws.destroy()
+
+
+# ------------------------------------------- every cluster size of the cluster regime
+@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 4), ("glm_gemma", 16), ("prefill", 3), ("ar_only", 37)])
+def test_every_cluster_size(cfg, T):
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        for c in (2, 4, 8, 16):
+            arf.ar_workspace_set_cluster_size(ws, c)
+            for fp32 in (False, True):
+                out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_CLUSTER)
+                torch.cuda.synchronize()
+                assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_CLUSTER, c)
+                check_bf16(out, ref["out"], f"{cfg} T={T} C={c} out")
+                if fp32:
+                    check_f32(r_out, ref["h"], ref["abs"], f"{cfg} T={T} C={c} residual_out")
+        assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()

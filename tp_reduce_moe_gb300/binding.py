@@ -33,6 +33,7 @@ AR_DEVERR_TIMEOUT = 0x2
 AR_REGIME_AUTO = 0
 AR_REGIME_CLUSTER = 1
 AR_REGIME_STREAM = 2
+AR_REGIME_ONESHOT = 3
 
 AR_MAX_RANKS = 16
 AR_MAX_TOP_K = 16
@@ -76,6 +77,10 @@ def load_library(path: str | None = None):
         lib.ar_workspace_device_error.argtypes = [P, ctypes.POINTER(I)]
         lib.ar_workspace_set_regime.restype = I
         lib.ar_workspace_set_regime.argtypes = [P, I]
+        lib.ar_workspace_set_stage_bytes.restype = I
+        lib.ar_workspace_set_stage_bytes.argtypes = [P, I]
+        lib.ar_workspace_set_cluster_size.restype = I
+        lib.ar_workspace_set_cluster_size.argtypes = [P, I]
         lib.ar_workspace_last_regime.restype = I
         lib.ar_workspace_last_regime.argtypes = [P, ctypes.POINTER(I)]
         lib.ar_status_string.restype = ctypes.c_char_p
@@ -137,6 +142,19 @@ def ar_workspace_destroy(ws: Workspace) -> None:
 def ar_workspace_set_regime(ws: Workspace, regime: int) -> None:
     _check(load_library().ar_workspace_set_regime(ctypes.c_void_p(ws.handle), int(regime)),
            "ar_workspace_set_regime")
+
+
+def ar_workspace_set_cluster_size(ws: Workspace, ctas_per_row: int) -> None:
+    """Force the CTAs per row of the cluster regime (2..16); 0 = automatic."""
+    _check(load_library().ar_workspace_set_cluster_size(ctypes.c_void_p(ws.handle),
+                                                        int(ctas_per_row)),
+           "ar_workspace_set_cluster_size")
+
+
+def ar_workspace_set_stage_bytes(ws: Workspace, nbytes: int) -> None:
+    """Target ring-slot size of the streaming kernels (tuning); 0 = automatic."""
+    _check(load_library().ar_workspace_set_stage_bytes(ctypes.c_void_p(ws.handle), int(nbytes)),
+           "ar_workspace_set_stage_bytes")
 
 
 def ar_workspace_last_regime(ws: Workspace):

@@ -26,12 +26,12 @@ struct ar_workspace {
     int num_sms;
     int smem_optin;
     int max_cluster;  // largest co-schedulable cluster for the cluster kernel
+    int max_cluster_stream;  // largest cluster for the clustered streaming kernel
     int regime_force;
+    int force_ctas_per_row;  // 0: automatic
+    int stage_bytes;         // 0: automatic
     int last_regime;
     int last_ctas;
-    bool stream_ok;
-    arf::StreamPlan splan;
-    int64_t stream_min_tokens;  // crossover: T >= this runs the stream kernel
 };
 
 namespace {
@@ -52,14 +52,6 @@ Range range_of(const void* p, int64_t bytes) {
 }
 
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
-
-// Crossover between the cluster (small T) and stream (large T) kernels.
-int64_t default_stream_min_tokens(int R, int K, int H, int num_sms) {
-    (void)R;
-    (void)K;
-    (void)H;
-    return 2LL * num_sms;
-}
 
 ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int32_t* perm,
               const float* w, const void* const* S, const void* residual, const void* gamma,
@@ -121,18 +113,40 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     if (overlap(r_out, r_res)) return AR_ERR_INVALID_ARG;
     if (!inplace && overlap(r_rout, r_res)) return AR_ERR_INVALID_ARG;
 
-    // Regime.
+    // Regime and launch plan.
+    const bool shared = S != nullptr;
     int regime = ws->regime_force;
-    if (regime == AR_REGIME_AUTO)
-        regime = (T >= ws->stream_min_tokens && ws->stream_ok) ? AR_REGIME_STREAM : AR_REGIME_CLUSTER;
     arf::ClusterPlan cplan{};
-    if (regime == AR_REGIME_CLUSTER) {
-        if (!arf::plan_cluster_rows(R, K, H, S != nullptr, ws->max_cluster, T, ws->num_sms, &cplan)) {
-            if (ws->regime_force == AR_REGIME_CLUSTER || !ws->stream_ok) return AR_ERR_UNSUPPORTED;
-            regime = AR_REGIME_STREAM;
-        }
+    arf::StreamPlan splan{};
+    if (regime == AR_REGIME_AUTO) {
+        // Light rows (at most 8 summands per 16-byte chunk, so one load wave
+        // per thread) below one row per SM: the one-shot kernel was fastest.
+        const int summands = (shared ? R : 0) + R * K;
+        if (summands <= 8 && T < ws->num_sms &&
+            arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &cplan))
+            regime = AR_REGIME_ONESHOT;
     }
-    if (regime == AR_REGIME_STREAM && !ws->stream_ok) return AR_ERR_UNSUPPORTED;
+    if (regime == AR_REGIME_ONESHOT) {
+        if (!cplan.C && !arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &cplan))
+            return AR_ERR_UNSUPPORTED;
+    } else {
+        int C = 0;  // automatic
+        if (regime == AR_REGIME_STREAM) C = 1;
+        if (regime == AR_REGIME_CLUSTER) {
+            C = ws->force_ctas_per_row;
+            if (C == 0) {
+                arf::StreamPlan probe{};
+                if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                           ws->max_cluster_stream, 0, ws->stage_bytes, &probe))
+                    return AR_ERR_UNSUPPORTED;
+                C = probe.geo.C > 1 ? probe.geo.C : 2;
+            }
+        }
+        if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                   ws->max_cluster_stream, C, ws->stage_bytes, &splan))
+            return AR_ERR_UNSUPPORTED;
+        regime = splan.geo.C > 1 ? AR_REGIME_CLUSTER : AR_REGIME_STREAM;
+    }
 
     if (ws->flags & AR_WS_DRY_RUN) return AR_VALIDATED;
 
@@ -165,14 +179,12 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     int ctas;
-    if (regime == AR_REGIME_CLUSTER) {
+    if (regime == AR_REGIME_ONESHOT) {
         e = arf::launch_cluster_rows(a, cplan, res_f32 != 0, s);
         ctas = cplan.C;
     } else {
-        const int64_t cap = (int64_t)ws->num_sms * ws->splan.ctas_per_sm;
-        const int grid = (int)(T < cap ? T : cap);
-        e = arf::launch_stream_rows(a, ws->splan, grid, res_f32 != 0, s);
-        ctas = grid;
+        e = arf::launch_stream_rows(a, splan, res_f32 != 0, s);
+        ctas = regime == AR_REGIME_CLUSTER ? splan.geo.C : splan.grid;
     }
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
@@ -209,6 +221,8 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
     ws->flags = flags;
     ws->d_err = nullptr;
     ws->regime_force = AR_REGIME_AUTO;
+    ws->force_ctas_per_row = 0;
+    ws->stage_bytes = 0;
     ws->last_regime = 0;
     ws->last_ctas = 0;
 
@@ -216,8 +230,7 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
         ws->num_sms = kDryRunSms;
         ws->smem_optin = kDryRunSmemOptin;
         ws->max_cluster = 16;
-        ws->stream_ok = arf::plan_stream_rows(hidden, ws->smem_optin, &ws->splan);
-        ws->stream_min_tokens = default_stream_min_tokens(ranks, top_k, hidden, ws->num_sms);
+        ws->max_cluster_stream = 16;
         *out = ws;
         return AR_OK;
     }
@@ -236,8 +249,7 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
     }
     ws->num_sms = prop.multiProcessorCount;
     ws->smem_optin = (int)prop.sharedMemPerBlockOptin;
-    ws->stream_ok = arf::plan_stream_rows(hidden, ws->smem_optin, &ws->splan);
-    if (ws->stream_ok && arf::stream_rows_set_attributes(ws->splan.smem) != cudaSuccess) {
+    if (arf::stream_rows_set_attributes(ws->smem_optin) != cudaSuccess) {
         st = AR_ERR_CUDA;
         goto fail;
     }
@@ -252,8 +264,13 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
         if (arf::plan_cluster_rows(ranks, top_k, hidden, true, 16, 1, ws->num_sms, &p))
             ws->max_cluster = arf::cluster_rows_max_cluster(p.threads, p.smem, false);
         if (ws->max_cluster < 1) ws->max_cluster = 1;
+        // ... and for the clustered streaming kernel (16 tiles of one row).
+        arf::StreamPlan sp{};
+        ws->max_cluster_stream = 1;
+        for (int c = 16; c >= 2 && ws->max_cluster_stream == 1; c >>= 1)
+            if (arf::plan_stream_rows(ranks, top_k, hidden, true, 1, ws->num_sms, ws->smem_optin, 16, c, 0, &sp))
+                ws->max_cluster_stream = arf::stream_rows_max_cluster(sp.threads, sp.smem, sp.cpt);
     }
-    ws->stream_min_tokens = default_stream_min_tokens(ranks, top_k, hidden, ws->num_sms);
     if (cudaMalloc(&ws->d_err, 256) != cudaSuccess || cudaMemset(ws->d_err, 0, 256) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         st = AR_ERR_CUDA;
@@ -327,15 +344,30 @@ ar_status ar_workspace_device_error(ar_workspace* ws, int* code) {
 
 ar_status ar_workspace_set_regime(ar_workspace* ws, int regime) {
     if (!ws) return AR_ERR_INVALID_ARG;
-    if (regime != AR_REGIME_AUTO && regime != AR_REGIME_CLUSTER && regime != AR_REGIME_STREAM)
+    if (regime != AR_REGIME_AUTO && regime != AR_REGIME_CLUSTER && regime != AR_REGIME_STREAM &&
+        regime != AR_REGIME_ONESHOT)
         return AR_ERR_INVALID_ARG;
     ws->regime_force = regime;
     return AR_OK;
 }
 
-int ar_workspace_last_regime(const ar_workspace* ws, int* cluster_ctas) {
+ar_status ar_workspace_set_cluster_size(ar_workspace* ws, int ctas_per_row) {
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (ctas_per_row != 0 && (ctas_per_row < 2 || ctas_per_row > 16)) return AR_ERR_INVALID_ARG;
+    ws->force_ctas_per_row = ctas_per_row;
+    return AR_OK;
+}
+
+ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes) {
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (bytes != 0 && (bytes < 1024 || bytes > 131072)) return AR_ERR_INVALID_ARG;
+    ws->stage_bytes = bytes;
+    return AR_OK;
+}
+
+int ar_workspace_last_regime(const ar_workspace* ws, int* ctas) {
     if (!ws) return 0;
-    if (cluster_ctas) *cluster_ctas = ws->last_ctas;
+    if (ctas) *ctas = ws->last_ctas;
     return ws->last_regime;
 }
 

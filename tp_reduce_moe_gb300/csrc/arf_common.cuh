@@ -158,18 +158,37 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
     return t;
 }
 
+// try_wait with acquire at cluster scope: for barriers that peers in the
+// cluster arrive on remotely (their prior stores become visible).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase of `bar` with the given parity has completed.  Gives
-// up (returns false) when *abort becomes non-zero, after kWaitLimitNs, or
-// after kWaitMaxIters polls, whichever comes first.
+// up (returns false) when *abort becomes non-zero, after limit_ns, or after
+// kWaitMaxIters polls, whichever comes first.
+template <bool CLUSTER_ACQUIRE = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  const volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                                  const volatile int* abort,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
+    auto poll = [&]() {
+        return CLUSTER_ACQUIRE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
     const unsigned long long t0 = global_timer_ns();
     for (unsigned it = 1; it < kWaitMaxIters; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((it & 31u) == 0u) {
             if (abort != nullptr && *abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
         }
     }
     return false;
@@ -217,6 +236,18 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
     return r;
 }
 
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Arrive on an mbarrier of a peer CTA (address from map_shared_rank); the
+// release orders this thread's earlier stores (e.g. st_shared_cluster_f32)
+// before the arrival.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -247,18 +278,37 @@ cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res
                                 cudaStream_t stream);
 cudaError_t cluster_rows_set_attributes();
 
-struct StreamPlan {
-    int cpt;       // 16-byte chunks per consumer thread
-    int threads;   // producer warp + consumer warps
-    int nstages;   // ring depth
-    int stage_bytes;
-    int smem;      // dynamic shared memory bytes
-    int ctas_per_sm;
+// Each ring slot starts with a header holding the coefficient of each of its
+// segments (1 for shared partials and the residual, w[t,k] for routed rows).
+constexpr int kSlotHeader = 128;
+
+// Geometry of one stream_rows launch (kernel parameter).
+struct StreamGeom {
+    int nstages;      // ring slots
+    int slot_bytes;   // bytes per slot: kSlotHeader + seg_per_stage * seg_stride
+    int seg_per_stage;  // segments (one bulk copy each) sharing one slot and one mbarrier
+    int seg_stride;   // bytes between the segments of a slot (>= tile bytes, multiple of 128)
+    int C;            // CTAs per token row (cluster size); 1 = whole rows per CTA
+    int tile_chunks;  // 16-byte column chunks per CTA tile (the row's last tile may be shorter)
 };
 
-bool plan_stream_rows(int H, int smem_optin, StreamPlan* p);
-cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, int grid, bool res_f32,
+struct StreamPlan {
+    StreamGeom geo;
+    int cpt;          // 16-byte chunks per consumer thread
+    int threads;      // producer warp + consumer warps
+    int smem;         // dynamic shared memory bytes
+    int grid;         // CTAs (a multiple of C)
+};
+
+// Plan a stream_rows launch for T rows.  C = 0 picks the CTAs per row from T
+// and the SM count; C >= 1 forces it.  stage_bytes = 0 picks the slot size,
+// otherwise it is the target.  Returns false if no plan fits.
+bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
+                      int max_cluster, int C, int stage_bytes, StreamPlan* p);
+cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, bool res_f32,
                                cudaStream_t stream);
-cudaError_t stream_rows_set_attributes(int smem_bytes);
+cudaError_t stream_rows_set_attributes(int smem_optin);
+// Largest cluster (<= 16) co-schedulable for a clustered plan of this shape.
+int stream_rows_max_cluster(int threads, int smem, int cpt);
 
 }  // namespace arf

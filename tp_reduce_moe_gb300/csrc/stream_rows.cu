@@ -1,195 +1,337 @@
-// stream_rows.cu -- large-T (prefill) kernel: persistent CTAs that each own
-// whole token rows and stream them through a shared-memory ring.
+// stream_rows.cu -- the streaming kernel family of libarfuse.
 //
-// Per token row the op reads R*(K+1)+1 contiguous rows of H bf16 (R shared
-// partials, the residual, R*K gathered expert rows) and writes two.  With
-// thousands of rows the work is a pure HBM stream, so each SM runs one CTA
-// whose producer thread keeps a deep ring of whole-row bulk async copies
-// (cp.async.bulk: the TMA engine, completion counted on an mbarrier) in
-// flight, while consumer warps fold each landed row into fp32 accumulators
-// held in registers (CPT 16-byte column chunks per thread).  After a row's
-// last summand the consumers finish it entirely on chip: residual_out, the
-// sum of squares (warp shuffle + one named barrier), the scale and the
-// bf16 out -- so every input byte is read once and every output byte
-// written once, and the next row's copies are already in flight.
+// Per token row the op reads nseg = R*(K+1)+1 contiguous rows of H bf16 (R
+// shared partials, the residual, R*K gathered expert rows) and writes two.
+// Each CTA owns a column tile of every row it processes -- the whole row
+// (C = 1, large T) or one of C tiles of the row, the C CTAs forming one
+// thread-block cluster (C = 2..16, small T) -- and streams its tile of the
+// row's nseg segments through a ring of shared-memory slots:
 //
-// Every wait is bounded (arf::mbar_wait_bounded); a wait that runs out sets
-// the workspace error word, the CTA stops issuing, drains its own copies and
-// returns.
+//   * a producer warp issues one 1-D bulk async copy per segment
+//     (cp.async.bulk, the TMA engine's untiled form, L2 evict-first),
+//     completion counted as transaction bytes on the slot's `full` mbarrier;
+//     whole rows use one issuing lane, tiles use all 32 lanes so that the
+//     many small copies of a tile go out at once;
+//   * consumer warps fold each landed slot into fp32 accumulators held in
+//     registers (CPT 16-byte chunks per thread, U slots per step so several
+//     shared-memory loads are in flight), then release it on the slot's
+//     `empty` mbarrier;
+//   * after a row's last segment the consumers finish the row on chip: store
+//     residual_out, reduce the sum of squares (warp shuffle + one named
+//     barrier), and -- for tiles -- push the CTA's partial into every peer's
+//     shared memory with a remote mbarrier arrive (distributed shared
+//     memory), then scale by rsqrt(mean + eps) * (gamma + weight_bias) and
+//     store out.  The ring keeps streaming the next row meanwhile.
+//
+// Every input byte is read once and every output byte written once.  Rows
+// go round-robin over persistent CTAs (C = 1) or clusters (C > 1).
+//
+// Every wait is bounded (arf::mbar_wait_bounded): a wait that runs out sets
+// the workspace error word and an abort flag, later waits are skipped (rows
+// are left unfinished, never hung), and the producer waits (bounded again)
+// for its own copies in flight before the CTA exits.  A clustered CTA ends
+// with a cluster barrier so that no CTA leaves while a peer may still write
+// into its shared memory.
 //
 // Operation: sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and
 // wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
 // 1-2; sglang PR #37104 "perf(mtp): fuse trailing TP all-reduce with final
 // RMSNorm", Changes.
+#include <type_traits>
+
 #include "arf_common.cuh"
 
 namespace arf {
 
 constexpr int kStreamMaxConsumers = 512;
 constexpr int kStreamMaxThreads = 32 + kStreamMaxConsumers;
-constexpr int kStreamMaxStages = 32;
+constexpr int kStreamMaxStages = 128;
+constexpr int kMaxCluster = 16;
 
-// Shared-memory header: full[nstages], empty[nstages] mbarriers, the per-row
-// sum-of-squares partials [2][32] and the abort flag; the ring follows at a
-// 128-byte boundary.
+// Shared-memory header: full[n], empty[n], xbar[2] mbarriers; xslot[2][16]
+// (pushed partial sums of squares), red[2][32] (per-warp partials), the abort
+// flag, rec[n] (0: slot never filled, 1 + parity of its latest fill); the
+// ring follows at a 128-byte boundary.
 __host__ __device__ constexpr int stream_ring_offset(int nstages) {
-    return ((nstages * 16 + 2 * 32 * 4 + 16) + 127) / 128 * 128;
+    return (nstages * 16 + 16 + 2 * kMaxCluster * 4 + 2 * 32 * 4 + 16 + nstages + 127) / 128 * 128;
 }
 
-template <int CPT, bool RES_F32>
+// Slot and parity of ring position q (0 <= q < 2 * nstages).
+__device__ __forceinline__ void ring_pos(int q, int nst, int& slot, uint32_t& parity) {
+    parity = q >= nst ? 1u : 0u;
+    slot = parity ? q - nst : q;
+}
+
+// Stages of one row: first the nsr = nS + 1 segments that need no routing
+// metadata (shared partials, residual) in stages of at most P, then the R*K
+// routed segments in stages of at most P.  Stage j covers segments
+// [s0, s0 + cnt).
+__device__ __forceinline__ void stage_range(int j, int P, int nsr, int nseg, int& s0, int& cnt) {
+    const int first = (nsr + P - 1) / P;
+    if (j < first) {
+        s0 = j * P;
+        cnt = min(P, nsr - s0);
+    } else {
+        s0 = nsr + (j - first) * P;
+        cnt = min(P, nseg - s0);
+    }
+}
+
+template <int CPT, int U, bool RES_F32, bool CLUSTERED>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1)
-    stream_rows_kernel(const __grid_constant__ RowArgs a, int nstages, int stage_bytes) {
+    stream_rows_kernel(const __grid_constant__ RowArgs a, const StreamGeom geo) {
     extern __shared__ __align__(128) uint8_t smem[];
+    const int nst = geo.nstages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + nstages;
-    float* red = reinterpret_cast<float*>(empty + nstages);        // [2][32]
+    uint64_t* empty = full + nst;
+    uint64_t* xbar = empty + nst;                                 // [2]
+    float* xslot = reinterpret_cast<float*>(xbar + 2);            // [2][kMaxCluster]
+    float* red = xslot + 2 * kMaxCluster;                         // [2][32]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 64);
-    uint8_t* ring = smem + stream_ring_offset(nstages);
+    uint8_t* rec = reinterpret_cast<uint8_t*>(red + 68);          // [nst]
+    uint8_t* ring = smem + stream_ring_offset(nst);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int ncw = (blockDim.x >> 5) - 1;  // consumer warps
+    const int C = CLUSTERED ? geo.C : 1;
+    const uint32_t crank = CLUSTERED ? cluster_ctarank() : 0u;
+    const int64_t first_row = blockIdx.x / C;
+    const int64_t row_step = gridDim.x / C;
+    const int H = a.H;
+    const int chunk0 = (int)crank * geo.tile_chunks;  // first 16-byte chunk of this tile
+    const int nchunk = min(geo.tile_chunks, H / 8 - chunk0);
+    const uint32_t tile_bytes = (uint32_t)nchunk * 16u;
+    const int nS = a.has_shared ? a.R : 0;
+    const int nseg = nS + 1 + a.R * a.K;
+    const int P = geo.seg_per_stage;
+    const int nstage_row = (nS + 1 + P - 1) / P + (a.R * a.K + P - 1) / P;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < nstages; ++s) {
+        for (int s = 0; s < nst; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), (uint32_t)ncw);
+            rec[s] = 0;
         }
+        mbar_init(smem_addr(&xbar[0]), (uint32_t)C);
+        mbar_init(smem_addr(&xbar[1]), (uint32_t)C);
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-
-    const int H = a.H;
-    const int nS = a.has_shared ? a.R : 0;
-    const uint32_t row_bytes = (uint32_t)H * 2u;
+    if (CLUSTERED) {  // every peer's barriers exist before anyone pushes
+        cluster_arrive_release();
+        cluster_wait_acquire();
+    }
 
     if (warp == 0) {
-        // ------------------------------------------------------- producer
-        if (lane != 0) return;
+        // ------------------------------------------------------------ producer
+        // One slot = up to P consecutive segments of one row, one bulk copy
+        // each, issued by lanes 0..cnt-1 and all counted on the slot's single
+        // `full` mbarrier (lane 0 arms it with the slot's total bytes).
         const uint64_t pol = l2_evict_first_policy();
-        int stage = 0;
+        const int64_t col = (int64_t)chunk0 * 8;
+        int slot = 0;
         uint32_t phase = 0;
-        uint32_t issued = 0, last_par = 0;  // per-stage bits, for the drain
         bool ok = true;
-        auto issue = [&](const void* src) -> bool {
-            if (!mbar_wait_bounded(smem_addr(&empty[stage]), phase ^ 1u, abort_flag)) {
-                if (!*abort_flag) atomicOr(a.err, kErrTimeout);
-                *abort_flag = 1;
-                return false;
-            }
-            const uint32_t fb = smem_addr(&full[stage]);
-            mbar_arrive_expect_tx(fb, row_bytes);
-            bulk_g2s(smem_addr(ring + (size_t)stage * stage_bytes), src, row_bytes, fb, pol);
-            issued |= 1u << stage;
-            last_par = (last_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == nstages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            return true;
-        };
-        for (int64_t t = blockIdx.x; t < a.T && ok; t += gridDim.x) {
-            int32_t prow[kMaxTopK];
-#pragma unroll
-            for (int k = 0; k < kMaxTopK; ++k)
-                if (k < a.K) prow[k] = __ldg(a.perm + t * a.K + k);
-            for (int r = 0; r < nS && ok; ++r) ok = issue(a.S[r] + t * H);
-            if (ok) ok = issue(a.residual + t * H);
-#pragma unroll
-            for (int k = 0; k < kMaxTopK; ++k) {
-                if (k < a.K && ok) {
-                    const int64_t row = checked_row(prow[k], a.rows_e, a.err);
-                    for (int r = 0; r < a.R && ok; ++r) ok = issue(a.E[r] + row * H);
+        // Routing metadata one row ahead: lane k holds perm[t, k] of the row
+        // being issued and has the next row's value in flight.
+        int32_t raw_next = 0;
+        float w_next = 0.0f;
+        if (lane < a.K && first_row < a.T) {
+            raw_next = __ldg(a.perm + first_row * a.K + lane);
+            w_next = __ldg(a.w + first_row * a.K + lane);
+        }
+        for (int64_t t = first_row; t < a.T && ok; t += row_step) {
+            const int32_t raw = raw_next;
+            const float my_w = w_next;
+            int64_t my_row = -1;  // checked lazily, at the first routed stage
+            for (int j = 0; j < nstage_row && ok; ++j) {
+                int s0, cnt;
+                stage_range(j, P, nS + 1, nseg, s0, cnt);
+                const int s = s0 + lane;
+                const int e = s - nS - 1;
+                int64_t row_k = 0;
+                float w_k = 1.0f;
+                if (s0 > nS) {  // routed stage
+                    if (my_row < 0) {
+                        my_row = lane < a.K ? checked_row(raw, a.rows_e, a.err) : 0;
+                        if (lane < a.K && t + row_step < a.T) {
+                            raw_next = __ldg(a.perm + (t + row_step) * a.K + lane);
+                            w_next = __ldg(a.w + (t + row_step) * a.K + lane);
+                        }
+                    }
+                    const int k = (lane < cnt) ? e / a.R : 0;
+                    row_k = __shfl_sync(0xffffffffu, my_row, k);
+                    w_k = __shfl_sync(0xffffffffu, my_w, k);
+                }
+                int go = 0;
+                if (lane == 0) {
+                    if (*abort_flag) {
+                        go = 0;
+                    } else if (mbar_wait_bounded(smem_addr(&empty[slot]), phase ^ 1u, abort_flag)) {
+                        go = 1;
+                    } else {
+                        if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+                        *abort_flag = 1;
+                    }
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                } else {
+                    uint8_t* sbase = ring + (size_t)slot * geo.slot_bytes;
+                    // Coefficients into the slot header (published by the
+                    // same mbarrier phase as the data).
+                    if (lane < cnt) reinterpret_cast<float*>(sbase)[lane] = e < 0 ? 1.0f : w_k;
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(smem_addr(&full[slot]), (uint32_t)cnt * tile_bytes);
+                        rec[slot] = (uint8_t)(1u + phase);
+                    }
+                    if (lane < cnt) {
+                        const uint16_t* src;
+                        if (s < nS) src = a.S[s] + t * H + col;
+                        else if (s == nS) src = a.residual + t * H + col;
+                        else src = a.E[e % a.R] + row_k * H + col;
+                        bulk_g2s(smem_addr(sbase + kSlotHeader + (size_t)lane * geo.seg_stride), src,
+                                 tile_bytes, smem_addr(&full[slot]), pol);
+                    }
+                }
+                if (++slot == nst) {
+                    slot = 0;
+                    phase ^= 1u;
                 }
             }
+            if (my_row < 0 && lane < a.K && t + row_step < a.T) {  // row without routed stages
+                raw_next = __ldg(a.perm + (t + row_step) * a.K + lane);
+                w_next = __ldg(a.w + (t + row_step) * a.K + lane);
+            }
         }
-        // Never leave with a copy still landing in this CTA's shared memory.
-        for (int s = 0; s < nstages; ++s)
-            if ((issued >> s) & 1u) (void)mbar_wait_bounded(smem_addr(&full[s]), (last_par >> s) & 1u, nullptr);
+        // After an abort, wait (briefly, bounded) for every copy still landing
+        // in this CTA's shared memory before the CTA may exit.
+        if (lane == 0 && *abort_flag) {
+            for (int j = 0; j < nst; ++j)
+                if (rec[j])
+                    (void)mbar_wait_bounded(smem_addr(&full[j]), (uint32_t)(rec[j] - 1), nullptr,
+                                            10000000ull);
+        }
+        __syncwarp();
+        if (CLUSTERED) {
+            cluster_arrive_release();
+            cluster_wait_acquire();
+        }
         return;
     }
 
-    // ----------------------------------------------------------- consumers
+    // -------------------------------------------------------------- consumers
     const int ci = threadIdx.x - 32;
     const int nct = ncw * 32;
-    const int chunks = H / 8;
-    int chunk[CPT];
+    int lch[CPT];
     bool valid[CPT];
     float gw[CPT][8];
 #pragma unroll
     for (int m = 0; m < CPT; ++m) {
-        chunk[m] = ci + m * nct;
-        valid[m] = chunk[m] < chunks;
+        lch[m] = ci + m * nct;
+        valid[m] = lch[m] < nchunk;
         if (valid[m]) {
             float gf[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.gamma + (size_t)chunk[m] * 8), gf);
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.gamma + (size_t)(chunk0 + lch[m]) * 8), gf);
 #pragma unroll
             for (int j = 0; j < 8; ++j) gw[m][j] = gf[j] + a.weight_bias;
         }
     }
 
-    int stage = 0;
+    int slot = 0;
     uint32_t phase = 0;
-    int par = 0;
+    int par_row = 0;
+    uint32_t xph = 0u;  // bit p: phase of xbar[p] to wait for next
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-        float wk[kMaxTopK];
-#pragma unroll
-        for (int k = 0; k < kMaxTopK; ++k)
-            if (k < a.K) wk[k] = __ldg(a.w + t * a.K + k);
+    for (int64_t t = first_row; t < a.T; t += row_step) {
         float acc[CPT][8];
 #pragma unroll
         for (int m = 0; m < CPT; ++m)
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[m][j] = 0.0f;
-
-        auto consume = [&](float coef) {
-            if (ok && !mbar_wait_bounded(smem_addr(&full[stage]), phase, abort_flag)) {
+        for (int j = 0; j < nstage_row; ++j) {
+            int s0, cnt;
+            stage_range(j, P, nS + 1, nseg, s0, cnt);
+            if (ok && !mbar_wait_bounded(smem_addr(&full[slot]), phase, abort_flag)) {
                 ok = false;
                 if (!*abort_flag) atomicOr(a.err, kErrTimeout);
                 *abort_flag = 1;
             }
-            const uint4* sp = reinterpret_cast<const uint4*>(ring + (size_t)stage * stage_bytes);
+            const uint8_t* base = ring + (size_t)slot * geo.slot_bytes;
+            const float* coef = reinterpret_cast<const float*>(base);
+            const uint8_t* seg = base + kSlotHeader;
+            // U segments at a time: loads first, then FMAs.
+            for (int i0 = 0; i0 < cnt; i0 += U) {
+                float cf[U];
+                uint4 v[U][CPT];
 #pragma unroll
-            for (int m = 0; m < CPT; ++m) {
-                if (valid[m]) {
-                    float f[8];
-                    bf16x8_to_f32(sp[chunk[m]], f);
+                for (int u = 0; u < U; ++u) cf[u] = i0 + u < cnt ? coef[i0 + u] : 0.0f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[m][j] = fmaf(coef, f[j], acc[m][j]);
-                }
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int m = 0; m < CPT; ++m)
+                        if (i0 + u < cnt && valid[m])
+                            v[u][m] = reinterpret_cast<const uint4*>(seg + (size_t)(i0 + u) * geo.seg_stride)[lch[m]];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int m = 0; m < CPT; ++m)
+                        if (i0 + u < cnt && valid[m]) {
+                            float f[8];
+                            bf16x8_to_f32(v[u][m], f);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) acc[m][j] = fmaf(cf[u], f[j], acc[m][j]);
+                        }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
-            if (++stage == nstages) {
-                stage = 0;
+            if (lane == 0) mbar_arrive(smem_addr(&empty[slot]));
+            if (++slot == nst) {
+                slot = 0;
                 phase ^= 1u;
             }
-        };
+        }
 
-        for (int r = 0; r < nS; ++r) consume(1.0f);
-        consume(1.0f);  // residual
-#pragma unroll
-        for (int k = 0; k < kMaxTopK; ++k)
-            if (k < a.K)
-                for (int r = 0; r < a.R; ++r) consume(wk[k]);
-
-        // Row epilogue, all on chip: residual_out, sum of squares, out.
+        // Row epilogue, all on chip.
         float ss = 0.0f;
 #pragma unroll
         for (int m = 0; m < CPT; ++m) {
             if (valid[m]) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) ss = fmaf(acc[m][j], acc[m][j], ss);
-                store_residual8<RES_F32>(a.residual_out, t * H + (int64_t)chunk[m] * 8, acc[m]);
+                store_residual8<RES_F32>(a.residual_out, t * H + (int64_t)(chunk0 + lch[m]) * 8, acc[m]);
             }
         }
         ss = warp_sum(ss);
-        if (lane == 0) red[par * 32 + (warp - 1)] = ss;
+        if (lane == 0) red[par_row * 32 + (warp - 1)] = ss;
         named_barrier_sync(1, nct);
         float tot = 0.0f;
-        for (int w = 0; w < ncw; ++w) tot += red[par * 32 + w];
+        for (int w = 0; w < ncw; ++w) tot += red[par_row * 32 + w];
+        if (CLUSTERED) {
+            // Push this CTA's partial into every peer (lane rk -> peer rk, all
+            // at once), then wait for all C partials of the row.
+            const uint32_t xb = smem_addr(&xbar[par_row]);
+            if (ci < C) {
+                const uint32_t mine = smem_addr(&xslot[par_row * kMaxCluster + crank]);
+                st_shared_cluster_f32(map_shared_rank(mine, (uint32_t)ci), tot);
+                mbar_arrive_remote(map_shared_rank(xb, (uint32_t)ci));
+            }
+            if (ok && !mbar_wait_bounded<true>(xb, (xph >> par_row) & 1u, abort_flag)) {
+                ok = false;
+                if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            xph ^= 1u << par_row;
+            const volatile float* xs = xslot + par_row * kMaxCluster;
+            tot = 0.0f;
+            for (int rk = 0; rk < C; ++rk) tot += xs[rk];
+            // After the last row's push, arrive on the exit barrier now and
+            // wait at the end: no CTA leaves while a peer may still push into it.
+            if (t + row_step >= a.T) cluster_arrive_release();
+        }
         const float inv = rsqrtf(tot / (float)H + a.eps);
 #pragma unroll
         for (int m = 0; m < CPT; ++m) {
@@ -197,70 +339,181 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
                 float o[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) o[j] = acc[m][j] * inv * gw[m][j];
-                st_global16(reinterpret_cast<uint16_t*>(a.out) + t * H + (int64_t)chunk[m] * 8,
+                st_global16(reinterpret_cast<uint16_t*>(a.out) + t * H + (int64_t)(chunk0 + lch[m]) * 8,
                             f32x8_to_bf16x8(o));
             }
         }
-        par ^= 1;
+        par_row ^= 1;
+    }
+    if (CLUSTERED) {
+        if (first_row >= a.T) cluster_arrive_release();  // a cluster without rows
+        cluster_wait_acquire();
     }
 }
 
-template <int CPT, bool RES_F32>
-static cudaError_t set_attr_one(int smem_bytes) {
-    return cudaFuncSetAttribute(stream_rows_kernel<CPT, RES_F32>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+// ------------------------------------------------------------------ host side
+template <bool CL>
+struct KernelTable {
+    using Fn = void (*)(RowArgs, StreamGeom);
+    static constexpr int kU = 4;
+    static Fn get(int cpt, bool res_f32) {
+        switch (cpt * 2 + (res_f32 ? 1 : 0)) {
+            case 2: return stream_rows_kernel<1, kU, false, CL>;
+            case 3: return stream_rows_kernel<1, kU, true, CL>;
+            case 4: return stream_rows_kernel<2, kU, false, CL>;
+            case 5: return stream_rows_kernel<2, kU, true, CL>;
+            case 8: return stream_rows_kernel<4, kU, false, CL>;
+            case 9: return stream_rows_kernel<4, kU, true, CL>;
+        }
+        return nullptr;
+    }
+};
+
+static void* kernel_for(int cpt, bool res_f32, bool clustered) {
+    return clustered ? reinterpret_cast<void*>(KernelTable<true>::get(cpt, res_f32))
+                     : reinterpret_cast<void*>(KernelTable<false>::get(cpt, res_f32));
 }
 
-cudaError_t stream_rows_set_attributes(int smem_bytes) {
-    cudaError_t e;
-    if ((e = set_attr_one<1, false>(smem_bytes)) != cudaSuccess) return e;
-    if ((e = set_attr_one<1, true>(smem_bytes)) != cudaSuccess) return e;
-    if ((e = set_attr_one<2, false>(smem_bytes)) != cudaSuccess) return e;
-    if ((e = set_attr_one<2, true>(smem_bytes)) != cudaSuccess) return e;
-    if ((e = set_attr_one<4, false>(smem_bytes)) != cudaSuccess) return e;
-    return set_attr_one<4, true>(smem_bytes);
+cudaError_t stream_rows_set_attributes(int smem_optin) {
+    for (int cl = 0; cl < 2; ++cl)
+        for (int cpt = 1; cpt <= 4; cpt <<= 1)
+            for (int f = 0; f < 2; ++f) {
+                const void* k = kernel_for(cpt, f != 0, cl != 0);
+                cudaError_t e =
+                    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+                if (e != cudaSuccess) return e;
+                if (cl) {
+                    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                    if (e != cudaSuccess) return e;
+                }
+            }
+    return cudaSuccess;
 }
 
-bool plan_stream_rows(int H, int smem_optin, StreamPlan* p) {
-    const int chunks = H / 8;
-    int cpt = 1;
-    while (cpt < 4 && chunks > cpt * kStreamMaxConsumers) cpt <<= 1;
-    if (chunks > cpt * kStreamMaxConsumers) return false;
-    const int consumers = (chunks + cpt - 1) / cpt;
-    const int ncw = (consumers + 31) / 32;
-    const int stage_bytes = (H * 2 + 127) / 128 * 128;
-    int nstages = kStreamMaxStages;
-    while (nstages > 2 && stream_ring_offset(nstages) + nstages * stage_bytes > smem_optin)
-        --nstages;
-    if (stream_ring_offset(nstages) + nstages * stage_bytes > smem_optin) return false;
-    p->cpt = cpt;
-    p->threads = 32 * (ncw + 1);
-    p->nstages = nstages;
-    p->stage_bytes = stage_bytes;
-    p->smem = stream_ring_offset(nstages) + nstages * stage_bytes;
-    p->ctas_per_sm = 1;
+static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Consumer layout for a tile of `chunks` 16-byte chunks.
+static bool consumer_layout(int chunks, int* cpt, int* threads) {
+    int c = 1;
+    while (c < 4 && chunks > c * kStreamMaxConsumers) c <<= 1;
+    if (chunks > c * kStreamMaxConsumers) return false;
+    *cpt = c;
+    *threads = 32 * (ceil_div(ceil_div(chunks, c), 32) + 1);
     return true;
 }
 
-cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, int grid, bool res_f32,
-                               cudaStream_t stream) {
-    const dim3 g((unsigned)grid), b((unsigned)p.threads);
-    const size_t sm = (size_t)p.smem;
-#define ARF_LAUNCH(CPT_)                                                                    \
-    do {                                                                                    \
-        if (res_f32)                                                                        \
-            stream_rows_kernel<CPT_, true><<<g, b, sm, stream>>>(a, p.nstages, p.stage_bytes); \
-        else                                                                                \
-            stream_rows_kernel<CPT_, false><<<g, b, sm, stream>>>(a, p.nstages, p.stage_bytes); \
-    } while (0)
-    switch (p.cpt) {
-        case 1: ARF_LAUNCH(1); break;
-        case 2: ARF_LAUNCH(2); break;
-        case 4: ARF_LAUNCH(4); break;
-        default: return cudaErrorInvalidValue;
+bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
+                      int max_cluster, int C, int stage_bytes, StreamPlan* p) {
+    const int chunks = H / 8;
+    const int nseg = (shared ? R : 0) + 1 + R * K;
+    if (chunks < 1 || T < 1) return false;
+    if (C <= 0) {
+        // Enough CTAs to cover every SM: split rows into tiles only when the
+        // rows alone cannot, and never so finely that a CTA owns no chunk.
+        // Whole rows once there are at least half as many rows as SMs
+        // (measured: one row per CTA beats split rows there).
+        C = 1;
+        if (2 * T < num_sms)
+            while (C < kMaxCluster && C * 2 <= max_cluster && (int64_t)C * T < num_sms &&
+                   (2 * C - 1) * ceil_div(chunks, 2 * C) < chunks)
+                C <<= 1;
     }
-#undef ARF_LAUNCH
-    return cudaGetLastError();
+    if (C < 1 || C > kMaxCluster || C > max_cluster) return false;
+    const int tile = ceil_div(chunks, C);
+    if ((C - 1) * tile >= chunks) return false;  // every CTA must own a chunk
+    int cpt, threads;
+    if (!consumer_layout(tile, &cpt, &threads)) return false;
+    const int seg_stride = ceil_div(tile * 16, 128) * 128;
+    // Segments per slot: enough for a ~16 KB (tiles) / ~32 KB (whole rows)
+    // slot, at most one per producer lane, spread evenly over the row.
+    const int target = stage_bytes > 0 ? stage_bytes : (C == 1 ? 65536 : 16384);
+    int P = target / seg_stride;
+    if (P < 1) P = 1;
+    if (P > 32) P = 32;
+    if (P > nseg) P = nseg;
+    while (P > 1 && stream_ring_offset(2) + 2 * (kSlotHeader + P * seg_stride) > smem_optin) --P;
+    const int nsr = (shared ? R : 0) + 1;
+    if (R * K > 0) P = ceil_div(R * K, ceil_div(R * K, P));  // routed stages of equal size
+    const int slot_bytes = kSlotHeader + P * seg_stride;
+    const int per_row = ceil_div(nsr, P) + ceil_div(R * K, P);
+    int nst;
+    if (C == 1) {
+        // Whole rows: one CTA per SM with the deepest ring that fits.
+        nst = kStreamMaxStages;
+        while (nst > 2 && stream_ring_offset(nst) + nst * slot_bytes > smem_optin) --nst;
+    } else {
+        // Tiles: a ring of ~1/3 of shared memory (three CTAs per SM, leaving
+        // room for the 1 KB the driver reserves per CTA), at most two rows deep.
+        const int budget = smem_optin / 3 - 3072;
+        nst = budget / slot_bytes;
+        if (nst > 2 * per_row) nst = 2 * per_row;
+        if (nst > kStreamMaxStages) nst = kStreamMaxStages;
+        if (nst < 2) nst = 2;
+    }
+    if (nst < 2 || stream_ring_offset(nst) + nst * slot_bytes > smem_optin) return false;
+    p->geo.nstages = nst;
+    p->geo.slot_bytes = slot_bytes;
+    p->geo.seg_per_stage = P;
+    p->geo.seg_stride = seg_stride;
+    p->geo.C = C;
+    p->geo.tile_chunks = tile;
+    p->cpt = cpt;
+    p->threads = threads;
+    p->smem = stream_ring_offset(nst) + nst * slot_bytes;
+    if (C == 1) {
+        p->grid = (int)(T < num_sms ? T : num_sms);
+    } else {
+        const int per_sm = smem_optin / p->smem > 0 ? smem_optin / p->smem : 1;
+        int64_t clusters = ((int64_t)num_sms * per_sm) / C;
+        if (clusters < 1) clusters = 1;
+        if (clusters > T) clusters = T;
+        p->grid = (int)clusters * C;
+    }
+    return true;
+}
+
+int stream_rows_max_cluster(int threads, int smem, int cpt) {
+    for (int C = kMaxCluster; C >= 2; C >>= 1) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3((unsigned)C);
+        cfg.blockDim = dim3((unsigned)threads);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        const void* k = kernel_for(cpt, false, true);
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0) return C;
+        (void)cudaGetLastError();
+    }
+    return 1;
+}
+
+cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, bool res_f32,
+                               cudaStream_t stream) {
+    const bool clustered = p.geo.C > 1;
+    const void* k = kernel_for(p.cpt, res_f32, clustered);
+    if (!k) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = (size_t)p.smem;
+    cfg.stream = stream;
+    if (clustered) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)p.geo.C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    void* args[] = {const_cast<RowArgs*>(&a), const_cast<StreamGeom*>(&p.geo)};
+    return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 }  // namespace arf
