@@ -216,6 +216,45 @@ ARFUSE_API ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes);
  * regime); may be NULL. */
 ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
 
+/*
+ * ar_finalize_rmsnorm_noalloc -- the fused op for callers that cannot allocate
+ * device memory.  (No counterpart on the pages: an addition of this library.)
+ *
+ * Some callers may not call cudaMalloc at all -- code that runs while an
+ * engine captures a CUDA graph, plugins whose host engine owns every byte of
+ * device memory through its own pool, deployments with a fixed memory budget
+ * -- and ar_workspace_create() allocates a small device block.  This entry
+ * point needs no workspace and allocates nothing (no cudaMalloc, no cudaFree,
+ * no allocating library routine): the kernels' only global memory beyond the
+ * caller's inputs and outputs, the 4-byte device status word, lives in a
+ * fixed 256-byte array inside this library (kept by every GPU that loads the
+ * library until the process exits).  The caller still passes every input and
+ * output, with the arguments, layouts, alignment rules and limits of
+ * ar_finalize_rmsnorm(); R, K, H and eps are taken from the call.  Sizes
+ * beyond the limits are rejected before anything runs: R > AR_MAX_RANKS or
+ * K > AR_MAX_TOP_K (AR_ERR_INVALID_ARG), H outside [8, AR_MAX_HIDDEN]
+ * (AR_ERR_UNSUPPORTED), T > 2^26 (AR_ERR_CAPACITY).  The status word needs 4
+ * bytes for any size, so the array's 256 bytes always suffice.
+ *
+ *   - The first call on a device (the current device) does a one-time set-up
+ *     there: kernel attributes and the device address of the array.  Make that
+ *     first call before any stream capture on that device.
+ *   - Each call clears the status word on `stream` before its kernel runs.
+ *     Device-side check results (a clamped perm value, a wait past its time
+ *     limit) land in that word and are not reported by this entry point; check
+ *     perm ranges on the host where they matter, or use a workspace.
+ *   - Every call shares the array: calls that overlap on the GPU (on
+ *     different streams, without ordering between them) race on the status
+ *     word.  Their outputs are unaffected.
+ */
+ARFUSE_API ar_status ar_finalize_rmsnorm_noalloc(const void* const* expert_out, int64_t rows_e,
+                                                 const int32_t* perm, const float* topk_w,
+                                                 const void* const* shared_out,
+                                                 const void* residual, const void* gamma,
+                                                 float weight_bias, float eps, int64_t T, int R,
+                                                 int K, int H, void* out, void* residual_out,
+                                                 int residual_out_is_fp32, void* stream);
+
 /* Static description of a status code; never NULL. */
 ARFUSE_API const char* ar_status_string(ar_status s);
 

@@ -11,6 +11,7 @@
 // be captured in a CUDA graph.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "arf_common.cuh"
@@ -383,6 +384,128 @@ const char* ar_status_string(ar_status s) {
         case AR_VALIDATED: return "validated (dry-run workspace, nothing launched)";
     }
     return "unknown status";
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc: code that runs while a serving
+// framework captures a CUDA graph (allocation is illegal inside a capture),
+// plugins living under an engine whose memory pool owns all device memory and
+// rejects allocations it did not make, or deployments with a fixed device
+// memory budget checked at start-up.  ar_workspace_create() allocates a small
+// device block for the kernels' status word, so those callers cannot use it.
+// ar_finalize_rmsnorm_noalloc() needs no workspace: the only global memory the
+// kernels use beyond the caller's inputs and outputs -- the status word that
+// device-side checks write -- lives in the fixed array below, which every GPU
+// that loads this library holds until the process exits.
+namespace {
+
+constexpr int kNoAllocScratchBytes = 256;  // stated maximum; a call uses 4 bytes
+static __device__ __align__(256) unsigned int g_noalloc_scratch[kNoAllocScratchBytes / 4];
+
+constexpr int kNoAllocMaxDevices = 64;
+struct NoAllocDevice {
+    bool ready;
+    unsigned* scratch;  // device address of g_noalloc_scratch on this device
+    int num_sms;
+    int smem_optin;
+    int max_cluster;
+    int max_cluster_stream;
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// One-time set-up for the current device: kernel attributes, launch limits and
+// the device address of the scratch array.  Allocates nothing.
+ar_status noalloc_setup(int device, NoAllocDevice** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice& d = g_noalloc_dev[device];
+    if (d.ready) {
+        *out = &d;
+        return AR_OK;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return AR_ERR_CUDA;
+    if (prop.major < 10) return AR_ERR_UNSUPPORTED;
+    if (arf::stream_rows_set_attributes((int)prop.sharedMemPerBlockOptin) != cudaSuccess ||
+        arf::cluster_rows_set_attributes() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    d.scratch = static_cast<unsigned*>(p);
+    d.num_sms = prop.multiProcessorCount;
+    d.smem_optin = (int)prop.sharedMemPerBlockOptin;
+    // Largest co-schedulable clusters for the biggest block shapes the plans
+    // can produce (one-shot: 768 threads, 24 KB; tiles: 544 threads, a third
+    // of shared memory).
+    d.max_cluster = arf::cluster_rows_max_cluster(768, 24576, false);
+    if (d.max_cluster < 1) d.max_cluster = 1;
+    d.max_cluster_stream = arf::stream_rows_max_cluster(544, d.smem_optin / 3, 1);
+    d.ready = true;
+    *out = &d;
+    return AR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ar_status ar_finalize_rmsnorm_noalloc(const void* const* expert_out, int64_t rows_e,
+                                      const int32_t* perm, const float* topk_w,
+                                      const void* const* shared_out, const void* residual,
+                                      const void* gamma, float weight_bias, float eps, int64_t T,
+                                      int R, int K, int H, void* out, void* residual_out,
+                                      int residual_out_is_fp32, void* stream) {
+    if (K < 0 || K > AR_MAX_TOP_K || R < 1 || R > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
+    if (H < 8 || H > AR_MAX_HIDDEN) return AR_ERR_UNSUPPORTED;
+    if (H % 8 != 0) return AR_ERR_ALIGNMENT;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return AR_ERR_INVALID_ARG;
+    if (T > kMaxTokensLimit) return AR_ERR_CAPACITY;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return AR_ERR_CUDA;
+    if (device < 0 || device >= kNoAllocMaxDevices) return AR_ERR_UNSUPPORTED;
+    NoAllocDevice* d = nullptr;
+    const ar_status st = noalloc_setup(device, &d);
+    if (st != AR_OK) return st;
+
+    // A workspace on the stack: the same validation, plans and kernels as
+    // ar_finalize_rmsnorm(), with the scratch array as the status word.
+    ar_workspace ws;
+    std::memset(&ws, 0, sizeof ws);
+    ws.device = device;
+    ws.R = R;
+    ws.K = K;
+    ws.H = H;
+    ws.max_tokens = kMaxTokensLimit;
+    ws.eps = eps;
+    ws.flags = AR_WS_DRY_RUN;  // first pass: validate only
+    ws.d_err = d->scratch;
+    ws.num_sms = d->num_sms;
+    ws.smem_optin = d->smem_optin;
+    ws.max_cluster = d->max_cluster;
+    ws.max_cluster_stream = d->max_cluster_stream;
+    ws.regime_force = AR_REGIME_AUTO;
+    ar_status v = run(&ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma,
+                      weight_bias, eps, T, R, K, H, out, residual_out, residual_out_is_fp32,
+                      stream, true);
+    if (v != AR_VALIDATED) return v;  // AR_OK for T == 0, else the rejection
+    // The status word must start at zero for this call.
+    if (cudaMemsetAsync(d->scratch, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    ws.flags = 0;
+    return run(&ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma, weight_bias,
+               eps, T, R, K, H, out, residual_out, residual_out_is_fp32, stream, true);
 }
 
 }  // extern "C"
