@@ -1,0 +1,73 @@
+// Host-only check of the streaming kernel's launch planner and of the address
+// arithmetic its kernel derives from a plan (compiled and run by
+// tests/test_plans.py; no GPU needed).  For every shape it checks that the
+// plan fits shared memory, that every CTA of a row owns at least one column
+// chunk, that consumer threads cover every chunk, that a slot holds its
+// segments and their coefficient header, and that a slot's bytes fit an
+// mbarrier transaction count.  The automatic plan must exist for every shape.
+#include "stream_rows.cu"
+#include <cstdio>
+#include <cstdlib>
+using namespace arf;
+int main() {
+  long checks = 0, fails = 0;
+  int Hs[] = {8, 56, 256, 264, 2048, 6144, 7168, 8192, 12296, 16384};
+  int Rs[] = {1, 2, 3, 8, 16};
+  int Ks[] = {0, 1, 2, 5, 8, 10, 16};
+  long Ts[] = {1, 2, 3, 4, 7, 16, 37, 64, 128, 151, 152, 153, 333, 512, 2048, 8192};
+  for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts) {
+    if (K == 0 && !sh) continue;
+    for (int sb : {0, 1024, 4096, 16384, 65536, 131072})
+    for (int Cf = 0; Cf <= 16; Cf = Cf ? Cf * 2 : 1) {
+      StreamPlan p;
+      if (!plan_stream_rows(R, K, H, sh, T, 152, 232448, 16, Cf, sb, &p)) {
+        if (Cf == 0 || Cf == 1) { ++fails; printf("auto/stream plan failed H=%d R=%d K=%d T=%ld Cf=%d\n", H, R, K, T, Cf); }
+        continue;
+      }
+      const auto& g = p.geo;
+      int C = g.C; int chunks = H / 8;
+      int nS = sh ? R : 0, nseg = nS + 1 + R * K;
+      ++checks;
+      bool bad = false;
+      if (p.smem > 232448) bad = true;
+      if (stream_ring_offset(g.nstages) + g.nstages * g.slot_bytes > p.smem) bad = true;
+      if (p.grid % C) bad = true;
+      if (p.threads > 544 || p.threads % 32) bad = true;
+      if (g.nstages < 2) bad = true;
+      if (g.seg_per_stage < 1 || g.seg_per_stage > 32 || g.seg_per_stage > nseg) bad = true;
+      if (g.slot_bytes != kSlotHeader + g.seg_per_stage * g.seg_stride) bad = true;
+      if (g.seg_per_stage * 4 > kSlotHeader) bad = true;
+      // the tx bytes of one slot fit an mbarrier's transaction count
+      if ((long)g.seg_per_stage * g.seg_stride >= (1 << 20)) bad = true;
+      int ncw = p.threads / 32 - 1, nct = ncw * 32;
+      for (int c = 0; c < C; ++c) {
+        int chunk0 = c * g.tile_chunks;
+        int nchunk = std::min(g.tile_chunks, chunks - chunk0);
+        if (nchunk < 1) bad = true;
+        if (nchunk * 16 > g.seg_stride) bad = true;
+        if (g.seg_stride % 128) bad = true;
+        // consumers cover every chunk of the tile exactly once
+        if ((long)nct * p.cpt < nchunk) bad = true;
+        // the last element written
+        if ((long)(chunk0 + nchunk) * 8 > H) bad = true;
+      }
+      // header: rec[] ends before the ring
+      int hdr = g.nstages * 16 + 16 + 2 * 16 * 4 + 64 * 4 + 16 + g.nstages;
+      if (hdr > stream_ring_offset(g.nstages)) bad = true;
+      if (nseg < 1) bad = true;
+      // ring positions: q in [0, 2n) maps to a slot < n
+      for (int q = 0; q < 2 * g.nstages; ++q) { int sl = q >= g.nstages ? q - g.nstages : q; if (sl < 0 || sl >= g.nstages) bad = true; }
+      if (bad) { ++fails; if (fails < 20) printf("BAD H=%d R=%d K=%d sh=%d T=%ld Cf=%d -> C=%d tile=%d nst=%d slot=%d thr=%d smem=%d grid=%d\n", H,R,K,sh,T,Cf,C,g.tile_chunks,g.nstages,g.slot_bytes,p.threads,p.smem,p.grid); }
+    }
+  }
+  // show the automatic plans for the workloads
+  struct W { const char* n; int R, K, H; bool sh; long T[8]; } ws[] = {
+    {"ar_only", 2, 0, 7168, true, {1, 2, 4, 8, 16, 32, 64, 128}},
+    {"dsv3", 8, 8, 7168, true, {1, 4, 16, 64, 128, 0}},
+    {"glm", 8, 8, 6144, true, {1, 2, 4, 8, 16, 0}},
+    {"prefill", 8, 10, 8192, true, {512, 2048, 8192, 0}}};
+  for (auto& w : ws) for (long T : w.T) { if (!T) break; StreamPlan p; bool ok = plan_stream_rows(w.R, w.K, w.H, w.sh, T, 152, 232448, 16, 0, 0, &p);
+      printf("%-8s T=%5ld ok=%d C=%2d tile=%4d cpt=%d thr=%3d nst=%3d P=%2d slot=%5d smem=%6d grid=%4d\n", w.n, T, ok, p.geo.C, p.geo.tile_chunks, p.cpt, p.threads, p.geo.nstages, p.geo.seg_per_stage, p.geo.slot_bytes, p.smem, p.grid); }
+  printf("checked %ld plans, %ld bad\n", checks, fails);
+  return fails != 0;
+}
