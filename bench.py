@@ -72,6 +72,8 @@ def parse():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=8)
+    p.add_argument("--e2e-streams", type=int, default=1,
+                   help="streams the per-step host->device input copies are spread over")
     p.add_argument("--regime", default="auto",
                    help="force a kernel regime for the timed call: auto, cluster, stream, "
                         "oneshot or c<N> (cluster regime with N CTAs per row)")
@@ -421,13 +423,30 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
     h2d = sum(x.numel() * x.element_size() for x in ins)
     d2h = 2 * T * H * 2
 
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(max(1, args.e2e_streams))]
+
     def step():
-        for h, x in zip(host, ins):
-            x.copy_(h, non_blocking=True)
+        # Inputs in over several copy streams (each after the previous step's
+        # kernel has read them), the op, outputs back.
+        ready = torch.cuda.Event()
+        ready.record(stream)
+        done = []
+        for i, (h, x) in enumerate(zip(host, ins)):
+            cs = copy_streams[i % len(copy_streams)]
+            cs.wait_event(ready)
+            with torch.cuda.stream(cs):
+                x.copy_(h, non_blocking=True)
+        for cs in copy_streams:
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            done.append(ev)
+        for ev in done:
+            stream.wait_event(ev)
         arf.ar_finalize_rmsnorm(ws, d["E"], d["perm"], d["w"], d["S"], d["residual"], d["gamma"],
                                 d["weight_bias"], d["eps"], out=out, residual_out=r_out, stream=stream)
-        h_out.copy_(out, non_blocking=True)
-        h_rout.copy_(r_out, non_blocking=True)
+        with torch.cuda.stream(stream):
+            h_out.copy_(out, non_blocking=True)
+            h_rout.copy_(r_out, non_blocking=True)
 
     for _ in range(2):
         step()
@@ -446,7 +465,8 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
     del host
     return {"value": round(world * bytes_step / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
-            "steps": n, "api": "tp_reduce_moe_gb300.ar_finalize_rmsnorm"}
+            "steps": n, "copy_streams": len(copy_streams),
+            "api": "tp_reduce_moe_gb300.ar_finalize_rmsnorm"}
 
 
 def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate"):
