@@ -52,6 +52,11 @@ def _bind(path: str):
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
         P, P, P, P, P, P, ctypes.c_double, ctypes.c_double, ctypes.c_int,
         P, P, P]
+    lib.oracle_ar_finalize_rmsnorm_gated.restype = ctypes.c_int
+    lib.oracle_ar_finalize_rmsnorm_gated.argtypes = [
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+        P, P, P, P, P, P, P, ctypes.c_double, ctypes.c_double, ctypes.c_int,
+        P, P, P]
     lib.oracle_round_bf16.restype = ctypes.c_double
     lib.oracle_round_bf16.argtypes = [ctypes.c_double]
     lib.oracle_round_bf16_array.restype = None
@@ -119,14 +124,15 @@ def round_bf16(x) -> np.ndarray:
 
 
 def ar_finalize_rmsnorm_ref(E, perm, w, S, residual, gamma, weight_bias, eps,
-                            h_bf16_before_norm=False, want_abs=False):
+                            h_bf16_before_norm=False, want_abs=False, shared_gate=None):
     """fp64 oracle of the fused boundary op for all T rows.
 
     E: list of R arrays [rows_e, H] (bf16 bits), or None/[] when K == 0.
     perm: int32 [T, K]; w: float32 [T, K]; S: list of R arrays [T, H] or None.
-    residual: [T, H]; gamma: [H].  Returns dict with float64 ``h`` (the
-    unrounded residual_out), ``out`` and, with ``want_abs``, ``abs`` (sum of
-    |terms| per element).
+    residual: [T, H]; gamma: [H].  shared_gate: optional float32 [T] gate
+    logits (the shared term of token t is scaled by sigmoid(shared_gate[t])).
+    Returns dict with float64 ``h`` (the unrounded residual_out), ``out`` and,
+    with ``want_abs``, ``abs`` (sum of |terms| per element).
     """
     residual = _u16(residual)
     T, H = residual.shape
@@ -159,14 +165,20 @@ def ar_finalize_rmsnorm_ref(E, perm, w, S, residual, gamma, weight_bias, eps,
     ab = np.empty((T, H), np.float64) if want_abs else None
     e_tab = _ptr_table(E) if E else None
     s_tab = _ptr_table(S) if S else None
-    rc = _load().oracle_ar_finalize_rmsnorm(
-        R, K, H, T, rows_e,
-        ctypes.cast(e_tab, ctypes.c_void_p) if e_tab is not None else None,
-        _ptr(perm), _ptr(w),
-        ctypes.cast(s_tab, ctypes.c_void_p) if s_tab is not None else None,
-        _ptr(residual), _ptr(gamma), float(weight_bias), float(eps),
-        1 if h_bf16_before_norm else 0,
-        _ptr(h), _ptr(out), _ptr(ab) if ab is not None else None)
+    common_head = (R, K, H, T, rows_e,
+                   ctypes.cast(e_tab, ctypes.c_void_p) if e_tab is not None else None,
+                   _ptr(perm), _ptr(w),
+                   ctypes.cast(s_tab, ctypes.c_void_p) if s_tab is not None else None)
+    common_tail = (_ptr(residual), _ptr(gamma), float(weight_bias), float(eps),
+                   1 if h_bf16_before_norm else 0,
+                   _ptr(h), _ptr(out), _ptr(ab) if ab is not None else None)
+    if shared_gate is not None:
+        gate = np.ascontiguousarray(shared_gate, dtype=np.float32)
+        if gate.shape != (T,):
+            raise ValueError(f"shared_gate shape {gate.shape} != {(T,)}")
+        rc = _load().oracle_ar_finalize_rmsnorm_gated(*common_head, _ptr(gate), *common_tail)
+    else:
+        rc = _load().oracle_ar_finalize_rmsnorm(*common_head, *common_tail)
     if rc == -2:
         raise IndexError("perm value outside [0, rows_e)")
     if rc != 0:

@@ -27,6 +27,9 @@
  *  - same page, Modifications section 2: the DeepSeek-V3 shared expert has no
  *    sigmoid gate (it is added unmodified), and a replicated shared expert
  *    must not be folded in: S_r is a per-rank partial, summed once over r.
+ *    The Qwen-style shared expert does carry a per-token sigmoid gate, applied
+ *    to the shared output before the fused add: with gate logits g[t] the
+ *    shared term becomes sigmoid(g[t]) * S_r[t,j] (oracle_..._gated).
  *  - sglang PR #37104 "perf(mtp): fuse trailing TP all-reduce with final
  *    RMSNorm", Changes: a residual is mandatory.
  *
@@ -90,9 +93,11 @@ void oracle_round_bf16_array(const double *x, double *y, int64_t n)
 static void oracle_row_sum(int64_t t, int R, int K, int H,
                            const uint16_t *const *E, const int32_t *perm,
                            const float *w, const uint16_t *const *S,
-                           const uint16_t *residual, double *h_row,
-                           double *abs_row)
+                           const float *gate, const uint16_t *residual,
+                           double *h_row, double *abs_row)
 {
+    /* shared-expert gate of this token: sigmoid of its logit (1 if none) */
+    const double g = gate ? 1.0 / (1.0 + exp(-(double)gate[t])) : 1.0;
     for (int j = 0; j < H; ++j) {
         double y = 0.0, a = 0.0;
         for (int r = 0; r < R; ++r) {
@@ -105,7 +110,7 @@ static void oracle_row_sum(int64_t t, int R, int K, int H,
                 a += fabs(term);
             }
             if (S) {
-                double s = bf16_bits_to_double(S[r][t * H + j]);
+                double s = g * bf16_bits_to_double(S[r][t * H + j]);
                 y_r += s;
                 a += fabs(s);
             }
@@ -154,12 +159,12 @@ static void oracle_row_norm(int H, const double *h_row, const uint16_t *gamma,
  * Returns ORACLE_OK, ORACLE_BAD_ARG, or ORACLE_PERM_RANGE when some perm value
  * is outside [0, rows_e) (nothing is computed then).
  */
-int oracle_ar_finalize_rmsnorm(int R, int K, int H, int64_t T, int64_t rows_e,
-                               const uint16_t *const *E, const int32_t *perm,
-                               const float *w, const uint16_t *const *S,
-                               const uint16_t *residual, const uint16_t *gamma,
-                               double weight_bias, double eps, int h_bf16,
-                               double *h_out, double *out, double *abs_terms)
+static int oracle_run(int R, int K, int H, int64_t T, int64_t rows_e,
+                      const uint16_t *const *E, const int32_t *perm, const float *w,
+                      const uint16_t *const *S, const float *gate,
+                      const uint16_t *residual, const uint16_t *gamma,
+                      double weight_bias, double eps, int h_bf16, double *h_out,
+                      double *out, double *abs_terms)
 {
     if (R < 1 || K < 0 || H < 1 || T < 0 || !residual || !gamma || !h_out ||
         !out)
@@ -168,6 +173,8 @@ int oracle_ar_finalize_rmsnorm(int R, int K, int H, int64_t T, int64_t rows_e,
         return ORACLE_BAD_ARG;
     if (K == 0 && !S)
         return ORACLE_BAD_ARG;   /* nothing to reduce */
+    if (gate && !S)
+        return ORACLE_BAD_ARG;   /* a gate needs a shared term */
     for (int64_t i = 0; i < T * (int64_t)K; ++i)
         if (perm[i] < 0 || (int64_t)perm[i] >= rows_e)
             return ORACLE_PERM_RANGE;
@@ -175,12 +182,40 @@ int oracle_ar_finalize_rmsnorm(int R, int K, int H, int64_t T, int64_t rows_e,
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < T; ++t) {
         double *h_row = h_out + t * H;
-        oracle_row_sum(t, R, K, H, E, perm, w, S, residual, h_row,
+        oracle_row_sum(t, R, K, H, E, perm, w, S, gate, residual, h_row,
                        abs_terms ? abs_terms + t * H : NULL);
         oracle_row_norm(H, h_row, gamma, weight_bias, eps, h_bf16,
                         out + t * H);
     }
     return ORACLE_OK;
+}
+
+int oracle_ar_finalize_rmsnorm(int R, int K, int H, int64_t T, int64_t rows_e,
+                               const uint16_t *const *E, const int32_t *perm,
+                               const float *w, const uint16_t *const *S,
+                               const uint16_t *residual, const uint16_t *gamma,
+                               double weight_bias, double eps, int h_bf16,
+                               double *h_out, double *out, double *abs_terms)
+{
+    return oracle_run(R, K, H, T, rows_e, E, perm, w, S, NULL, residual, gamma,
+                      weight_bias, eps, h_bf16, h_out, out, abs_terms);
+}
+
+/* The same with the Qwen-style per-token sigmoid gate on the shared term:
+ * gate[t] is the fp32 gate logit of token t (required, as is S). */
+int oracle_ar_finalize_rmsnorm_gated(int R, int K, int H, int64_t T,
+                                     int64_t rows_e, const uint16_t *const *E,
+                                     const int32_t *perm, const float *w,
+                                     const uint16_t *const *S, const float *gate,
+                                     const uint16_t *residual,
+                                     const uint16_t *gamma, double weight_bias,
+                                     double eps, int h_bf16, double *h_out,
+                                     double *out, double *abs_terms)
+{
+    if (!gate || !S)
+        return ORACLE_BAD_ARG;
+    return oracle_run(R, K, H, T, rows_e, E, perm, w, S, gate, residual, gamma,
+                      weight_bias, eps, h_bf16, h_out, out, abs_terms);
 }
 
 /* Trailing all-reduce + residual RMSNorm without a MoE term: the K = 0 case,

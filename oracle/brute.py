@@ -28,12 +28,15 @@ def _fr_bf16(b) -> Fraction:
     return Fraction(bf16_bits_to_float(int(b)))
 
 
-def brute_ar_finalize_rmsnorm(E, perm, w, S, residual, gamma, weight_bias, eps):
+def brute_ar_finalize_rmsnorm(E, perm, w, S, residual, gamma, weight_bias, eps,
+                              shared_gate=None):
     """Nested Python lists/arrays in, exact ``h`` (Fractions) and ``out`` (floats) out.
 
     E: list over r of [rows_e][H] bf16 bit patterns (or None when K == 0);
     perm, w: [T][K]; S: list over r of [T][H] bits, or None;
-    residual: [T][H] bits; gamma: [H] bits.
+    residual: [T][H] bits; gamma: [H] bits; shared_gate: optional [T] gate
+    logits -- the shared term of token t is scaled by sigmoid(gate[t]) (the
+    sigmoid is taken in binary64, then used exactly).
     """
     T = len(residual)
     H = len(residual[0])
@@ -44,13 +47,16 @@ def brute_ar_finalize_rmsnorm(E, perm, w, S, residual, gamma, weight_bias, eps):
     h = [[Fraction(0)] * H for _ in range(T)]
     out = [[0.0] * H for _ in range(T)]
     for t in range(T):
+        g = Fraction(1)
+        if shared_gate is not None:
+            g = Fraction(1.0 / (1.0 + math.exp(-float(shared_gate[t]))))
         for j in range(H):
             y = Fraction(0)
             for r in range(R):
                 for k in range(K):
                     y += Fraction(float(w[t][k])) * _fr_bf16(E[r][int(perm[t][k])][j])
                 if S:
-                    y += _fr_bf16(S[r][t][j])
+                    y += g * _fr_bf16(S[r][t][j])
             h[t][j] = y + _fr_bf16(residual[t][j])
         ms = sum(x * x for x in h[t]) / H
         root = math.sqrt(ms + ep)            # the one binary64 step

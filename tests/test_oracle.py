@@ -301,3 +301,59 @@ def test_page_tolerance_fixture():
     for v in (2.0, 3.99, 100.0):
         assert d <= atol + rtol * v
     assert (rtol, atol) == (BF16_RTOL, BF16_ATOL)
+
+
+# ------------------------------------------------ gated shared expert (Qwen-style)
+# PR #37196 "[Comm] Share the CuTe DSL AR fusion core ...", Modifications
+# section 2: the Qwen-style shared expert carries a per-token sigmoid gate,
+# applied to the shared output before the fused add.
+@pytest.mark.parametrize("R,K", [(1, 1), (2, 2), (2, 0)])
+def test_gated_brute_force_2x4(R, K):
+    rng = np.random.default_rng(77 + R + 10 * K)
+    E, perm, w, S, res, gamma = _small_problem(rng, 2, 4, K, R, True, False, rows_e=5 if K else None)
+    gate = rng.normal(0, 2, 2).astype(np.float32)
+    h_ex, out_ex = brute_ar_finalize_rmsnorm(E, perm, w, S, res, gamma, 0.0, 1e-6, shared_gate=gate)
+    got = oracle.ar_finalize_rmsnorm_ref(E, perm, w, S, res, gamma, 0.0, 1e-6, want_abs=True,
+                                         shared_gate=gate)
+    for t in range(2):
+        for j in range(4):
+            assert abs(got["h"][t, j] - float(h_ex[t][j])) <= 1e-14 * got["abs"][t, j] + 1e-300
+            assert math.isclose(got["out"][t, j], out_ex[t][j], rel_tol=1e-12, abs_tol=1e-300)
+
+
+def test_gate_limits_are_exact():
+    """sigmoid(+50) == 1 and sigmoid(-800) == 0 in binary64; sigmoid(0) == 1/2."""
+    inp = make_inputs("dsv3_decode", 3)
+    a = oracle_args(inp)
+    T = inp["T"]
+    call = lambda S, gate: oracle.ar_finalize_rmsnorm_ref(a["E"], a["perm"], a["w"], S, a["residual"],
+                                                          a["gamma"], 0.0, a["eps"], shared_gate=gate)
+    plain = call(a["S"], None)
+    no_shared = call(None, None)
+    assert np.array_equal(call(a["S"], np.full(T, 50, np.float32))["h"], plain["h"])
+    assert np.array_equal(call(a["S"], np.full(T, -800, np.float32))["h"], no_shared["h"])
+    half_S = [bf16_bits((torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).float() * 0.5)
+                        .to(torch.bfloat16)) for s in a["S"]]
+    np.testing.assert_allclose(call(a["S"], np.zeros(T, np.float32))["h"], call(half_S, None)["h"],
+                               rtol=0, atol=1e-12)
+
+
+def test_gate_scales_only_the_shared_term():
+    inp = make_inputs("glm_gemma", 4)
+    a = oracle_args(inp)
+    gate = np.array([-3.0, -0.5, 0.7, 4.0], np.float32)
+    call = lambda S, g: oracle.ar_finalize_rmsnorm_ref(a["E"], a["perm"], a["w"], S, a["residual"],
+                                                       a["gamma"], 0.0, a["eps"], shared_gate=g)["h"]
+    base = call(None, None)
+    full = call(a["S"], None)
+    gated = call(a["S"], gate)
+    sig = 1.0 / (1.0 + np.exp(-gate.astype(np.float64)))
+    np.testing.assert_allclose(gated - base, sig[:, None] * (full - base), rtol=1e-12, atol=1e-12)
+
+
+def test_gate_needs_a_shared_term():
+    rng = np.random.default_rng(1)
+    E, perm, w, S, res, gamma = _small_problem(rng, 2, 8, 2, 1)
+    with pytest.raises(ValueError):
+        oracle.ar_finalize_rmsnorm_ref(E, perm, w, None, res, gamma, 0.0, 1e-6,
+                                       shared_gate=np.zeros(2, np.float32))

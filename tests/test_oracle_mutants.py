@@ -32,6 +32,9 @@ MUTANTS = [
     ("last column of the norm skipped", "for (int j = 0; j < H; ++j) {\n        double hj = h_bf16 ? oracle_round_bf16(h_row[j]) : h_row[j];\n        ssq",
      "for (int j = 0; j + 1 < H; ++j) {\n        double hj = h_bf16 ? oracle_round_bf16(h_row[j]) : h_row[j];\n        ssq"),
     ("rounding quantum off by one", "int q = e - 8;", "int q = e - 9;"),
+    ("shared gate dropped", "double s = g * bf16_bits_to_double(S[r][t * H + j]);",
+     "double s = bf16_bits_to_double(S[r][t * H + j]);"),
+    ("shared gate sign flipped", "1.0 / (1.0 + exp(-(double)gate[t]))", "1.0 / (1.0 + exp((double)gate[t]))"),
 ]
 
 PINS = [
@@ -43,6 +46,8 @@ PINS = [
     pins.test_gemma_weight_bias_equivalence,
     pins.test_shared_partial_counted_once_per_rank,
     pins.test_round_bf16_matches_fp32_to_bf16_for_fp32_values,
+    lambda: [pins.test_gated_brute_force_2x4(R, K) for R, K in ((1, 1), (2, 2), (2, 0))],
+    pins.test_gate_scales_only_the_shared_term,
 ]
 
 
