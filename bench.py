@@ -77,6 +77,9 @@ def parse():
     p.add_argument("--regime", default="auto",
                    help="force a kernel regime for the timed call: auto, cluster, stream, "
                         "oneshot or c<N> (cluster regime with N CTAs per row)")
+    p.add_argument("--gated", action="store_true",
+                   help="time the gated shared-expert variant (shared partials scaled by a "
+                        "per-token sigmoid gate)")
     p.add_argument("--stage-bytes", type=int, default=0,
                    help="target ring-slot bytes of the streaming kernels (0 = automatic)")
     p.add_argument("--sweep-regimes", default="auto",
@@ -315,6 +318,11 @@ def main_ours(args):
     r_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    gate = None
+    if args.gated:
+        from gen import make_gate_logits
+        gate = make_gate_logits(T, device=dev)
+
     def step():
         if K == 0:
             arf.ar_rmsnorm(ws, d["S"], d["residual"], d["gamma"], d["weight_bias"], d["eps"],
@@ -322,7 +330,7 @@ def main_ours(args):
         else:
             arf.ar_finalize_rmsnorm(ws, d["E"], d["perm"], d["w"], d["S"], d["residual"], d["gamma"],
                                     d["weight_bias"], d["eps"], out=out, residual_out=r_out,
-                                    stream=stream)
+                                    stream=stream, shared_gate=gate)
 
     for _ in range(args.warmup):
         step()
@@ -382,7 +390,8 @@ def main_ours(args):
     sweep = None
     if not args.no_sweep and rank == 0:
         sweep = run_sweep(arf, torch, dev, stream, peak, args.sweep_regimes.split(","),
-                          [w for w in args.sweep_only.split(",") if w], args.sweep_mode)
+                          [w for w in args.sweep_only.split(",") if w], args.sweep_mode,
+                          gated=args.gated)
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
@@ -398,7 +407,7 @@ def main_ours(args):
                 "data": "synthetic",
                 "config": headline_config(args.workload, T, world),
                 "us_per_call": round(1e3 * ms_per_step, 3),
-                "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas,
+                "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas, "gated": bool(args.gated),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps, "clocks": clocks.summary(), "sweep": sweep}
         print(json.dumps(line), flush=True)
@@ -469,7 +478,8 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
             "api": "tp_reduce_moe_gb300.ar_finalize_rmsnorm"}
 
 
-def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate"):
+def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate",
+              gated=False):
     """µs/call vs T for every workload: L2-cold by rotating through disjoint
     input sets (>= 3x L2 in total; each set gathers only within its own block
     of expert rows, like successive layers), timed by replaying a CUDA graph
@@ -486,13 +496,15 @@ def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="r
                 continue
             for regime_name in regimes:
                 res.append(sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T,
-                                       *parse_regime(regime_name), mode=mode))
+                                       *parse_regime(regime_name), mode=mode,
+                                       gated=gated and cfg.K > 0))
     return res
 
 
-def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0, mode="rotate"):
+def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0, mode="rotate",
+                gated=False):
     """One (workload, T, regime) point of the sweep."""
-    from gen import make_inputs, problem_bytes
+    from gen import make_gate_logits, make_inputs, problem_bytes
     b = problem_bytes(cfg.R, cfg.K, cfg.H, T)
     n_sets = int(min(8192, max(2, math.ceil(3 * l2 / b))))
     if mode == "warm":
@@ -504,6 +516,7 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
     arf.ar_workspace_set_cluster_size(ws, csize)
     outs = torch.empty((n_sets, T, cfg.H), dtype=torch.bfloat16, device=dev)
     routs = torch.empty((n_sets, T, cfg.H), dtype=torch.bfloat16, device=dev)
+    gates = make_gate_logits(T * n_sets, device=dev) if gated else None
 
     def call(i, st):
         sl = slice(i * T, (i + 1) * T)
@@ -515,7 +528,8 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
             arf.ar_finalize_rmsnorm(ws, big["E"], big["perm"][sl], big["w"][sl], S,
                                     big["residual"][sl], big["gamma"], 0.0, cfg.eps,
                                     out=outs[i], residual_out=routs[i], stream=st,
-                                    rows_e=big["rows_e"])
+                                    rows_e=big["rows_e"],
+                                    shared_gate=gates[sl] if gates is not None else None)
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
@@ -553,7 +567,8 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
             "us_per_call": round(us, 3), "GBps": round(gbs, 1),
             "frac_of_hbm_peak": round(gbs / peak, 4),
             "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas,
-            "forced": force != 0, "calls_per_graph": n_sets, "mode": mode, "device_error": err}
+            "forced": force != 0, "calls_per_graph": n_sets, "mode": mode, "gated": gated,
+            "device_error": err}
 
 
 def main():

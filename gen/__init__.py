@@ -36,7 +36,7 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = ["CONFIGS", "Config", "make_inputs", "make_perm_decode_inputs",
-           "bf16_bits", "problem_bytes"]
+           "make_gate_logits", "bf16_bits", "problem_bytes"]
 
 
 @dataclass(frozen=True)
@@ -177,6 +177,12 @@ def make_inputs(cfg, T: int, seed: int | None = None, device="cpu",
     return dict(cfg=cfg, R=R, K=K, H=H, T=T, rows_e=rows_e, eps=cfg.eps,
                 weight_bias=cfg.weight_bias, E=E, perm=perm, w=w, S=S,
                 residual=residual, gamma=gamma)
+
+
+def make_gate_logits(T: int, seed: int = 4242, device="cpu", sigma: float = 2.0):
+    """Shared-expert gate logits, fp32 [T] ~ N(0, sigma) (sigmoid spans ~0.02..0.98)."""
+    g = _gen(seed, device)
+    return (torch.randn((T,), generator=g, device=device) * sigma).contiguous()
 
 
 def hex_digits_needed(rows: int) -> int:

@@ -81,7 +81,9 @@ typedef enum ar_status {
 } ar_status;
 
 /* ar_workspace_create() flags. */
-#define AR_WS_DRY_RUN 0x1u   /* no GPU state: calls validate, then return AR_VALIDATED */
+#define AR_WS_DRY_RUN 0x1u      /* no GPU state: calls validate, then return AR_VALIDATED   */
+#define AR_WS_NORM_BF16_H 0x2u  /* the norm reads h rounded to bf16, as a bf16 residual_out  */
+                                /* stores it (default: the unrounded fp32 sum)              */
 
 /* Bits of the device error word (ar_workspace_device_error). */
 #define AR_DEVERR_PERM_RANGE 0x1   /* some perm value was outside [0, rows_e); clamped */
@@ -109,7 +111,7 @@ typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
  *   hidden      8 .. AR_MAX_HIDDEN, a multiple of 8
  *   max_tokens  largest T any call may pass (>= 1)
  *   eps         RMSNorm epsilon every call must repeat
- *   flags       0 or AR_WS_DRY_RUN
+ *   flags       0, or AR_WS_DRY_RUN and/or AR_WS_NORM_BF16_H
  *   out         host pointer that receives the handle (set to NULL on error)
  * Errors: AR_ERR_INVALID_ARG (out NULL, max_tokens < 1, eps < 0 or not
  * finite), AR_ERR_ALIGNMENT (hidden % 8), AR_ERR_UNSUPPORTED (limits above,
@@ -163,6 +165,28 @@ ARFUSE_API ar_status ar_finalize_rmsnorm(ar_workspace* ws,
                                          int64_t T, int R, int K, int H,
                                          void* out, void* residual_out,
                                          int residual_out_is_fp32, void* stream);
+
+/*
+ * The fused op with a gated shared expert: as ar_finalize_rmsnorm, except that
+ * each rank's shared partial of token t is scaled by sigmoid(shared_gate[t])
+ * before the add (the Qwen-style shared expert carries such a per-token gate,
+ * while the DeepSeek-V3 one adds unmodified: sglang PR #37196, Modifications
+ * section 2).
+ *   shared_gate  device fp32 [T] gate logits (4-byte aligned), required
+ *   shared_out   required (a gate needs a shared term)
+ * Errors as for ar_finalize_rmsnorm; a NULL shared_gate or shared_out is
+ * AR_ERR_INVALID_ARG.
+ */
+ARFUSE_API ar_status ar_finalize_rmsnorm_gated(ar_workspace* ws,
+                                               const void* const* expert_out, int64_t rows_e,
+                                               const int32_t* perm, const float* topk_w,
+                                               const void* const* shared_out,
+                                               const float* shared_gate,
+                                               const void* residual, const void* gamma,
+                                               float weight_bias, float eps,
+                                               int64_t T, int R, int K, int H,
+                                               void* out, void* residual_out,
+                                               int residual_out_is_fp32, void* stream);
 
 /*
  * Trailing all-reduce + residual RMSNorm without a MoE term (the K = 0 form):

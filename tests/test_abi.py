@@ -285,3 +285,34 @@ def test_binding_checks_shapes(lib, ws):
     with pytest.raises(TypeError):
         arf.ar_finalize_rmsnorm(ws, E, torch.zeros(4, 2, dtype=torch.int64), x(4, 2, dt=torch.float32),
                                 None, x(4, H), x(H), 0.0, EPS)
+
+
+# ------------------------------------------------------------ gated shared expert
+def _gated(lib, ws, f, gate, **over):
+    a = dict(E=f.E, rows_e=f.rows_e, perm=f.perm, w=f.w, S=f.S, res=f.res, gamma=f.gamma, T=f.T,
+             R=R, K=K, H=H, out=f.out, rout=f.rout, f32=0)
+    a.update(over)
+    E = ctypes.cast((ctypes.c_void_p * len(a["E"]))(*a["E"]), ctypes.c_void_p)
+    S = ctypes.cast((ctypes.c_void_p * len(a["S"]))(*a["S"]), ctypes.c_void_p) if a["S"] else None
+    return lib.ar_finalize_rmsnorm_gated(ctypes.c_void_p(ws.handle), E, a["rows_e"], a["perm"], a["w"],
+                                         S, gate, a["res"], a["gamma"], 0.0, EPS, a["T"], a["R"], a["K"],
+                                         a["H"], a["out"], a["rout"], a["f32"], None)
+
+
+def test_gated_validation(lib, ws):
+    f = Fake()
+    gate = BASE + 40 * MB
+    assert _gated(lib, ws, f, gate) == arf.AR_VALIDATED
+    assert _gated(lib, ws, f, None) == arf.AR_ERR_INVALID_ARG           # gate required
+    assert _gated(lib, ws, f, gate, S=None) == arf.AR_ERR_INVALID_ARG   # shared term required
+    assert _gated(lib, ws, f, gate + 2) == arf.AR_ERR_ALIGNMENT
+    assert _gated(lib, ws, f, f.out) == arf.AR_ERR_INVALID_ARG          # overlaps an output
+    assert _gated(lib, ws, f, gate, T=0, res=None) == arf.AR_OK
+
+
+def test_norm_bf16_h_flag_is_accepted(lib):
+    w = arf.ar_workspace_create(R, K, H, TMAX, EPS, flags=arf.AR_WS_DRY_RUN | arf.AR_WS_NORM_BF16_H)
+    try:
+        assert Fake().call(lib, w) == arf.AR_VALIDATED
+    finally:
+        w.destroy()

@@ -395,3 +395,56 @@ def test_every_cluster_size(cfg, T):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+# ------------------------------------- gated shared expert (Qwen-style shared gate)
+@pytest.mark.parametrize("cfg,T", [("tiny", 4), ("dsv3_decode", 4), ("glm_gemma", 16),
+                                   ("dsv3_decode", 128), ("prefill", 512)])
+def test_gated_shared_expert(cfg, T):
+    from gen import make_gate_logits
+    inp = make_inputs(cfg, T)
+    gate = make_gate_logits(T)
+    a = oracle_args(inp)
+    ref = oracle.ar_finalize_rmsnorm_ref(a["E"], a["perm"], a["w"], a["S"], a["residual"], a["gamma"],
+                                         a["weight_bias"], a["eps"], want_abs=True,
+                                         shared_gate=gate.numpy())
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        g = gate.to(DEV)
+        for regime in KERNELS:
+            for fp32 in (False, True):
+                out, r_out = run_gpu(ws, d, fp32=fp32, regime=regime, shared_gate=g)
+                torch.cuda.synchronize()
+                tag = f"gated {cfg} T={T} regime={regime} fp32={fp32}"
+                check_bf16(out, ref["out"], tag + " out")
+                if fp32:
+                    check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+                else:
+                    check_bf16(r_out, ref["h"], tag + " residual_out")
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
+
+
+# -------------------------------- the norm of bf16-rounded h (workspace flag)
+@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 16), ("ar_only", 8), ("prefill", 512)])
+def test_norm_reads_bf16_h(cfg, T):
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True, h_bf16_before_norm=True)
+    ws = arf.ar_workspace_create(inp["R"], inp["K"], inp["H"], T, inp["eps"], device=0,
+                                 flags=arf.AR_WS_NORM_BF16_H)
+    plain = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        for regime in KERNELS:
+            out, r_out = run_gpu(ws, d, fp32=True, regime=regime)
+            out0, _ = run_gpu(plain, d, fp32=True, regime=regime)
+            torch.cuda.synchronize()
+            check_bf16(out, ref["out"], f"bf16-h {cfg} T={T} regime={regime} out")
+            check_f32(r_out, ref["h"], ref["abs"], f"bf16-h {cfg} T={T} regime={regime} residual_out")
+            assert not torch.equal(out, out0)          # the flag changes the result ...
+            assert (out.float() - out0.float()).abs().max().item() < 0.05   # ... within a few ulps
+    finally:
+        ws.destroy()
+        plain.destroy()

@@ -28,6 +28,7 @@ AR_ERR_DEVICE_CHECK = 6
 AR_VALIDATED = 7
 
 AR_WS_DRY_RUN = 0x1
+AR_WS_NORM_BF16_H = 0x2
 AR_DEVERR_PERM_RANGE = 0x1
 AR_DEVERR_TIMEOUT = 0x2
 AR_REGIME_AUTO = 0
@@ -71,6 +72,9 @@ def load_library(path: str | None = None):
         lib.ar_finalize_rmsnorm.restype = I
         lib.ar_finalize_rmsnorm.argtypes = [P, P, I64, P, P, P, P, P, F, F, I64, I, I, I,
                                             P, P, I, P]
+        lib.ar_finalize_rmsnorm_gated.restype = I
+        lib.ar_finalize_rmsnorm_gated.argtypes = [P, P, I64, P, P, P, P, P, P, F, F, I64, I, I, I,
+                                                  P, P, I, P]
         lib.ar_rmsnorm.restype = I
         lib.ar_rmsnorm.argtypes = [P, P, I, P, P, F, F, I64, I, P, P, I, P]
         lib.ar_workspace_device_error.restype = I
@@ -206,14 +210,15 @@ def _stream_handle(stream, device) -> int:
 def ar_finalize_rmsnorm(ws: Workspace, expert_out, perm, topk_w, shared_out, residual, gamma,
                         weight_bias: float, eps: float, out=None, residual_out=None,
                         residual_out_fp32: bool = False, stream=None, rows_e: int | None = None,
-                        T: int | None = None):
+                        T: int | None = None, shared_gate=None):
     """Fused MoE finalize + shared add + rank sum + residual + RMSNorm.
 
     expert_out: list of R bf16 [rows_e, H] tensors; perm int32 [T, K]; topk_w
     fp32 [T, K]; shared_out: list of R bf16 [T, H] or None; residual bf16
-    [T, H]; gamma bf16 [H].  Returns (out, residual_out); outputs are
-    allocated when not given.  ``residual_out`` may be ``residual`` (in place,
-    bf16 only).
+    [T, H]; gamma bf16 [H].  shared_gate: optional fp32 [T] gate logits (calls
+    ar_finalize_rmsnorm_gated: shared partials scaled by sigmoid(gate[t])).
+    Returns (out, residual_out); outputs are allocated when not given.
+    ``residual_out`` may be ``residual`` (in place, bf16 only).
     """
     R, K, H = ws.R, ws.K, ws.H
     if T is None:
@@ -236,6 +241,8 @@ def ar_finalize_rmsnorm(ws: Workspace, expert_out, perm, topk_w, shared_out, res
             _need(s, torch.bfloat16, (T, H), f"shared_out[{r}]")
     _need(residual, torch.bfloat16, (T, H), "residual")
     _need(gamma, torch.bfloat16, (H,), "gamma")
+    if shared_gate is not None:
+        _need(shared_gate, torch.float32, (T,), "shared_gate")
     dev = residual.device if not isinstance(residual, int) else None
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -247,14 +254,21 @@ def ar_finalize_rmsnorm(ws: Workspace, expert_out, perm, topk_w, shared_out, res
           "residual_out")
     e_arr = _ptr_array(expert_out) if K > 0 else None
     s_arr = _ptr_array(shared_out) if shared_out is not None else None
-    st = load_library().ar_finalize_rmsnorm(
-        ctypes.c_void_p(ws.handle), ctypes.cast(e_arr, ctypes.c_void_p) if e_arr is not None else None,
-        int(rows_e), _ptr(perm) if K > 0 else None, _ptr(topk_w) if K > 0 else None,
-        ctypes.cast(s_arr, ctypes.c_void_p) if s_arr is not None else None,
-        _ptr(residual), _ptr(gamma), float(weight_bias), float(eps), int(T), int(R), int(K), int(H),
-        _ptr(out), _ptr(residual_out), 1 if residual_out_fp32 else 0,
-        _stream_handle(stream, dev) if not ws.dry_run else None)
-    _check(st, "ar_finalize_rmsnorm", ok=(AR_OK, AR_VALIDATED) if ws.dry_run else (AR_OK,))
+    head = (ctypes.c_void_p(ws.handle),
+            ctypes.cast(e_arr, ctypes.c_void_p) if e_arr is not None else None,
+            int(rows_e), _ptr(perm) if K > 0 else None, _ptr(topk_w) if K > 0 else None,
+            ctypes.cast(s_arr, ctypes.c_void_p) if s_arr is not None else None)
+    tail = (_ptr(residual), _ptr(gamma), float(weight_bias), float(eps), int(T), int(R), int(K),
+            int(H), _ptr(out), _ptr(residual_out), 1 if residual_out_fp32 else 0,
+            _stream_handle(stream, dev) if not ws.dry_run else None)
+    lib = load_library()
+    if shared_gate is not None:
+        st = lib.ar_finalize_rmsnorm_gated(*head, _ptr(shared_gate), *tail)
+        where = "ar_finalize_rmsnorm_gated"
+    else:
+        st = lib.ar_finalize_rmsnorm(*head, *tail)
+        where = "ar_finalize_rmsnorm"
+    _check(st, where, ok=(AR_OK, AR_VALIDATED) if ws.dry_run else (AR_OK,))
     return out, residual_out
 
 

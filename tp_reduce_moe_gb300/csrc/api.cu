@@ -57,7 +57,8 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.
 ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int32_t* perm,
               const float* w, const void* const* S, const void* residual, const void* gamma,
               float weight_bias, float eps, int64_t T, int R, int K, int H, void* out,
-              void* residual_out, int res_f32, void* stream, bool routed_call) {
+              void* residual_out, int res_f32, void* stream, bool routed_call,
+              const float* gate = nullptr) {
     if (!ws) return AR_ERR_INVALID_ARG;
     if (R != ws->R || H != ws->H) return AR_ERR_INVALID_ARG;
     if (routed_call && K != ws->K) return AR_ERR_INVALID_ARG;
@@ -90,6 +91,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     if (S)
         for (int r = 0; r < R; ++r)
             if (!aligned(S[r], 16)) return AR_ERR_ALIGNMENT;
+    if (gate && !aligned(gate, 4)) return AR_ERR_ALIGNMENT;
 
     // Outputs must not overlap each other or an input (the exact bf16 in-place
     // residual alias excepted).
@@ -98,7 +100,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     const Range r_rout = range_of(residual_out, res_f32 ? 2 * row2 : row2);
     const bool inplace = (residual_out == residual) && !res_f32;
     if (overlap(r_out, r_rout)) return AR_ERR_INVALID_ARG;
-    Range ins[2 * AR_MAX_RANKS + 4];
+    Range ins[2 * AR_MAX_RANKS + 5];
     int n_in = 0;
     ins[n_in++] = range_of(gamma, (int64_t)H * 2);
     if (K > 0) {
@@ -108,6 +110,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     }
     if (S)
         for (int r = 0; r < R; ++r) ins[n_in++] = range_of(S[r], row2);
+    if (gate) ins[n_in++] = range_of(gate, T * 4);
     for (int i = 0; i < n_in; ++i)
         if (overlap(r_out, ins[i]) || overlap(r_rout, ins[i])) return AR_ERR_INVALID_ARG;
     const Range r_res = range_of(residual, row2);
@@ -174,6 +177,8 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     a.K = K;
     a.H = H;
     a.has_shared = S ? 1 : 0;
+    a.shared_gate = gate;
+    a.norm_bf16_h = (ws->flags & AR_WS_NORM_BF16_H) ? 1 : 0;
     a.weight_bias = weight_bias;
     a.eps = eps;
 
@@ -205,7 +210,7 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
     if (!out) return AR_ERR_INVALID_ARG;
     *out = nullptr;
     if (max_tokens < 1 || !(eps >= 0.0f) || eps > 3.0e38f) return AR_ERR_INVALID_ARG;
-    if ((flags & ~AR_WS_DRY_RUN) != 0) return AR_ERR_INVALID_ARG;
+    if ((flags & ~(AR_WS_DRY_RUN | AR_WS_NORM_BF16_H)) != 0) return AR_ERR_INVALID_ARG;
     if (hidden < 8 || hidden % 8 != 0) return hidden < 8 ? AR_ERR_UNSUPPORTED : AR_ERR_ALIGNMENT;
     if (ranks < 1 || ranks > AR_MAX_RANKS || top_k < 0 || top_k > AR_MAX_TOP_K ||
         hidden > AR_MAX_HIDDEN || max_tokens > kMaxTokensLimit)
@@ -312,6 +317,19 @@ ar_status ar_finalize_rmsnorm(ar_workspace* ws, const void* const* expert_out, i
     if (K < 0 || K > AR_MAX_TOP_K || R < 1 || R > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
     return run(ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma, weight_bias, eps,
                T, R, K, H, out, residual_out, residual_out_is_fp32, stream, true);
+}
+
+ar_status ar_finalize_rmsnorm_gated(ar_workspace* ws, const void* const* expert_out,
+                                    int64_t rows_e, const int32_t* perm, const float* topk_w,
+                                    const void* const* shared_out, const float* shared_gate,
+                                    const void* residual, const void* gamma, float weight_bias,
+                                    float eps, int64_t T, int R, int K, int H, void* out,
+                                    void* residual_out, int residual_out_is_fp32, void* stream) {
+    if (K < 0 || K > AR_MAX_TOP_K || R < 1 || R > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (T > 0 && (!shared_gate || !shared_out)) return AR_ERR_INVALID_ARG;
+    return run(ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma, weight_bias, eps,
+               T, R, K, H, out, residual_out, residual_out_is_fp32, stream, true, shared_gate);
 }
 
 ar_status ar_rmsnorm(ar_workspace* ws, const void* const* partials, int R, const void* residual,

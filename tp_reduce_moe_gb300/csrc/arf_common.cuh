@@ -31,6 +31,7 @@ struct RowArgs {
     const uint16_t* S[kMaxRanks];  // bf16 [T, H] per rank (has_shared)
     const int32_t* perm;           // [T, K] gather rows into E
     const float* w;                // [T, K] routing weights
+    const float* shared_gate;      // [T] gate logits, or nullptr: S scaled by sigmoid(gate[t])
     const uint16_t* residual;      // bf16 [T, H]
     const uint16_t* gamma;         // bf16 [H]
     void* out;                     // bf16 [T, H]
@@ -40,9 +41,21 @@ struct RowArgs {
     int64_t rows_e;
     int R, K, H;
     int has_shared;
+    int norm_bf16_h;               // the norm reads h rounded to bf16 (as a bf16 residual_out stores it)
     float weight_bias;
     float eps;
 };
+
+// Coefficient of the shared partials of row t: sigmoid of the row's gate
+// logit for a gated shared expert, else 1.
+__device__ __forceinline__ float shared_coef(const RowArgs& a, int64_t t) {
+    return a.shared_gate ? 1.0f / (1.0f + expf(-__ldg(a.shared_gate + t))) : 1.0f;
+}
+
+// h as the norm reads it: unrounded, or rounded to bf16 (round to nearest even).
+__device__ __forceinline__ float norm_input(float h, int bf16) {
+    return bf16 ? __bfloat162float(__float2bfloat16_rn(h)) : h;
+}
 
 // ------------------------------------------------------------------ bf16 data
 // A bf16 value is the top half of an IEEE binary32 word, so widening is a

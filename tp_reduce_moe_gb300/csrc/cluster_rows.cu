@@ -59,12 +59,13 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
     // Pass 1: loads that do not depend on the routing metadata.
     uint4 v[kClusterMaxTerms];
     float coef[kClusterMaxTerms];
+    const float s_coef = shared_coef(a, t);
 #pragma unroll
     for (int m = 0; m < kClusterMaxTerms; ++m) {
         const int q = g + m * G;
         if (q < nS && q < NT) {
             v[m] = ld_stream16(a.S[q] + rowoff);
-            coef[m] = 1.0f;
+            coef[m] = s_coef;
         }
     }
     uint4 res = make_uint4(0, 0, 0, 0);
@@ -117,11 +118,13 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
         float rf[8];
         bf16x8_to_f32(res, rf);
 #pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = acc[j] + rf[j];
+        store_residual8<RES_F32>(a.residual_out, rowoff, h);
+#pragma unroll
         for (int j = 0; j < 8; ++j) {
-            h[j] = acc[j] + rf[j];
+            h[j] = norm_input(h[j], a.norm_bf16_h);
             ss = fmaf(h[j], h[j], ss);
         }
-        store_residual8<RES_F32>(a.residual_out, rowoff, h);
     }
 
     // Row sum of squares: warps -> CTA -> cluster (fixed order everywhere,

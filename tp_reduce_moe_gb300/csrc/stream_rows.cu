@@ -138,13 +138,17 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         // being issued and has the next row's value in flight.
         int32_t raw_next = 0;
         float w_next = 0.0f;
+        float gate_next = 0.0f;
         if (lane < a.K && first_row < a.T) {
             raw_next = __ldg(a.perm + first_row * a.K + lane);
             w_next = __ldg(a.w + first_row * a.K + lane);
         }
+        if (a.shared_gate && first_row < a.T) gate_next = __ldg(a.shared_gate + first_row);
         for (int64_t t = first_row; t < a.T && ok; t += row_step) {
             const int32_t raw = raw_next;
             const float my_w = w_next;
+            const float s_coef = a.shared_gate ? 1.0f / (1.0f + expf(-gate_next)) : 1.0f;
+            if (a.shared_gate && t + row_step < a.T) gate_next = __ldg(a.shared_gate + t + row_step);
             int64_t my_row = -1;  // checked lazily, at the first routed stage
             for (int j = 0; j < nstage_row && ok; ++j) {
                 int s0, cnt;
@@ -183,7 +187,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
                     uint8_t* sbase = ring + (size_t)slot * geo.slot_bytes;
                     // Coefficients into the slot header (published by the
                     // same mbarrier phase as the data).
-                    if (lane < cnt) reinterpret_cast<float*>(sbase)[lane] = e < 0 ? 1.0f : w_k;
+                    if (lane < cnt)
+                        reinterpret_cast<float*>(sbase)[lane] = e >= 0 ? w_k : (s < nS ? s_coef : 1.0f);
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive_expect_tx(smem_addr(&full[slot]), (uint32_t)cnt * tile_bytes);
@@ -300,9 +305,12 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
 #pragma unroll
         for (int m = 0; m < CPT; ++m) {
             if (valid[m]) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) ss = fmaf(acc[m][j], acc[m][j], ss);
                 store_residual8<RES_F32>(a.residual_out, t * H + (int64_t)(chunk0 + lch[m]) * 8, acc[m]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    acc[m][j] = norm_input(acc[m][j], a.norm_bf16_h);
+                    ss = fmaf(acc[m][j], acc[m][j], ss);
+                }
             }
         }
         ss = warp_sum(ss);
