@@ -448,3 +448,19 @@ def test_norm_reads_bf16_h(cfg, T):
     finally:
         ws.destroy()
         plain.destroy()
+
+
+def test_results_are_bitwise_reproducible():
+    """Fixed summation order: repeated calls give identical bits, per kernel."""
+    inp = make_inputs("dsv3_decode", 64)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        for regime in KERNELS:
+            first = run_gpu(ws, d, regime=regime)
+            for _ in range(3):
+                again = run_gpu(ws, d, regime=regime)
+                torch.cuda.synchronize()
+                assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+    finally:
+        ws.destroy()
