@@ -45,14 +45,17 @@ METRIC = "µs/call and achieved HBM GB/s (% of GB300 roofline) vs tokens T, 1 GP
 UNIT = "GB/s"
 HEADLINE = ("prefill", 8192)
 FALLBACK_HBM_GBS = 6800.0
-REGIMES = {"auto": 0, "cluster": 1, "stream": 2, "oneshot": 3}
-REGIME_NAMES = {1: "cluster", 2: "stream", 3: "oneshot"}
+REGIMES = {"auto": 0, "cluster": 1, "stream": 2, "oneshot": 3, "split": 4}
+REGIME_NAMES = {1: "cluster", 2: "stream", 3: "oneshot", 4: "split"}
 
 
 def parse_regime(tok: str):
-    """'auto' | 'cluster' | 'stream' | 'oneshot' | 'c<N>' (cluster regime, N CTAs per row)."""
+    """'auto' | 'cluster' | 'stream' | 'oneshot' | 'split' | 'c<N>' (cluster regime, N CTAs
+    per row) | 's<N>' (split regime, N CTAs per row)."""
     if tok.startswith("c") and tok[1:].isdigit():
         return REGIMES["cluster"], int(tok[1:])
+    if tok.startswith("s") and tok[1:].isdigit():
+        return REGIMES["split"], int(tok[1:])
     return REGIMES[tok], 0
 CPU_SAMPLE_T = 512
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "stream_rows_prefill_traffic.json")
@@ -533,9 +536,14 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
-    with torch.cuda.stream(side):
-        for i in range(min(n_sets, 8)):
-            call(i, side)
+    try:
+        with torch.cuda.stream(side):
+            for i in range(min(n_sets, 8)):
+                call(i, side)
+    except arf.ArfuseError as e:  # a forced regime with no plan for this shape
+        ws.destroy()
+        return {"workload": name, "T": T, "regime": REGIME_NAMES.get(force, "auto"), "ctas": csize,
+                "forced": True, "unsupported": arf.ar_status_string(e.status)}
     torch.cuda.current_stream(dev).wait_stream(side)
     torch.cuda.synchronize()
     regime, ctas = arf.ar_workspace_last_regime(ws)

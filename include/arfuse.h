@@ -97,6 +97,9 @@ typedef enum ar_status {
 #define AR_REGIME_STREAM 2   /* large T: persistent CTAs, whole rows through the ring     */
 #define AR_REGIME_ONESHOT 3  /* one cluster per row, every load in flight at once from    */
                              /* registers, no pipeline (latency-optimal for tiny rows)    */
+#define AR_REGIME_SPLIT 4    /* small T: one cluster per row, the row's segments dealt    */
+                             /* to its C CTAs, partial rows reduce-scattered through      */
+                             /* distributed shared memory (fewest copies per CTA)         */
 
 typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
 
@@ -219,7 +222,7 @@ ARFUSE_API ar_status ar_workspace_set_regime(ar_workspace* ws, int regime);
 
 /*
  * Force the number of CTAs per token row (the cluster size C, 2..16) that
- * AR_REGIME_CLUSTER uses; 0 restores the automatic choice.  A size that
+ * AR_REGIME_CLUSTER and AR_REGIME_SPLIT use; 0 restores the automatic choice.  A size that
  * cannot be launched for a call makes that call return AR_ERR_UNSUPPORTED.
  */
 ARFUSE_API ar_status ar_workspace_set_cluster_size(ar_workspace* ws, int ctas_per_row);
@@ -234,9 +237,9 @@ ARFUSE_API ar_status ar_workspace_set_cluster_size(ar_workspace* ws, int ctas_pe
  */
 ARFUSE_API ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes);
 
-/* Regime (AR_REGIME_CLUSTER / AR_REGIME_STREAM / AR_REGIME_ONESHOT) of the
- * last launched call, 0 before the first one.  *ctas receives the CTAs per
- * row (cluster and one-shot regimes) or the persistent grid size (stream
+/* Regime (AR_REGIME_CLUSTER / _STREAM / _ONESHOT / _SPLIT) of the last
+ * launched call, 0 before the first one.  *ctas receives the CTAs per row
+ * (cluster, one-shot and split regimes) or the persistent grid size (stream
  * regime); may be NULL. */
 ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
 

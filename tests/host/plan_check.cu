@@ -6,6 +6,7 @@
 // segments and their coefficient header, and that a slot's bytes fit an
 // mbarrier transaction count.  The automatic plan must exist for every shape.
 #include "stream_rows.cu"
+#include "split_rows.cu"
 #include <cstdio>
 #include <cstdlib>
 using namespace arf;
@@ -58,6 +59,31 @@ int main() {
       // ring positions: q in [0, 2n) maps to a slot < n
       for (int q = 0; q < 2 * g.nstages; ++q) { int sl = q >= g.nstages ? q - g.nstages : q; if (sl < 0 || sl >= g.nstages) bad = true; }
       if (bad) { ++fails; if (fails < 20) printf("BAD H=%d R=%d K=%d sh=%d T=%ld Cf=%d -> C=%d tile=%d nst=%d slot=%d thr=%d smem=%d grid=%d\n", H,R,K,sh,T,Cf,C,g.tile_chunks,g.nstages,g.slot_bytes,p.threads,p.smem,p.grid); }
+    }
+  }
+  // split plans (one row per cluster, segments dealt round-robin)
+  for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts) {
+    if (K == 0 && !sh) continue;
+    for (int Cf = 0; Cf <= 16; Cf = Cf ? Cf * 2 : 2) {
+      SplitPlan p;
+      if (!plan_split_rows(R, K, H, sh, T, 152, 232448, 16, Cf, &p)) continue;
+      ++checks;
+      const auto& g = p.geo;
+      const int chunks = H / 8, nseg = (sh ? R : 0) + 1 + R * K, C = g.C;
+      bool bad = false;
+      if (p.smem > 232448 || p.grid != T * C || p.threads > 544 || p.threads % 32) bad = true;
+      const int consumers = p.threads - 32;
+      if ((long)consumers * p.cpt < chunks) bad = true;       // partial row fully covered
+      if (2 * g.tile_chunks > p.cpt * consumers) bad = true;  // <= CPT float4 items per thread
+      if (g.seg_stride < H * 2 || g.seg_stride % 128 || g.part_bytes < H * 4) bad = true;
+      for (int c = 0; c < C; ++c) {
+        const int ns = (nseg - c + C - 1) / C;
+        if (ns < 1 || ns > 32) bad = true;
+        if (1024 + g.part_bytes + (long)ns * g.seg_stride > p.smem) bad = true;
+        if ((long)ns * H * 2 >= (1 << 20)) bad = true;        // mbarrier transaction count
+        if (std::min(g.tile_chunks, chunks - c * g.tile_chunks) < 1) bad = true;
+      }
+      if (bad) { ++fails; if (fails < 20) printf("BAD split H=%d R=%d K=%d sh=%d T=%ld Cf=%d\n", H, R, K, sh, T, Cf); }
     }
   }
   // show the automatic plans for the workloads

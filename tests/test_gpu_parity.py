@@ -19,8 +19,11 @@ from tests._util import check_bf16, check_f32, oracle_args, run_oracle
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-REGIMES = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_ONESHOT, arf.AR_REGIME_AUTO)
-KERNELS = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_ONESHOT)
+REGIMES = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_ONESHOT, arf.AR_REGIME_SPLIT,
+           arf.AR_REGIME_AUTO)
+KERNELS = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_ONESHOT, arf.AR_REGIME_SPLIT)
+# Regimes that split a row over several CTAs cannot run a row of one 16-byte chunk.
+SPLITTING = (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_SPLIT)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -60,7 +63,7 @@ def run_gpu(ws, d, fp32=False, regime=arf.AR_REGIME_AUTO, **kw):
 def check_all(ws, d, ref, what, regimes=REGIMES, fp32s=(False, True)):
     for regime in regimes:
         for fp32 in fp32s:
-            if regime == arf.AR_REGIME_CLUSTER and d["H"] // 8 < 2:
+            if regime in SPLITTING and d["H"] // 8 < 2:
                 with pytest.raises(arf.ArfuseError) as e:   # one chunk cannot be split
                     run_gpu(ws, d, fp32=fp32, regime=regime)
                 assert e.value.status == arf.AR_ERR_UNSUPPORTED
@@ -462,5 +465,37 @@ def test_results_are_bitwise_reproducible():
                 again = run_gpu(ws, d, regime=regime)
                 torch.cuda.synchronize()
                 assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+    finally:
+        ws.destroy()
+
+
+
+@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 4), ("glm_gemma", 16), ("prefill", 3), ("ar_only", 5),
+                                   ("tiny", 4)])
+def test_every_split_cluster_size(cfg, T):
+    """The split regime at every cluster size whose plan fits shared memory; a
+    size that does not fit is a clean AR_ERR_UNSUPPORTED."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    ran = 0
+    try:
+        d = to_dev(inp)
+        for c in (2, 4, 8, 16):
+            arf.ar_workspace_set_cluster_size(ws, c)
+            for fp32 in (False, True):
+                try:
+                    out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_SPLIT)
+                except arf.ArfuseError as e:
+                    assert e.status == arf.AR_ERR_UNSUPPORTED
+                    continue
+                torch.cuda.synchronize()
+                ran += 1
+                assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_SPLIT, c)
+                check_bf16(out, ref["out"], f"split {cfg} T={T} C={c} out")
+                if fp32:
+                    check_f32(r_out, ref["h"], ref["abs"], f"split {cfg} T={T} C={c} residual_out")
+        assert ran >= 2
+        assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()

@@ -9,7 +9,7 @@ Python binding of that library (argument marshalling only) and its build step.
 from .binding import (  # noqa: F401
     AR_DEVERR_PERM_RANGE, AR_DEVERR_TIMEOUT, AR_ERR_ALIGNMENT, AR_ERR_CAPACITY, AR_ERR_CUDA,
     AR_ERR_DEVICE_CHECK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_MAX_HIDDEN, AR_MAX_RANKS,
-    AR_MAX_TOP_K, AR_OK, AR_REGIME_AUTO, AR_REGIME_CLUSTER, AR_REGIME_ONESHOT, AR_REGIME_STREAM,
+    AR_MAX_TOP_K, AR_OK, AR_REGIME_AUTO, AR_REGIME_CLUSTER, AR_REGIME_ONESHOT, AR_REGIME_SPLIT, AR_REGIME_STREAM,
     AR_VALIDATED,
     AR_WS_DRY_RUN, AR_WS_NORM_BF16_H, LIB_PATH, ArfuseError, Workspace, ar_finalize_rmsnorm, ar_rmsnorm,
     ar_status_string, ar_workspace_create, ar_workspace_destroy, ar_workspace_device_error,

@@ -35,6 +35,7 @@ AR_REGIME_AUTO = 0
 AR_REGIME_CLUSTER = 1
 AR_REGIME_STREAM = 2
 AR_REGIME_ONESHOT = 3
+AR_REGIME_SPLIT = 4
 
 AR_MAX_RANKS = 16
 AR_MAX_TOP_K = 16

@@ -28,6 +28,7 @@ struct ar_workspace {
     int smem_optin;
     int max_cluster;  // largest co-schedulable cluster for the cluster kernel
     int max_cluster_stream;  // largest cluster for the clustered streaming kernel
+    int max_cluster_split;   // largest cluster for the split kernel
     int regime_force;
     int force_ctas_per_row;  // 0: automatic
     int stage_bytes;         // 0: automatic
@@ -122,17 +123,39 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     int regime = ws->regime_force;
     arf::ClusterPlan cplan{};
     arf::StreamPlan splan{};
+    arf::SplitPlan xplan{};
     if (regime == AR_REGIME_AUTO) {
-        // Light rows (at most 8 summands per 16-byte chunk, so one load wave
-        // per thread) below one row per SM: the one-shot kernel was fastest.
+        // Measured on GB300 (bench.py sweep):
+        //  - light rows (at most 8 summands per 16-byte chunk, one load wave
+        //    per thread) below one row per two SMs: the one-shot kernel;
+        //  - heavy rows at the smallest T (one cluster per row fits in half
+        //    the SMs): the split kernel, fewest bulk copies per CTA;
+        //  - otherwise the streaming kernel (tiles over a cluster for small
+        //    T, whole rows for large T).
         const int summands = (shared ? R : 0) + R * K;
-        if (summands <= 8 && T < ws->num_sms &&
+        if (summands <= 8 && 2 * T < ws->num_sms &&
             arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &cplan))
             regime = AR_REGIME_ONESHOT;
+        else if (summands > 8 && arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                                      ws->max_cluster_split, 0, &xplan))
+            regime = AR_REGIME_SPLIT;
     }
     if (regime == AR_REGIME_ONESHOT) {
         if (!cplan.C && !arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &cplan))
             return AR_ERR_UNSUPPORTED;
+    } else if (regime == AR_REGIME_SPLIT) {
+        if (!xplan.geo.C) {
+            // forced: the given cluster size, else the largest that fits
+            int C = ws->force_ctas_per_row;
+            if (C == 0)
+                for (int c = 16; c >= 2 && C == 0; c >>= 1)
+                    if (arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                             ws->max_cluster_split, c, &xplan))
+                        C = c;
+            if (C == 0 || !arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                                ws->max_cluster_split, C, &xplan))
+                return AR_ERR_UNSUPPORTED;
+        }
     } else {
         int C = 0;  // automatic
         if (regime == AR_REGIME_STREAM) C = 1;
@@ -188,6 +211,9 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     if (regime == AR_REGIME_ONESHOT) {
         e = arf::launch_cluster_rows(a, cplan, res_f32 != 0, s);
         ctas = cplan.C;
+    } else if (regime == AR_REGIME_SPLIT) {
+        e = arf::launch_split_rows(a, xplan, res_f32 != 0, s);
+        ctas = xplan.geo.C;
     } else {
         e = arf::launch_stream_rows(a, splan, res_f32 != 0, s);
         ctas = regime == AR_REGIME_CLUSTER ? splan.geo.C : splan.grid;
@@ -237,6 +263,7 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
         ws->smem_optin = kDryRunSmemOptin;
         ws->max_cluster = 16;
         ws->max_cluster_stream = 16;
+        ws->max_cluster_split = 16;
         *out = ws;
         return AR_OK;
     }
@@ -259,7 +286,8 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
         st = AR_ERR_CUDA;
         goto fail;
     }
-    if (arf::cluster_rows_set_attributes() != cudaSuccess) {
+    if (arf::cluster_rows_set_attributes() != cudaSuccess ||
+        arf::split_rows_set_attributes(ws->smem_optin) != cudaSuccess) {
         st = AR_ERR_CUDA;
         goto fail;
     }
@@ -276,6 +304,12 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
         for (int c = 16; c >= 2 && ws->max_cluster_stream == 1; c >>= 1)
             if (arf::plan_stream_rows(ranks, top_k, hidden, true, 1, ws->num_sms, ws->smem_optin, 16, c, 0, &sp))
                 ws->max_cluster_stream = arf::stream_rows_max_cluster(sp.threads, sp.smem, sp.cpt);
+        // ... and for the split kernel.
+        arf::SplitPlan xp{};
+        ws->max_cluster_split = 1;
+        for (int c = 16; c >= 2 && ws->max_cluster_split == 1; c >>= 1)
+            if (arf::plan_split_rows(ranks, top_k, hidden, true, 1, ws->num_sms, ws->smem_optin, 16, c, &xp))
+                ws->max_cluster_split = arf::split_rows_max_cluster(xp.threads, xp.smem, xp.cpt);
     }
     if (cudaMalloc(&ws->d_err, 256) != cudaSuccess || cudaMemset(ws->d_err, 0, 256) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
@@ -364,7 +398,7 @@ ar_status ar_workspace_device_error(ar_workspace* ws, int* code) {
 ar_status ar_workspace_set_regime(ar_workspace* ws, int regime) {
     if (!ws) return AR_ERR_INVALID_ARG;
     if (regime != AR_REGIME_AUTO && regime != AR_REGIME_CLUSTER && regime != AR_REGIME_STREAM &&
-        regime != AR_REGIME_ONESHOT)
+        regime != AR_REGIME_ONESHOT && regime != AR_REGIME_SPLIT)
         return AR_ERR_INVALID_ARG;
     ws->regime_force = regime;
     return AR_OK;
@@ -432,6 +466,7 @@ struct NoAllocDevice {
     int smem_optin;
     int max_cluster;
     int max_cluster_stream;
+    int max_cluster_split;
 };
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 std::mutex g_noalloc_mu;
@@ -449,7 +484,8 @@ ar_status noalloc_setup(int device, NoAllocDevice** out) {
     if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return AR_ERR_CUDA;
     if (prop.major < 10) return AR_ERR_UNSUPPORTED;
     if (arf::stream_rows_set_attributes((int)prop.sharedMemPerBlockOptin) != cudaSuccess ||
-        arf::cluster_rows_set_attributes() != cudaSuccess) {
+        arf::cluster_rows_set_attributes() != cudaSuccess ||
+        arf::split_rows_set_attributes((int)prop.sharedMemPerBlockOptin) != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ERR_CUDA;
     }
@@ -467,6 +503,7 @@ ar_status noalloc_setup(int device, NoAllocDevice** out) {
     d.max_cluster = arf::cluster_rows_max_cluster(768, 24576, false);
     if (d.max_cluster < 1) d.max_cluster = 1;
     d.max_cluster_stream = arf::stream_rows_max_cluster(544, d.smem_optin / 3, 1);
+    d.max_cluster_split = arf::split_rows_max_cluster(544, d.smem_optin, 2);
     d.ready = true;
     *out = &d;
     return AR_OK;
@@ -510,6 +547,7 @@ ar_status ar_finalize_rmsnorm_noalloc(const void* const* expert_out, int64_t row
     ws.smem_optin = d->smem_optin;
     ws.max_cluster = d->max_cluster;
     ws.max_cluster_stream = d->max_cluster_stream;
+    ws.max_cluster_split = d->max_cluster_split;
     ws.regime_force = AR_REGIME_AUTO;
     ar_status v = run(&ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma,
                       weight_bias, eps, T, R, K, H, out, residual_out, residual_out_is_fp32,

@@ -324,4 +324,29 @@ cudaError_t stream_rows_set_attributes(int smem_optin);
 // Largest cluster (<= 16) co-schedulable for a clustered plan of this shape.
 int stream_rows_max_cluster(int threads, int smem, int cpt);
 
+// Geometry of one split_rows launch (kernel parameter).
+struct SplitGeom {
+    int C;            // CTAs per row (cluster size); CTA c copies segments c, c+C, ...
+    int seg_stride;   // bytes between segment buffers in shared memory
+    int part_bytes;   // bytes of the fp32 partial row
+    int tile_chunks;  // 16-byte chunks of the column tile each CTA finishes
+};
+
+struct SplitPlan {
+    SplitGeom geo;
+    int cpt;
+    int threads;
+    int smem;
+    int grid;
+};
+
+// Plan a split_rows launch (one row per cluster); C = 0 picks the largest
+// cluster that fits.  Returns false if no plan fits.
+bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
+                     int max_cluster, int C, SplitPlan* p);
+cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32,
+                              cudaStream_t stream);
+cudaError_t split_rows_set_attributes(int smem_optin);
+int split_rows_max_cluster(int threads, int smem, int cpt);
+
 }  // namespace arf

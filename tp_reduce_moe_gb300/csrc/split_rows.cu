@@ -1,0 +1,403 @@
+// split_rows.cu -- decode-latency kernel: one token row per thread-block
+// cluster, the row's segments dealt round-robin to the cluster's C CTAs.
+//
+// At decode sizes a row is nseg = R*(K+1)+1 segments of H bf16 (~1 MB) and
+// the TMA engine completes a bulk copy every ~50 ns whatever its size, so the
+// number of copies per CTA -- not the bytes -- sets the time.  Here CTA c of
+// the cluster copies only segments c, c+C, c+2C, ... (~nseg/C full-width rows,
+// all in flight at once), accumulates them into a full-width fp32 partial
+// row, and the cluster then reduce-scatters the partials through distributed
+// shared memory: CTA c sums column tile c over all C partials (fixed rank
+// order), which is h for that tile.  Then the row's sum of squares meets
+// across the cluster, and each CTA normalises and stores its tile.
+//
+//   producer warp: shared partials + residual copies go out at once (they
+//     need no routing metadata) on mbarrier 0; the routed copies follow as
+//     soon as perm arrives, on mbarrier 1; per-segment coefficients go into
+//     a shared-memory table published by the same barrier phases.
+//   consumers: fold the CTA's segments into registers, write the partial row
+//     to shared memory; cluster barrier; reduce-scatter; cluster barrier for
+//     the sum of squares; normalise; store.
+//
+// Waits on the two mbarriers are bounded (arf::mbar_wait_bounded); the three
+// cluster barriers are reached unconditionally by every thread, so a CTA
+// never leaves while a peer still reads its shared memory.
+//
+// Operation: sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and
+// wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
+// 1-2; sglang PR #37104 "perf(mtp): fuse trailing TP all-reduce with final
+// RMSNorm", Changes.
+#include "arf_common.cuh"
+
+namespace arf {
+
+constexpr int kSplitMaxSegs = 32;       // segments per CTA (one producer lane each)
+constexpr int kSplitMaxConsumers = 512;
+constexpr int kSplitMaxThreads = 32 + kSplitMaxConsumers;
+constexpr int kSplitHeader = 1024;      // barriers, coefficient table, partial sums, flags
+
+// Header layout (bytes): 0 bar[2]; 16 coef[32] f32; 144 red[32] f32;
+// 272 ss slot f32; 288 abort flag; 1024 partial row [H] f32; then the
+// segment buffers at seg_stride.
+__device__ __forceinline__ void ld_shared_cluster_v4(uint32_t addr, float4& v) {
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+}
+
+template <int CPT, bool RES_F32>
+__global__ void __launch_bounds__(kSplitMaxThreads, 1)
+    split_rows_kernel(const __grid_constant__ RowArgs a, const SplitGeom geo) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    float* coef = reinterpret_cast<float*>(smem + 16);
+    float* red = reinterpret_cast<float*>(smem + 144);
+    float* ss_slot = reinterpret_cast<float*>(smem + 272);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 288);
+    float* part = reinterpret_cast<float*>(smem + kSplitHeader);
+    uint8_t* segbuf = smem + kSplitHeader + geo.part_bytes;
+
+    const int C = geo.C;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ncw = (blockDim.x >> 5) - 1;
+    const uint32_t c = cluster_ctarank();
+    const int64_t t = blockIdx.x / C;
+    const int H = a.H;
+    const int chunks = H / 8;
+    const uint32_t row_bytes = (uint32_t)H * 2u;
+    const int nS = a.has_shared ? a.R : 0;
+    const int nsr = nS + 1;                          // shared partials + residual
+    const int nseg = nsr + a.R * a.K;
+    // Segments of this CTA: s = c + i*C, i < ns; the first nsr_c need no perm.
+    const int ns = (nseg - (int)c + C - 1) / C;
+    const int nsr_c = (nsr > (int)c) ? (nsr - 1 - (int)c) / C + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar[0]), 1);
+        mbar_init(smem_addr(&bar[1]), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = l2_evict_first_policy();
+        const int i = lane;
+        const int s = (int)c + i * C;
+        const bool mine = i < ns;
+        const bool is_sr = mine && i < nsr_c;
+        const uint32_t dst = smem_addr(segbuf + (size_t)i * geo.seg_stride);
+        // 1. perm-independent copies, at once
+        if (is_sr) {
+            const uint16_t* src = s < nS ? a.S[s] + t * H : a.residual + t * H;
+            bulk_g2s(dst, src, row_bytes, smem_addr(&bar[0]), pol);
+        }
+        // 2. routing metadata -> routed copies
+        int32_t raw = 0;
+        float wv = 0.0f;
+        if (lane < a.K) {
+            raw = __ldg(a.perm + t * a.K + lane);
+            wv = __ldg(a.w + t * a.K + lane);
+        }
+        const int64_t rowv = lane < a.K ? checked_row(raw, a.rows_e, a.err) : 0;
+        const int e = s - nsr;
+        const int k = (mine && !is_sr) ? e / a.R : 0;
+        const int64_t row_k = __shfl_sync(0xffffffffu, rowv, k);
+        const float w_k = __shfl_sync(0xffffffffu, wv, k);
+        if (mine && !is_sr)
+            bulk_g2s(dst, a.E[e % a.R] + row_k * H, row_bytes, smem_addr(&bar[1]), pol);
+        // 3. coefficients, then arm both barriers (a phase needs lane 0's
+        //    arrival as well as the bytes, so it cannot complete early)
+        if (mine) coef[i] = is_sr ? (s < nS ? shared_coef(a, t) : 1.0f) : w_k;
+        __syncwarp();
+        if (lane == 0) {
+            if (nsr_c > 0) mbar_arrive_expect_tx(smem_addr(&bar[0]), (uint32_t)nsr_c * row_bytes);
+            if (ns > nsr_c) mbar_arrive_expect_tx(smem_addr(&bar[1]), (uint32_t)(ns - nsr_c) * row_bytes);
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int ci = threadIdx.x - 32;
+        const int nct = ncw * 32;
+        float acc[CPT][8];
+#pragma unroll
+        for (int m = 0; m < CPT; ++m)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[m][j] = 0.0f;
+        bool ok = true;
+        for (int phase_set = 0; phase_set < 2; ++phase_set) {
+            const int i_begin = phase_set == 0 ? 0 : nsr_c;
+            const int i_end = phase_set == 0 ? nsr_c : ns;
+            if (i_begin >= i_end) continue;
+            if (ok && !mbar_wait_bounded(smem_addr(&bar[phase_set]), 0u, abort_flag)) {
+                ok = false;
+                if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            for (int i0 = i_begin; i0 < i_end; i0 += 4) {
+                float cf[4];
+                uint4 v[4][CPT];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) cf[u] = i0 + u < i_end ? coef[i0 + u] : 0.0f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int m = 0; m < CPT; ++m) {
+                        const int ch = ci + m * nct;
+                        if (i0 + u < i_end && ch < chunks)
+                            v[u][m] = reinterpret_cast<const uint4*>(segbuf + (size_t)(i0 + u) * geo.seg_stride)[ch];
+                    }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int m = 0; m < CPT; ++m) {
+                        const int ch = ci + m * nct;
+                        if (i0 + u < i_end && ch < chunks) {
+                            float f[8];
+                            bf16x8_to_f32(v[u][m], f);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) acc[m][j] = fmaf(cf[u], f[j], acc[m][j]);
+                        }
+                    }
+            }
+        }
+        // partial row of this CTA -> shared memory
+#pragma unroll
+        for (int m = 0; m < CPT; ++m) {
+            const int ch = ci + m * nct;
+            if (ch < chunks) {
+                float4* p = reinterpret_cast<float4*>(part + (size_t)ch * 8);
+                p[0] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+                p[1] = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
+            }
+        }
+    }
+
+    // ---- sync 1: every CTA's partial row is complete and visible
+    __syncwarp();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+
+    // ---- reduce-scatter: this CTA's column tile summed over all partials.
+    // Work item q = one float4 (half a 16-byte bf16 chunk) of the tile; a
+    // consumer thread owns items ci + m*nct (m < CPT, enough since a tile is
+    // at most half the row), and requests every peer's value before the first
+    // add (remote loads are slow one at a time).  Sums run in rank order, the
+    // same in every CTA.
+    const int tile0 = (int)c * geo.tile_chunks;
+    const int ntile = min(geo.tile_chunks, chunks - tile0);
+    const int ci = threadIdx.x - 32;
+    const int nct = ncw * 32;
+    float4 hq[CPT];
+    bool hv[CPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int m = 0; m < CPT; ++m) {
+        const int q = ci + m * nct;
+        hv[m] = warp > 0 && q < 2 * ntile;
+        hq[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!hv[m]) continue;
+        const uint32_t mine = smem_addr(part + (size_t)tile0 * 8 + (size_t)q * 4);
+        for (int r0 = 0; r0 < C; r0 += 8) {
+            float4 x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (r0 + u < C) ld_shared_cluster_v4(map_shared_rank(mine, (uint32_t)(r0 + u)), x[u]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (r0 + u < C) {
+                    hq[m].x += x[u].x;
+                    hq[m].y += x[u].y;
+                    hq[m].z += x[u].z;
+                    hq[m].w += x[u].w;
+                }
+        }
+        const int64_t elem = t * H + (int64_t)tile0 * 8 + (int64_t)q * 4;
+        if (RES_F32) {
+            st_global16(reinterpret_cast<float*>(a.residual_out) + elem,
+                        make_uint4(__float_as_uint(hq[m].x), __float_as_uint(hq[m].y),
+                                   __float_as_uint(hq[m].z), __float_as_uint(hq[m].w)));
+        } else {
+            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.residual_out) + elem) =
+                make_uint2(pack_bf16x2(hq[m].x, hq[m].y), pack_bf16x2(hq[m].z, hq[m].w));
+        }
+        hq[m].x = norm_input(hq[m].x, a.norm_bf16_h);
+        hq[m].y = norm_input(hq[m].y, a.norm_bf16_h);
+        hq[m].z = norm_input(hq[m].z, a.norm_bf16_h);
+        hq[m].w = norm_input(hq[m].w, a.norm_bf16_h);
+        ss += hq[m].x * hq[m].x + hq[m].y * hq[m].y + hq[m].z * hq[m].z + hq[m].w * hq[m].w;
+    }
+    if (warp > 0) {
+        ss = warp_sum(ss);
+        if (lane == 0) red[warp - 1] = ss;
+        named_barrier_sync(1, nct);
+        if (ci == 0) {
+            float tot = 0.0f;
+            for (int w = 0; w < ncw; ++w) tot += red[w];
+            *ss_slot = tot;
+        }
+    }
+
+    // ---- sync 2: every CTA's tile sum of squares is visible (and every CTA
+    // has finished reading its peers' partial rows)
+    __syncwarp();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+
+    float total = 0.0f;
+    if (hv[0]) {
+        const uint32_t slot = smem_addr(ss_slot);
+        float xs[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (u < C) xs[u] = ld_shared_cluster_f32(map_shared_rank(slot, (uint32_t)u));
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (u < C) total += xs[u];
+    }
+    // ---- sync 3 (arrive now, wait at the end): no CTA leaves while a peer
+    // may still read its sum of squares
+    __syncwarp();
+    cluster_arrive_release();
+
+    const float inv = rsqrtf(total / (float)H + a.eps);
+    const float wb = a.weight_bias;
+#pragma unroll
+    for (int m = 0; m < CPT; ++m) {
+        if (!hv[m]) continue;
+        const int64_t col = (int64_t)tile0 * 8 + (int64_t)(ci + m * nct) * 4;
+        const uint2 gv = *reinterpret_cast<const uint2*>(a.gamma + col);
+        const float g0 = __uint_as_float(gv.x << 16) + wb, g1 = __uint_as_float(gv.x & 0xffff0000u) + wb;
+        const float g2 = __uint_as_float(gv.y << 16) + wb, g3 = __uint_as_float(gv.y & 0xffff0000u) + wb;
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + t * H + col) =
+            make_uint2(pack_bf16x2(hq[m].x * inv * g0, hq[m].y * inv * g1),
+                       pack_bf16x2(hq[m].z * inv * g2, hq[m].w * inv * g3));
+    }
+
+    // After an abort, copies may still be landing: wait (briefly) for both
+    // barriers before the CTA may exit.
+    if (threadIdx.x == 0 && *abort_flag) {
+        if (nsr_c > 0) (void)mbar_wait_bounded(smem_addr(&bar[0]), 0u, nullptr, 10000000ull);
+        if (ns > nsr_c) (void)mbar_wait_bounded(smem_addr(&bar[1]), 0u, nullptr, 10000000ull);
+    }
+    __syncwarp();
+    cluster_wait_acquire();
+}
+
+// ------------------------------------------------------------------ host side
+static int ceil_div_s(int a, int b) { return (a + b - 1) / b; }
+
+bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
+                     int max_cluster, int C, SplitPlan* p) {
+    const int chunks = H / 8;
+    const int nseg = (shared ? R : 0) + 1 + R * K;
+    if (chunks < 2 || T < 1) return false;
+    const int seg_stride = ceil_div_s(H * 2, 128) * 128;
+    const int part_bytes = ceil_div_s(H * 4, 128) * 128;
+    auto fits = [&](int c) {
+        if (c < 2 || c > 16 || c > max_cluster || c > nseg) return false;
+        const int ns = ceil_div_s(nseg, c);
+        if (ns > kSplitMaxSegs) return false;
+        const int tile = ceil_div_s(chunks, c);
+        if ((c - 1) * tile >= chunks) return false;
+        int cpt_c = 1;
+        while (cpt_c < 4 && chunks > cpt_c * kSplitMaxConsumers) cpt_c <<= 1;
+        const int consumers_c = ceil_div_s(ceil_div_s(chunks, cpt_c), 32) * 32;
+        if (2 * tile > cpt_c * consumers_c) return false;  // <= CPT items per thread
+        return kSplitHeader + part_bytes + ns * seg_stride <= smem_optin;
+    };
+    if (C <= 0) {
+        // Automatic: the largest cluster that fits with at most one CTA per
+        // two SMs over all rows (measured: beyond that the tiled streaming
+        // kernel is faster); no plan otherwise.
+        C = 0;
+        for (int c = 16; c >= 2; c >>= 1)
+            if (fits(c) && (int64_t)c * T * 2 <= num_sms) {
+                C = c;
+                break;
+            }
+        if (!C) return false;
+    }
+    if (!fits(C)) return false;
+    int cpt = 1;
+    while (cpt < 4 && chunks > cpt * kSplitMaxConsumers) cpt <<= 1;
+    if (chunks > cpt * kSplitMaxConsumers) return false;
+    const int consumers = ceil_div_s(ceil_div_s(chunks, cpt), 32) * 32;
+    p->geo.C = C;
+    p->geo.seg_stride = seg_stride;
+    p->geo.part_bytes = part_bytes;
+    p->geo.tile_chunks = ceil_div_s(chunks, C);
+    p->cpt = cpt;
+    p->threads = 32 + consumers;
+    p->smem = kSplitHeader + part_bytes + ceil_div_s(nseg, C) * seg_stride;
+    p->grid = (int)(T * C);
+    return true;
+}
+
+static const void* split_kernel_for(int cpt, bool res_f32) {
+    switch (cpt * 2 + (res_f32 ? 1 : 0)) {
+        case 2: return reinterpret_cast<const void*>(split_rows_kernel<1, false>);
+        case 3: return reinterpret_cast<const void*>(split_rows_kernel<1, true>);
+        case 4: return reinterpret_cast<const void*>(split_rows_kernel<2, false>);
+        case 5: return reinterpret_cast<const void*>(split_rows_kernel<2, true>);
+        case 8: return reinterpret_cast<const void*>(split_rows_kernel<4, false>);
+        case 9: return reinterpret_cast<const void*>(split_rows_kernel<4, true>);
+    }
+    return nullptr;
+}
+
+cudaError_t split_rows_set_attributes(int smem_optin) {
+    for (int cpt = 1; cpt <= 4; cpt <<= 1)
+        for (int f = 0; f < 2; ++f) {
+            const void* k = split_kernel_for(cpt, f != 0);
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+    return cudaSuccess;
+}
+
+int split_rows_max_cluster(int threads, int smem, int cpt) {
+    for (int C = 16; C >= 2; C >>= 1) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3((unsigned)C);
+        cfg.blockDim = dim3((unsigned)threads);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, split_kernel_for(cpt, false), &cfg) == cudaSuccess && n > 0)
+            return C;
+        (void)cudaGetLastError();
+    }
+    return 1;
+}
+
+cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32, cudaStream_t stream) {
+    const void* k = split_kernel_for(p.cpt, res_f32);
+    if (!k) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = (size_t)p.smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.geo.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {const_cast<RowArgs*>(&a), const_cast<SplitGeom*>(&p.geo)};
+    return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+}  // namespace arf
