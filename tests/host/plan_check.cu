@@ -75,7 +75,7 @@ int main() {
       const int consumers = p.threads - 32;
       if ((long)consumers * p.cpt < chunks) bad = true;       // partial row fully covered
       if (2 * g.tile_chunks > p.cpt * consumers) bad = true;  // <= CPT float4 items per thread
-      if (g.seg_stride < H * 2 || g.seg_stride % 128 || g.part_bytes < H * 4) bad = true;
+      if (g.seg_stride < H * 2 || g.seg_stride % 128 || g.part_bytes < C * g.tile_chunks * 32) bad = true;
       for (int c = 0; c < C; ++c) {
         const int ns = (nseg - c + C - 1) / C;
         if (ns < 1 || ns > 32) bad = true;

@@ -261,6 +261,12 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -328,7 +334,7 @@ int stream_rows_max_cluster(int threads, int smem, int cpt);
 struct SplitGeom {
     int C;            // CTAs per row (cluster size); CTA c copies segments c, c+C, ...
     int seg_stride;   // bytes between segment buffers in shared memory
-    int part_bytes;   // bytes of the fp32 partial row
+    int part_bytes;   // bytes of the fp32 receive buffer (C slices of a column tile)
     int tile_chunks;  // 16-byte chunks of the column tile each CTA finishes
 };
 

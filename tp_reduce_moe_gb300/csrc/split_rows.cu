@@ -7,21 +7,25 @@
 // the cluster copies only segments c, c+C, c+2C, ... (~nseg/C full-width rows,
 // all in flight at once), accumulates them into a full-width fp32 partial
 // row, and the cluster then reduce-scatters the partials through distributed
-// shared memory: CTA c sums column tile c over all C partials (fixed rank
-// order), which is h for that tile.  Then the row's sum of squares meets
-// across the cluster, and each CTA normalises and stores its tile.
+// shared memory: every CTA stores slice j of its partial row straight into
+// CTA j's receive buffer (remote stores pipeline; remote loads would each
+// wait a round trip), and after one cluster barrier CTA c sums its C slices
+// locally (fixed rank order), which is h for column tile c.  The tile sums of
+// squares are pushed the same way behind a second barrier; after it no CTA
+// touches a peer's memory, so each normalises, stores its tile and leaves.
 //
 //   producer warp: shared partials + residual copies go out at once (they
 //     need no routing metadata) on mbarrier 0; the routed copies follow as
 //     soon as perm arrives, on mbarrier 1; per-segment coefficients go into
 //     a shared-memory table published by the same barrier phases.
-//   consumers: fold the CTA's segments into registers, write the partial row
-//     to shared memory; cluster barrier; reduce-scatter; cluster barrier for
-//     the sum of squares; normalise; store.
+//   consumers: fold the CTA's segments into registers, push the partial row's
+//     slices to their owners; cluster barrier; local sums; push the tile's
+//     sum of squares; cluster barrier; normalise; store.
 //
-// Waits on the two mbarriers are bounded (arf::mbar_wait_bounded); the three
-// cluster barriers are reached unconditionally by every thread, so a CTA
-// never leaves while a peer still reads its shared memory.
+// Waits on the two mbarriers are bounded (arf::mbar_wait_bounded); both
+// cluster barriers are reached unconditionally by every thread, and every
+// remote store precedes the second one, so no CTA can be written to after it
+// has passed that barrier.
 //
 // Operation: sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and
 // wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
@@ -37,15 +41,9 @@ constexpr int kSplitMaxThreads = 32 + kSplitMaxConsumers;
 constexpr int kSplitHeader = 1024;      // barriers, coefficient table, partial sums, flags
 
 // Header layout (bytes): 0 bar[2]; 16 coef[32] f32; 144 red[32] f32;
-// 272 ss slot f32; 288 abort flag; 1024 partial row [H] f32; then the
-// segment buffers at seg_stride.
-__device__ __forceinline__ void ld_shared_cluster_v4(uint32_t addr, float4& v) {
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-}
-
+// 272 ss slots [16] f32 (one per source CTA); 336 abort flag; 1024 receive
+// buffer [C][tile_chunks*8] f32 (slice of every source CTA's partial row);
+// then the segment buffers at seg_stride.
 template <int CPT, bool RES_F32>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     split_rows_kernel(const __grid_constant__ RowArgs a, const SplitGeom geo) {
@@ -53,9 +51,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     float* coef = reinterpret_cast<float*>(smem + 16);
     float* red = reinterpret_cast<float*>(smem + 144);
-    float* ss_slot = reinterpret_cast<float*>(smem + 272);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 288);
-    float* part = reinterpret_cast<float*>(smem + kSplitHeader);
+    float* ss_slots = reinterpret_cast<float*>(smem + 272);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 336);
+    float* recv = reinterpret_cast<float*>(smem + kSplitHeader);
     uint8_t* segbuf = smem + kSplitHeader + geo.part_bytes;
 
     const int C = geo.C;
@@ -163,33 +161,36 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                     }
             }
         }
-        // partial row of this CTA -> shared memory
+        // Push the partial row: chunk ch belongs to column tile j = ch / tile
+        // of CTA j, into its receive slot for this CTA.
+        const int tile = geo.tile_chunks;
 #pragma unroll
         for (int m = 0; m < CPT; ++m) {
             const int ch = ci + m * nct;
             if (ch < chunks) {
-                float4* p = reinterpret_cast<float4*>(part + (size_t)ch * 8);
-                p[0] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-                p[1] = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
+                const int j = ch / tile;
+                const uint32_t dst = map_shared_rank(
+                    smem_addr(recv + ((size_t)c * tile + (ch - j * tile)) * 8), (uint32_t)j);
+                st_shared_cluster_v4(dst, make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]));
+                st_shared_cluster_v4(dst + 16, make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]));
             }
         }
     }
 
-    // ---- sync 1: every CTA's partial row is complete and visible
+    // ---- sync 1: every slice has landed in its owner's receive buffer
     __syncwarp();
     cluster_arrive_release();
     cluster_wait_acquire();
 
-    // ---- reduce-scatter: this CTA's column tile summed over all partials.
-    // Work item q = one float4 (half a 16-byte bf16 chunk) of the tile; a
+    // ---- this CTA's column tile: the C received slices summed locally, in
+    // rank order.  Work item q = one float4 (half a 16-byte bf16 chunk); a
     // consumer thread owns items ci + m*nct (m < CPT, enough since a tile is
-    // at most half the row), and requests every peer's value before the first
-    // add (remote loads are slow one at a time).  Sums run in rank order, the
-    // same in every CTA.
+    // at most half the row).
     const int tile0 = (int)c * geo.tile_chunks;
     const int ntile = min(geo.tile_chunks, chunks - tile0);
     const int ci = threadIdx.x - 32;
     const int nct = ncw * 32;
+    const size_t slice = (size_t)geo.tile_chunks * 8;  // floats per source slice
     float4 hq[CPT];
     bool hv[CPT];
     float ss = 0.0f;
@@ -199,20 +200,13 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         hv[m] = warp > 0 && q < 2 * ntile;
         hq[m] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (!hv[m]) continue;
-        const uint32_t mine = smem_addr(part + (size_t)tile0 * 8 + (size_t)q * 4);
-        for (int r0 = 0; r0 < C; r0 += 8) {
-            float4 x[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (r0 + u < C) ld_shared_cluster_v4(map_shared_rank(mine, (uint32_t)(r0 + u)), x[u]);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (r0 + u < C) {
-                    hq[m].x += x[u].x;
-                    hq[m].y += x[u].y;
-                    hq[m].z += x[u].z;
-                    hq[m].w += x[u].w;
-                }
+        const float* src = recv + (size_t)q * 4;
+        for (int r = 0; r < C; ++r) {
+            const float4 x = *reinterpret_cast<const float4*>(src + r * slice);
+            hq[m].x += x.x;
+            hq[m].y += x.y;
+            hq[m].z += x.z;
+            hq[m].w += x.w;
         }
         const int64_t elem = t * H + (int64_t)tile0 * 8 + (int64_t)q * 4;
         if (RES_F32) {
@@ -233,34 +227,20 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         ss = warp_sum(ss);
         if (lane == 0) red[warp - 1] = ss;
         named_barrier_sync(1, nct);
-        if (ci == 0) {
-            float tot = 0.0f;
-            for (int w = 0; w < ncw; ++w) tot += red[w];
-            *ss_slot = tot;
-        }
+        float tot = 0.0f;
+        for (int w = 0; w < ncw; ++w) tot += red[w];
+        // push this tile's sum of squares into every peer's slot c
+        if (ci < C) st_shared_cluster_f32(map_shared_rank(smem_addr(ss_slots + c), (uint32_t)ci), tot);
     }
 
-    // ---- sync 2: every CTA's tile sum of squares is visible (and every CTA
-    // has finished reading its peers' partial rows)
+    // ---- sync 2: every tile's sum of squares has landed in every CTA; no
+    // remote access follows
     __syncwarp();
     cluster_arrive_release();
     cluster_wait_acquire();
 
     float total = 0.0f;
-    if (hv[0]) {
-        const uint32_t slot = smem_addr(ss_slot);
-        float xs[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-            if (u < C) xs[u] = ld_shared_cluster_f32(map_shared_rank(slot, (uint32_t)u));
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-            if (u < C) total += xs[u];
-    }
-    // ---- sync 3 (arrive now, wait at the end): no CTA leaves while a peer
-    // may still read its sum of squares
-    __syncwarp();
-    cluster_arrive_release();
+    for (int r = 0; r < C; ++r) total += ss_slots[r];
 
     const float inv = rsqrtf(total / (float)H + a.eps);
     const float wb = a.weight_bias;
@@ -282,8 +262,6 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         if (nsr_c > 0) (void)mbar_wait_bounded(smem_addr(&bar[0]), 0u, nullptr, 10000000ull);
         if (ns > nsr_c) (void)mbar_wait_bounded(smem_addr(&bar[1]), 0u, nullptr, 10000000ull);
     }
-    __syncwarp();
-    cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------------ host side
@@ -295,7 +273,7 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
     const int nseg = (shared ? R : 0) + 1 + R * K;
     if (chunks < 2 || T < 1) return false;
     const int seg_stride = ceil_div_s(H * 2, 128) * 128;
-    const int part_bytes = ceil_div_s(H * 4, 128) * 128;
+    auto recv_bytes = [&](int c) { return ceil_div_s(c * ceil_div_s(chunks, c) * 32, 128) * 128; };
     auto fits = [&](int c) {
         if (c < 2 || c > 16 || c > max_cluster || c > nseg) return false;
         const int ns = ceil_div_s(nseg, c);
@@ -306,7 +284,7 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
         while (cpt_c < 4 && chunks > cpt_c * kSplitMaxConsumers) cpt_c <<= 1;
         const int consumers_c = ceil_div_s(ceil_div_s(chunks, cpt_c), 32) * 32;
         if (2 * tile > cpt_c * consumers_c) return false;  // <= CPT items per thread
-        return kSplitHeader + part_bytes + ns * seg_stride <= smem_optin;
+        return kSplitHeader + recv_bytes(c) + ns * seg_stride <= smem_optin;
     };
     if (C <= 0) {
         // Automatic: the largest cluster that fits with at most one CTA per
@@ -327,11 +305,11 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
     const int consumers = ceil_div_s(ceil_div_s(chunks, cpt), 32) * 32;
     p->geo.C = C;
     p->geo.seg_stride = seg_stride;
-    p->geo.part_bytes = part_bytes;
+    p->geo.part_bytes = recv_bytes(C);
     p->geo.tile_chunks = ceil_div_s(chunks, C);
     p->cpt = cpt;
     p->threads = 32 + consumers;
-    p->smem = kSplitHeader + part_bytes + ceil_div_s(nseg, C) * seg_stride;
+    p->smem = kSplitHeader + recv_bytes(C) + ceil_div_s(nseg, C) * seg_stride;
     p->grid = (int)(T * C);
     return true;
 }
