@@ -79,7 +79,8 @@ int main() {
       for (int c = 0; c < C; ++c) {
         const int ns = (nseg - c + C - 1) / C;
         if (ns < 1 || ns > 32) bad = true;
-        if (1024 + g.part_bytes + (long)ns * g.seg_stride > p.smem) bad = true;
+        if (1024 + g.part_bytes + g.row_f32_bytes + (long)ns * g.seg_stride > p.smem) bad = true;
+        if (g.row_f32_bytes < chunks * 32) bad = true;
         if ((long)ns * H * 2 >= (1 << 20)) bad = true;        // mbarrier transaction count
         if (std::min(g.tile_chunks, chunks - c * g.tile_chunks) < 1) bad = true;
       }

@@ -227,6 +227,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Copy `bytes` (multiple of 16, 16-byte aligned) from this CTA's shared
+// memory into a peer's shared memory (addresses from map_shared_rank),
+// completing as transaction bytes on the peer's mbarrier `remote_bar`.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
+                                               uint32_t remote_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            remote_dst),
+        "r"(local_src), "r"(bytes), "r"(remote_bar)
+        : "memory");
+}
+
 // ------------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -335,6 +347,7 @@ struct SplitGeom {
     int C;            // CTAs per row (cluster size); CTA c copies segments c, c+C, ...
     int seg_stride;   // bytes between segment buffers in shared memory
     int part_bytes;   // bytes of the fp32 receive buffer (C slices of a column tile)
+    int row_f32_bytes;  // bytes of the CTA's own fp32 partial row
     int tile_chunks;  // 16-byte chunks of the column tile each CTA finishes
 };
 

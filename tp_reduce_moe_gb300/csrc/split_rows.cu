@@ -7,25 +7,28 @@
 // the cluster copies only segments c, c+C, c+2C, ... (~nseg/C full-width rows,
 // all in flight at once), accumulates them into a full-width fp32 partial
 // row, and the cluster then reduce-scatters the partials through distributed
-// shared memory: every CTA stores slice j of its partial row straight into
-// CTA j's receive buffer (remote stores pipeline; remote loads would each
-// wait a round trip), and after one cluster barrier CTA c sums its C slices
-// locally (fixed rank order), which is h for column tile c.  The tile sums of
-// squares are pushed the same way behind a second barrier; after it no CTA
-// touches a peer's memory, so each normalises, stores its tile and leaves.
+// shared memory: every CTA sends slice j of its partial row to CTA j with one
+// bulk copy (shared -> peer shared, the TMA engine), completing on CTA j's
+// receive mbarrier; CTA c then sums its C received slices locally (fixed rank
+// order), which is h for column tile c.  The tile sums of squares are pushed
+// into every peer with a remote mbarrier arrive; each CTA normalises and
+// stores its tile.
 //
 //   producer warp: shared partials + residual copies go out at once (they
 //     need no routing metadata) on mbarrier 0; the routed copies follow as
 //     soon as perm arrives, on mbarrier 1; per-segment coefficients go into
 //     a shared-memory table published by the same barrier phases.
-//   consumers: fold the CTA's segments into registers, push the partial row's
-//     slices to their owners; cluster barrier; local sums; push the tile's
-//     sum of squares; cluster barrier; normalise; store.
+//   consumers: fold the CTA's segments into registers, write the partial row
+//     locally, send its slices; wait for the C slices of this tile; local sums;
+//     push the tile's sum of squares; wait for the C sums; normalise; store.
 //
-// Waits on the two mbarriers are bounded (arf::mbar_wait_bounded); both
-// cluster barriers are reached unconditionally by every thread, and every
-// remote store precedes the second one, so no CTA can be written to after it
-// has passed that barrier.
+// Cluster barrier A (arrived on right after the mbarriers are initialised,
+// waited on just before the first send) keeps peers from signalling a
+// barrier that does not exist yet; barrier B (arrived on once everything
+// expected has been received, waited on at exit) keeps every CTA resident
+// until the copies reading its shared memory have landed.  Every mbarrier
+// wait is bounded (arf::mbar_wait_bounded); both cluster barriers are reached
+// unconditionally by every thread.
 //
 // Operation: sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and
 // wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
@@ -40,21 +43,25 @@ constexpr int kSplitMaxConsumers = 512;
 constexpr int kSplitMaxThreads = 32 + kSplitMaxConsumers;
 constexpr int kSplitHeader = 1024;      // barriers, coefficient table, partial sums, flags
 
-// Header layout (bytes): 0 bar[2]; 16 coef[32] f32; 144 red[32] f32;
-// 272 ss slots [16] f32 (one per source CTA); 336 abort flag; 1024 receive
+// Header layout (bytes): 0 bar[2] (segment loads), 16 rbar (slices received),
+// 24 ssbar (sums of squares received); 32 coef[32] f32; 160 red[32] f32;
+// 288 ss slots [16] f32 (one per source CTA); 352 abort flag; 1024 receive
 // buffer [C][tile_chunks*8] f32 (slice of every source CTA's partial row);
-// then the segment buffers at seg_stride.
+// then the partial row [chunks*8] f32 and the segment buffers at seg_stride.
 template <int CPT, bool RES_F32>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     split_rows_kernel(const __grid_constant__ RowArgs a, const SplitGeom geo) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    float* coef = reinterpret_cast<float*>(smem + 16);
-    float* red = reinterpret_cast<float*>(smem + 144);
-    float* ss_slots = reinterpret_cast<float*>(smem + 272);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 336);
+    uint64_t* rbar = bar + 2;
+    uint64_t* ssbar = bar + 3;
+    float* coef = reinterpret_cast<float*>(smem + 32);
+    float* red = reinterpret_cast<float*>(smem + 160);
+    float* ss_slots = reinterpret_cast<float*>(smem + 288);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 352);
     float* recv = reinterpret_cast<float*>(smem + kSplitHeader);
-    uint8_t* segbuf = smem + kSplitHeader + geo.part_bytes;
+    float* part = reinterpret_cast<float*>(smem + kSplitHeader + geo.part_bytes);
+    uint8_t* segbuf = smem + kSplitHeader + geo.part_bytes + geo.row_f32_bytes;
 
     const int C = geo.C;
     const int warp = threadIdx.x >> 5;
@@ -72,13 +79,21 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     const int ns = (nseg - (int)c + C - 1) / C;
     const int nsr_c = (nsr > (int)c) ? (nsr - 1 - (int)c) / C + 1 : 0;
 
+    const int tile = geo.tile_chunks;
+    const int ntile_c = min(tile, chunks - (int)c * tile);  // chunks of this CTA's tile
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&bar[0]), 1);
         mbar_init(smem_addr(&bar[1]), 1);
+        mbar_init(smem_addr(rbar), 1);
+        mbar_init(smem_addr(ssbar), (uint32_t)C);
         *abort_flag = 0;
         fence_mbar_init();
+        // every source CTA sends this tile's slice of its partial row
+        mbar_arrive_expect_tx(smem_addr(rbar), (uint32_t)(C * ntile_c * 32));
     }
     __syncthreads();
+    // barrier A, arrive: this CTA's mbarriers exist
+    cluster_arrive_release();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -161,39 +176,50 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                     }
             }
         }
-        // Push the partial row: chunk ch belongs to column tile j = ch / tile
-        // of CTA j, into its receive slot for this CTA.
-        const int tile = geo.tile_chunks;
+        // The partial row, locally; made visible to the bulk-copy engine.
 #pragma unroll
         for (int m = 0; m < CPT; ++m) {
             const int ch = ci + m * nct;
             if (ch < chunks) {
-                const int j = ch / tile;
-                const uint32_t dst = map_shared_rank(
-                    smem_addr(recv + ((size_t)c * tile + (ch - j * tile)) * 8), (uint32_t)j);
-                st_shared_cluster_v4(dst, make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]));
-                st_shared_cluster_v4(dst + 16, make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]));
+                float4* p = reinterpret_cast<float4*>(part + (size_t)ch * 8);
+                p[0] = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+                p[1] = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
             }
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        named_barrier_sync(1, nct);
     }
 
-    // ---- sync 1: every slice has landed in its owner's receive buffer
+    // ---- barrier A, wait: every peer's receive barrier exists
     __syncwarp();
-    cluster_arrive_release();
     cluster_wait_acquire();
+    // send slice j of the partial row to CTA j (one bulk copy each)
+    if (warp == 1 && lane < C) {
+        const int j = lane;
+        const int nj = min(tile, chunks - j * tile);
+        bulk_s2cluster(map_shared_rank(smem_addr(recv + ((size_t)c * tile) * 8), (uint32_t)j),
+                       smem_addr(part + (size_t)j * tile * 8), (uint32_t)nj * 32u,
+                       map_shared_rank(smem_addr(rbar), (uint32_t)j));
+    }
 
     // ---- this CTA's column tile: the C received slices summed locally, in
     // rank order.  Work item q = one float4 (half a 16-byte bf16 chunk); a
     // consumer thread owns items ci + m*nct (m < CPT, enough since a tile is
     // at most half the row).
-    const int tile0 = (int)c * geo.tile_chunks;
-    const int ntile = min(geo.tile_chunks, chunks - tile0);
+    const int tile0 = (int)c * tile;
+    const int ntile = ntile_c;
     const int ci = threadIdx.x - 32;
     const int nct = ncw * 32;
-    const size_t slice = (size_t)geo.tile_chunks * 8;  // floats per source slice
+    const size_t slice = (size_t)tile * 8;  // floats per source slice
     float4 hq[CPT];
     bool hv[CPT];
     float ss = 0.0f;
+    bool ok2 = true;
+    if (warp > 0 && !mbar_wait_bounded(smem_addr(rbar), 0u, abort_flag)) {
+        ok2 = false;
+        if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+        *abort_flag = 1;
+    }
 #pragma unroll
     for (int m = 0; m < CPT; ++m) {
         const int q = ci + m * nct;
@@ -230,17 +256,23 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         float tot = 0.0f;
         for (int w = 0; w < ncw; ++w) tot += red[w];
         // push this tile's sum of squares into every peer's slot c
-        if (ci < C) st_shared_cluster_f32(map_shared_rank(smem_addr(ss_slots + c), (uint32_t)ci), tot);
+        if (ci < C) {
+            st_shared_cluster_f32(map_shared_rank(smem_addr(ss_slots + c), (uint32_t)ci), tot);
+            mbar_arrive_remote(map_shared_rank(smem_addr(ssbar), (uint32_t)ci));
+        }
+        if (ok2 && !mbar_wait_bounded<true>(smem_addr(ssbar), 0u, abort_flag)) {
+            if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+            *abort_flag = 1;
+        }
     }
 
-    // ---- sync 2: every tile's sum of squares has landed in every CTA; no
-    // remote access follows
+    // ---- barrier B, arrive: everything this CTA expects has arrived (so the
+    // copies that read its partial row have landed in their targets' memory)
     __syncwarp();
     cluster_arrive_release();
-    cluster_wait_acquire();
 
     float total = 0.0f;
-    for (int r = 0; r < C; ++r) total += ss_slots[r];
+    for (int r = 0; r < C; ++r) total += reinterpret_cast<volatile float*>(ss_slots)[r];
 
     const float inv = rsqrtf(total / (float)H + a.eps);
     const float wb = a.weight_bias;
@@ -261,7 +293,11 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) {
         if (nsr_c > 0) (void)mbar_wait_bounded(smem_addr(&bar[0]), 0u, nullptr, 10000000ull);
         if (ns > nsr_c) (void)mbar_wait_bounded(smem_addr(&bar[1]), 0u, nullptr, 10000000ull);
+        (void)mbar_wait_bounded(smem_addr(rbar), 0u, nullptr, 10000000ull);
     }
+    // ---- barrier B, wait: no CTA leaves while a peer may still read it
+    __syncwarp();
+    cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------------ host side
@@ -274,6 +310,7 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
     if (chunks < 2 || T < 1) return false;
     const int seg_stride = ceil_div_s(H * 2, 128) * 128;
     auto recv_bytes = [&](int c) { return ceil_div_s(c * ceil_div_s(chunks, c) * 32, 128) * 128; };
+    const int row_f32 = ceil_div_s(chunks * 32, 128) * 128;
     auto fits = [&](int c) {
         if (c < 2 || c > 16 || c > max_cluster || c > nseg) return false;
         const int ns = ceil_div_s(nseg, c);
@@ -284,7 +321,7 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
         while (cpt_c < 4 && chunks > cpt_c * kSplitMaxConsumers) cpt_c <<= 1;
         const int consumers_c = ceil_div_s(ceil_div_s(chunks, cpt_c), 32) * 32;
         if (2 * tile > cpt_c * consumers_c) return false;  // <= CPT items per thread
-        return kSplitHeader + recv_bytes(c) + ns * seg_stride <= smem_optin;
+        return kSplitHeader + recv_bytes(c) + row_f32 + ns * seg_stride <= smem_optin;
     };
     if (C <= 0) {
         // Automatic: the largest cluster that fits with at most one CTA per
@@ -306,10 +343,11 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
     p->geo.C = C;
     p->geo.seg_stride = seg_stride;
     p->geo.part_bytes = recv_bytes(C);
+    p->geo.row_f32_bytes = row_f32;
     p->geo.tile_chunks = ceil_div_s(chunks, C);
     p->cpt = cpt;
     p->threads = 32 + consumers;
-    p->smem = kSplitHeader + recv_bytes(C) + ceil_div_s(nseg, C) * seg_stride;
+    p->smem = kSplitHeader + recv_bytes(C) + row_f32 + ceil_div_s(nseg, C) * seg_stride;
     p->grid = (int)(T * C);
     return true;
 }
