@@ -230,18 +230,68 @@ ARFUSE_API ar_status ar_workspace_set_cluster_size(ar_workspace* ws, int ctas_pe
 /*
  * Set the target size in bytes of one ring slot of the streaming kernels (a
  * slot holds as many whole row segments as fit, at least one, one bulk copy
- * each, all signalled on one mbarrier); 0 restores the automatic size (32 KB
- * for whole rows, 16 KB for column tiles).  Values outside 0 or
+ * each, all signalled on one mbarrier); 0 restores the automatic size
+ * (64 KB).  Values outside 0 or
  * [1024, 131072] are AR_ERR_INVALID_ARG.  A tuning control: results are
  * identical for every value.
  */
 ARFUSE_API ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes);
 
+/*
+ * Cap the producer warps of the streaming kernels (1..4; 0 restores the
+ * automatic count, up to four and at most one per ring slot).  Each producer
+ * warp fills its own ring slots; a bulk copy holds the warp that issues it
+ * for about one memory latency, so more warps keep more slots in flight.
+ * Other values are AR_ERR_INVALID_ARG.  A tuning control: results are
+ * identical for every value.
+ */
+ARFUSE_API ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps);
+
 /* Regime (AR_REGIME_CLUSTER / _STREAM / _ONESHOT / _SPLIT) of the last
- * launched call, 0 before the first one.  *ctas receives the CTAs per row
+ * launched call (on a dry-run workspace: of the last validated call), 0
+ * before the first one.  *ctas receives the CTAs per row
  * (cluster, one-shot and split regimes) or the persistent grid size (stream
  * regime); may be NULL. */
 ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
+
+/*
+ * Regime table: the kernel regime (and CTAs per row) that AR_REGIME_AUTO runs
+ * at each token count.  The fastest regime depends on T and on the shape, and
+ * crossovers measured at one hidden size do not carry over to another
+ * (sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and wire it for
+ * DeepSeek-V3 / GLM-5.x", Known gaps and Related: the shipped bounds did not
+ * transfer from H = 8192 to H = 6144, so tuning is per shape).
+ *
+ * A table is at most AR_MAX_REGIME_RULES rules with strictly ascending
+ * max_tokens >= 1; a call with T tokens takes the first rule with
+ * T <= max_tokens.  regime is AR_REGIME_CLUSTER, _STREAM, _ONESHOT or _SPLIT,
+ * or AR_REGIME_AUTO for the built-in heuristic over that range; ctas_per_row
+ * is 0 (the regime's own choice) or, for the cluster and split regimes,
+ * 2..16.  A call past the last rule, or one whose rule has no launch plan for
+ * it (a cluster size the device cannot co-schedule, a row too long for the
+ * split kernel), runs the heuristic.  A regime forced with
+ * ar_workspace_set_regime takes precedence over the table.  Results are
+ * identical under every table.
+ *
+ * ar_workspace_create installs a table measured on GB300 when (ranks, top_k,
+ * hidden) is one of the shapes the library carries one for, else none.
+ * ar_workspace_set_regime_table replaces it (rules: host array of n rules,
+ * copied; n = 0 removes the table).  An invalid table is AR_ERR_INVALID_ARG
+ * and leaves the previous one in place.  ar_workspace_get_regime_table copies
+ * up to cap rules into rules (host) and stores the table's length in *n
+ * (rules may be NULL when cap is 0).  The Python module
+ * tp_reduce_moe_gb300.tune measures a table for any shape on the GPU at hand.
+ */
+typedef struct ar_regime_rule {
+    int64_t max_tokens;
+    int32_t regime;        /* AR_REGIME_* */
+    int32_t ctas_per_row;  /* 0, or 2..16 for AR_REGIME_CLUSTER / AR_REGIME_SPLIT */
+} ar_regime_rule;
+#define AR_MAX_REGIME_RULES 32
+ARFUSE_API ar_status ar_workspace_set_regime_table(ar_workspace* ws, const ar_regime_rule* rules,
+                                                   int n);
+ARFUSE_API ar_status ar_workspace_get_regime_table(const ar_workspace* ws, ar_regime_rule* rules,
+                                                   int cap, int* n);
 
 /*
  * ar_finalize_rmsnorm_noalloc -- the fused op for callers that cannot allocate

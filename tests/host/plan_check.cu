@@ -33,14 +33,17 @@ int main() {
       if (p.smem > 232448) bad = true;
       if (stream_ring_offset(g.nstages) + g.nstages * g.slot_bytes > p.smem) bad = true;
       if (p.grid % C) bad = true;
-      if (p.threads > 544 || p.threads % 32) bad = true;
+      if (p.threads > 640 || p.threads % 32) bad = true;
       if (g.nstages < 2) bad = true;
+      // every producer warp owns at least one slot
+      if (g.producers < 1 || g.producers > 4 || g.producers > g.nstages) bad = true;
       if (g.seg_per_stage < 1 || g.seg_per_stage > 32 || g.seg_per_stage > nseg) bad = true;
       if (g.slot_bytes != kSlotHeader + g.seg_per_stage * g.seg_stride) bad = true;
       if (g.seg_per_stage * 4 > kSlotHeader) bad = true;
       // the tx bytes of one slot fit an mbarrier's transaction count
       if ((long)g.seg_per_stage * g.seg_stride >= (1 << 20)) bad = true;
-      int ncw = p.threads / 32 - 1, nct = ncw * 32;
+      int ncw = p.threads / 32 - g.producers, nct = ncw * 32;
+      if (ncw < 1) bad = true;
       for (int c = 0; c < C; ++c) {
         int chunk0 = c * g.tile_chunks;
         int nchunk = std::min(g.tile_chunks, chunks - chunk0);

@@ -231,12 +231,15 @@ def test_ar_rmsnorm_validation(lib):
 
 
 def test_regime_setter(lib, ws):
+    assert arf.ar_workspace_last_regime(ws) == (0, 0)     # nothing planned yet
     for r in (arf.AR_REGIME_AUTO, arf.AR_REGIME_CLUSTER, arf.AR_REGIME_STREAM, arf.AR_REGIME_ONESHOT):
         arf.ar_workspace_set_regime(ws, r)
         assert Fake().call(lib, ws) == arf.AR_VALIDATED
+        if r != arf.AR_REGIME_AUTO:                       # a dry run records its plan
+            assert arf.ar_workspace_last_regime(ws)[0] == r
     with pytest.raises(arf.ArfuseError):
         arf.ar_workspace_set_regime(ws, 7)
-    assert arf.ar_workspace_last_regime(ws) == (0, 0)     # nothing launched
+    assert arf.ar_workspace_last_regime(ws)[0] == arf.AR_REGIME_ONESHOT
 
 
 def test_cluster_size_setter(lib, ws):
@@ -256,6 +259,15 @@ def test_stage_bytes_setter(lib, ws):
     for b in (-1, 1023, 131073):
         with pytest.raises(arf.ArfuseError):
             arf.ar_workspace_set_stage_bytes(ws, b)
+
+
+def test_producer_warps_setter(lib, ws):
+    for n in (0, 1, 2, 3, 4):
+        arf.ar_workspace_set_producer_warps(ws, n)
+        assert Fake().call(lib, ws) == arf.AR_VALIDATED
+    for n in (-1, 5, 32):
+        with pytest.raises(arf.ArfuseError):
+            arf.ar_workspace_set_producer_warps(ws, n)
 
 
 def test_cluster_regime_needs_two_chunks(lib):

@@ -499,3 +499,26 @@ def test_every_split_cluster_size(cfg, T):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+@pytest.mark.parametrize("cfg,T,split_c", [("glm_gemma", 8, 8), ("tiny", 4, 4)])
+def test_regime_table_routes_calls(cfg, T, split_c):
+    """AR_REGIME_AUTO under a regime table runs the rule's regime and cluster
+    size, with the same results as every other regime."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        for regime, ctas in ((arf.AR_REGIME_STREAM, 0), (arf.AR_REGIME_CLUSTER, 4),
+                             (arf.AR_REGIME_ONESHOT, 0), (arf.AR_REGIME_SPLIT, split_c)):
+            arf.ar_workspace_set_regime_table(ws, [(T, regime, ctas)])
+            out, r_out = run_gpu(ws, d, fp32=True)
+            torch.cuda.synchronize()
+            got = arf.ar_workspace_last_regime(ws)
+            assert got[0] == regime and (ctas == 0 or got[1] == ctas), (regime, ctas, got)
+            check_bf16(out, ref["out"], f"table {cfg} T={T} regime={regime} out")
+            check_f32(r_out, ref["h"], ref["abs"], f"table {cfg} T={T} regime={regime} residual_out")
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()

@@ -1,0 +1,149 @@
+"""Host-side tests of the regime table (no GPU needed).
+
+A dry-run workspace plans every call and records the regime it would launch
+(ar_workspace_last_regime) without touching a device, so the table's lookup,
+its precedence rules and its fallback to the heuristic can be checked here;
+results under every table are identical, which the GPU parity tests check
+for each regime.
+"""
+import pytest
+
+import tp_reduce_moe_gb300 as arf
+
+SPACING = 1 << 28          # fake device addresses, far apart, 16-byte aligned
+BASE = 1 << 44
+EPS = 1e-6
+
+
+class Shape:
+    def __init__(self, R, K, H, max_tokens=512):
+        self.R, self.K, self.H = R, K, H
+        self.ws = arf.ar_workspace_create(R, K, H, max_tokens, EPS, flags=arf.AR_WS_DRY_RUN)
+        a = iter(range(BASE, BASE + 64 * SPACING, SPACING))
+        self.E = [next(a) for _ in range(R)]
+        self.S = [next(a) for _ in range(R)]
+        self.perm, self.w, self.res, self.gamma, self.out, self.rout = (next(a) for _ in range(6))
+
+    def plan(self, T):
+        """Validate a call with T tokens; returns (regime, ctas) it would launch."""
+        if self.K == 0:
+            arf.ar_rmsnorm(self.ws, self.S, self.res, self.gamma, 0.0, EPS, out=self.out,
+                           residual_out=self.rout, T=T)
+        else:
+            arf.ar_finalize_rmsnorm(self.ws, self.E, self.perm, self.w, self.S, self.res, self.gamma,
+                                    0.0, EPS, out=self.out, residual_out=self.rout, rows_e=T * self.K,
+                                    T=T)
+        return arf.ar_workspace_last_regime(self.ws)
+
+
+@pytest.fixture()
+def dsv3():
+    s = Shape(8, 8, 7168)
+    yield s
+    s.ws.destroy()
+
+
+def test_builtin_table_is_installed_for_measured_shapes(dsv3):
+    rules = arf.ar_workspace_get_regime_table(dsv3.ws)
+    assert len(rules) >= 2
+    assert [t for t, _, _ in rules] == sorted({t for t, _, _ in rules})
+    other = Shape(3, 5, 1024)
+    try:
+        assert arf.ar_workspace_get_regime_table(other.ws) == []
+    finally:
+        other.ws.destroy()
+
+
+def test_table_rules_are_followed(dsv3):
+    arf.ar_workspace_set_regime_table(dsv3.ws, [
+        (2, arf.AR_REGIME_SPLIT, 8),
+        (40, arf.AR_REGIME_CLUSTER, 4),
+        (100, arf.AR_REGIME_STREAM, 0),
+    ])
+    assert dsv3.plan(1) == (arf.AR_REGIME_SPLIT, 8)
+    assert dsv3.plan(2) == (arf.AR_REGIME_SPLIT, 8)
+    assert dsv3.plan(3) == (arf.AR_REGIME_CLUSTER, 4)
+    assert dsv3.plan(40) == (arf.AR_REGIME_CLUSTER, 4)
+    regime, grid = dsv3.plan(41)
+    assert regime == arf.AR_REGIME_STREAM and grid == 41  # one CTA per row below the SM count
+
+
+def test_past_the_last_rule_and_auto_rules_use_the_heuristic(dsv3):
+    arf.ar_workspace_set_regime_table(dsv3.ws, [])
+    heuristic = {T: dsv3.plan(T) for T in (1, 4, 16, 64, 300)}
+    arf.ar_workspace_set_regime_table(dsv3.ws, [(8, arf.AR_REGIME_STREAM, 0),
+                                                (32, arf.AR_REGIME_AUTO, 0)])
+    assert dsv3.plan(4)[0] == arf.AR_REGIME_STREAM
+    assert dsv3.plan(16) == heuristic[16]      # AUTO rule
+    assert dsv3.plan(64) == heuristic[64]      # past the last rule
+    assert dsv3.plan(300) == heuristic[300]
+
+
+def test_rule_without_a_plan_falls_back(dsv3):
+    arf.ar_workspace_set_regime_table(dsv3.ws, [])
+    h1 = dsv3.plan(1)
+    # 81 segments over a 2-CTA split cluster is 41 per CTA: beyond the split
+    # kernel's 32 producer lanes, so the rule has no plan
+    arf.ar_workspace_set_regime_table(dsv3.ws, [(4, arf.AR_REGIME_SPLIT, 2)])
+    assert dsv3.plan(1) == h1
+
+
+def test_forced_regime_takes_precedence(dsv3):
+    arf.ar_workspace_set_regime_table(dsv3.ws, [(512, arf.AR_REGIME_STREAM, 0)])
+    arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_CLUSTER)
+    arf.ar_workspace_set_cluster_size(dsv3.ws, 8)
+    assert dsv3.plan(4) == (arf.AR_REGIME_CLUSTER, 8)
+    arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_AUTO)
+    assert dsv3.plan(4)[0] == arf.AR_REGIME_STREAM
+
+
+@pytest.mark.parametrize("rules", [
+    [(0, arf.AR_REGIME_STREAM, 0)],                                  # max_tokens < 1
+    [(8, arf.AR_REGIME_STREAM, 0), (8, arf.AR_REGIME_SPLIT, 0)],     # not strictly ascending
+    [(8, arf.AR_REGIME_STREAM, 0), (4, arf.AR_REGIME_SPLIT, 0)],
+    [(8, 9, 0)],                                                     # unknown regime
+    [(8, arf.AR_REGIME_STREAM, 4)],                                  # ctas for a regime without
+    [(8, arf.AR_REGIME_ONESHOT, 2)],
+    [(8, arf.AR_REGIME_CLUSTER, 1)],                                 # ctas out of range
+    [(8, arf.AR_REGIME_SPLIT, 17)],
+    [(t + 1, arf.AR_REGIME_STREAM, 0) for t in range(arf.AR_MAX_REGIME_RULES + 1)],  # too long
+])
+def test_invalid_tables_are_rejected_and_keep_the_old_one(dsv3, rules):
+    before = arf.ar_workspace_get_regime_table(dsv3.ws)
+    with pytest.raises(arf.ArfuseError) as e:
+        arf.ar_workspace_set_regime_table(dsv3.ws, rules)
+    assert e.value.status == arf.AR_ERR_INVALID_ARG
+    assert arf.ar_workspace_get_regime_table(dsv3.ws) == before
+
+
+def test_table_round_trip(dsv3):
+    rules = [(t, arf.AR_REGIME_CLUSTER, 2 << (t % 4)) for t in range(1, arf.AR_MAX_REGIME_RULES + 1)]
+    arf.ar_workspace_set_regime_table(dsv3.ws, rules)
+    assert arf.ar_workspace_get_regime_table(dsv3.ws) == rules
+
+
+def test_get_with_small_capacity(lib_handle=None):
+    import ctypes
+    s = Shape(8, 8, 7168)
+    try:
+        lib = arf.load_library()
+        n = ctypes.c_int(-1)
+        assert lib.ar_workspace_get_regime_table(ctypes.c_void_p(s.ws.handle), None, 0,
+                                                 ctypes.byref(n)) == arf.AR_OK
+        assert n.value == len(arf.ar_workspace_get_regime_table(s.ws))
+        assert lib.ar_workspace_get_regime_table(None, None, 0, ctypes.byref(n)) == arf.AR_ERR_INVALID_ARG
+        assert lib.ar_workspace_get_regime_table(ctypes.c_void_p(s.ws.handle), None, 1,
+                                                 ctypes.byref(n)) == arf.AR_ERR_INVALID_ARG
+        assert lib.ar_workspace_set_regime_table(ctypes.c_void_p(s.ws.handle), None, 1) == \
+            arf.AR_ERR_INVALID_ARG
+    finally:
+        s.ws.destroy()
+
+
+def test_k0_table_selects_oneshot_then_stream():
+    s = Shape(2, 0, 7168)
+    try:
+        assert s.plan(8)[0] == arf.AR_REGIME_ONESHOT
+        assert s.plan(200)[0] == arf.AR_REGIME_STREAM
+    finally:
+        s.ws.destroy()

@@ -84,6 +84,12 @@ def load_library(path: str | None = None):
         lib.ar_workspace_set_regime.argtypes = [P, I]
         lib.ar_workspace_set_stage_bytes.restype = I
         lib.ar_workspace_set_stage_bytes.argtypes = [P, I]
+        lib.ar_workspace_set_producer_warps.restype = I
+        lib.ar_workspace_set_producer_warps.argtypes = [P, I]
+        lib.ar_workspace_set_regime_table.restype = I
+        lib.ar_workspace_set_regime_table.argtypes = [P, P, I]
+        lib.ar_workspace_get_regime_table.restype = I
+        lib.ar_workspace_get_regime_table.argtypes = [P, P, I, ctypes.POINTER(I)]
         lib.ar_workspace_set_cluster_size.restype = I
         lib.ar_workspace_set_cluster_size.argtypes = [P, I]
         lib.ar_workspace_last_regime.restype = I
@@ -160,6 +166,43 @@ def ar_workspace_set_stage_bytes(ws: Workspace, nbytes: int) -> None:
     """Target ring-slot size of the streaming kernels (tuning); 0 = automatic."""
     _check(load_library().ar_workspace_set_stage_bytes(ctypes.c_void_p(ws.handle), int(nbytes)),
            "ar_workspace_set_stage_bytes")
+
+
+class RegimeRule(ctypes.Structure):
+    """One rule of a regime table (``ar_regime_rule``)."""
+    _fields_ = [("max_tokens", ctypes.c_int64), ("regime", ctypes.c_int32),
+                ("ctas_per_row", ctypes.c_int32)]
+
+
+AR_MAX_REGIME_RULES = 32
+
+
+def ar_workspace_set_regime_table(ws: Workspace, rules) -> None:
+    """Replace the workspace's regime table: ``[(max_tokens, regime, ctas_per_row), ...]``
+    with strictly ascending max_tokens (empty: heuristic only)."""
+    rules = list(rules)
+    arr = (RegimeRule * max(1, len(rules)))(*[RegimeRule(int(t), int(r), int(c)) for t, r, c in rules])
+    _check(load_library().ar_workspace_set_regime_table(ctypes.c_void_p(ws.handle),
+                                                        ctypes.cast(arr, ctypes.c_void_p), len(rules)),
+           "ar_workspace_set_regime_table")
+
+
+def ar_workspace_get_regime_table(ws: Workspace):
+    """The workspace's regime table as ``[(max_tokens, regime, ctas_per_row), ...]``."""
+    arr = (RegimeRule * AR_MAX_REGIME_RULES)()
+    n = ctypes.c_int(0)
+    _check(load_library().ar_workspace_get_regime_table(ctypes.c_void_p(ws.handle),
+                                                        ctypes.cast(arr, ctypes.c_void_p),
+                                                        AR_MAX_REGIME_RULES, ctypes.byref(n)),
+           "ar_workspace_get_regime_table")
+    return [(int(arr[i].max_tokens), int(arr[i].regime), int(arr[i].ctas_per_row))
+            for i in range(min(n.value, AR_MAX_REGIME_RULES))]
+
+
+def ar_workspace_set_producer_warps(ws: Workspace, warps: int) -> None:
+    """Cap the streaming kernels' producer warps (1..4; tuning); 0 = automatic."""
+    _check(load_library().ar_workspace_set_producer_warps(ctypes.c_void_p(ws.handle), int(warps)),
+           "ar_workspace_set_producer_warps")
 
 
 def ar_workspace_last_regime(ws: Workspace):

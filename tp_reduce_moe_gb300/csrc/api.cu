@@ -32,8 +32,11 @@ struct ar_workspace {
     int regime_force;
     int force_ctas_per_row;  // 0: automatic
     int stage_bytes;         // 0: automatic
+    int producer_warps;      // 0: automatic
     int last_regime;
     int last_ctas;
+    int table_n;  // rules in `table` (0: heuristic only)
+    ar_regime_rule table[AR_MAX_REGIME_RULES];
 };
 
 namespace {
@@ -54,6 +57,127 @@ Range range_of(const void* p, int64_t bytes) {
 }
 
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+// Regime tables measured on GB300 (tp_reduce_moe_gb300.tune: every regime and
+// cluster size, L2-cold, T = 1..256), installed for these shapes at create.
+struct BuiltinTable {
+    int R, K, H, n;
+    ar_regime_rule rules[6];
+};
+const BuiltinTable kBuiltinTables[] = {
+    // DeepSeek-V3 decode, TP8 (H = 7168, top-8)
+    {8, 8, 7168, 5,
+     {{4, AR_REGIME_SPLIT, 16}, {12, AR_REGIME_SPLIT, 8}, {32, AR_REGIME_CLUSTER, 8},
+      {64, AR_REGIME_CLUSTER, 4}, {256, AR_REGIME_STREAM, 0}}},
+    // DeepSeek-V3 decode, TP4
+    {4, 8, 7168, 5,
+     {{4, AR_REGIME_SPLIT, 16}, {12, AR_REGIME_SPLIT, 8}, {16, AR_REGIME_CLUSTER, 8},
+      {64, AR_REGIME_CLUSTER, 4}, {256, AR_REGIME_STREAM, 0}}},
+    // GLM-style decode, TP8 (H = 6144, top-8)
+    {8, 8, 6144, 5,
+     {{4, AR_REGIME_SPLIT, 16}, {12, AR_REGIME_SPLIT, 8}, {32, AR_REGIME_CLUSTER, 8},
+      {64, AR_REGIME_CLUSTER, 4}, {256, AR_REGIME_STREAM, 0}}},
+    // H = 8192, top-10, TP8
+    {8, 10, 8192, 4,
+     {{4, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 2},
+      {256, AR_REGIME_STREAM, 0}}},
+    // trailing all-reduce + RMSNorm, two partials (K = 0)
+    {2, 0, 7168, 2, {{96, AR_REGIME_ONESHOT, 0}, {256, AR_REGIME_STREAM, 0}}},
+};
+
+bool valid_regime(int r) {
+    return r == AR_REGIME_AUTO || r == AR_REGIME_CLUSTER || r == AR_REGIME_STREAM ||
+           r == AR_REGIME_ONESHOT || r == AR_REGIME_SPLIT;
+}
+
+bool valid_table(const ar_regime_rule* rules, int n) {
+    if (n < 0 || n > AR_MAX_REGIME_RULES || (n > 0 && !rules)) return false;
+    for (int i = 0; i < n; ++i) {
+        const ar_regime_rule& r = rules[i];
+        if (r.max_tokens < 1 || (i > 0 && r.max_tokens <= rules[i - 1].max_tokens)) return false;
+        if (!valid_regime(r.regime)) return false;
+        if (r.ctas_per_row != 0) {
+            if (r.regime != AR_REGIME_CLUSTER && r.regime != AR_REGIME_SPLIT) return false;
+            if (r.ctas_per_row < 2 || r.ctas_per_row > 16) return false;
+        }
+    }
+    return true;
+}
+
+// The built-in table for the workspace's shape, if the library has one.
+void install_builtin_table(ar_workspace* ws) {
+    ws->table_n = 0;
+    for (const BuiltinTable& b : kBuiltinTables)
+        if (b.R == ws->R && b.K == ws->K && b.H == ws->H) {
+            ws->table_n = b.n;
+            for (int i = 0; i < b.n; ++i) ws->table[i] = b.rules[i];
+        }
+}
+
+struct Plans {
+    arf::ClusterPlan c{};
+    arf::StreamPlan s{};
+    arf::SplitPlan x{};
+};
+
+// Plan `regime` with `ctas` CTAs per row (0: the regime's own choice).
+// Returns the regime that will run (a streaming plan reports CLUSTER when its
+// rows are split over a cluster, STREAM otherwise), 0 when there is no plan.
+int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int H, bool shared,
+                int64_t T, Plans* p) {
+    switch (regime) {
+        case AR_REGIME_ONESHOT:
+            return arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c)
+                       ? AR_REGIME_ONESHOT
+                       : 0;
+        case AR_REGIME_SPLIT:
+            // the given cluster size, else the largest that fits
+            for (int c = ctas ? ctas : 16; c >= 2; c = ctas ? 0 : c >> 1)
+                if (arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                         ws->max_cluster_split, c, &p->x))
+                    return AR_REGIME_SPLIT;
+            return 0;
+        case AR_REGIME_STREAM:
+        case AR_REGIME_CLUSTER: {
+            int C = regime == AR_REGIME_STREAM ? 1 : ctas;
+            if (C == 0) {
+                arf::StreamPlan probe{};
+                if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                           ws->max_cluster_stream, 0, ws->stage_bytes, &probe,
+                                           ws->producer_warps))
+                    return 0;
+                C = probe.geo.C > 1 ? probe.geo.C : 2;
+            }
+            if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                       ws->max_cluster_stream, C, ws->stage_bytes, &p->s,
+                                       ws->producer_warps))
+                return 0;
+            return p->s.geo.C > 1 ? AR_REGIME_CLUSTER : AR_REGIME_STREAM;
+        }
+    }
+    return 0;
+}
+
+// The built-in choice (measured on GB300 with bench.py's sweep):
+//  - light rows (at most 8 summands per 16-byte chunk, one load wave per
+//    thread) below one row per two SMs: the one-shot kernel;
+//  - heavy rows at the smallest T (one cluster per row fits in half the
+//    SMs): the split kernel, fewest bulk copies per CTA;
+//  - otherwise the streaming kernel (tiles over a cluster for small T, whole
+//    rows for large T).
+int plan_heuristic(const ar_workspace* ws, int R, int K, int H, bool shared, int64_t T, Plans* p) {
+    const int summands = (shared ? R : 0) + R * K;
+    if (summands <= 8 && 2 * T < ws->num_sms &&
+        arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c))
+        return AR_REGIME_ONESHOT;
+    if (summands > 8 && arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                             ws->max_cluster_split, 0, &p->x))
+        return AR_REGIME_SPLIT;
+    if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                               ws->max_cluster_stream, 0, ws->stage_bytes, &p->s, ws->producer_warps))
+        return 0;
+    return p->s.geo.C > 1 ? AR_REGIME_CLUSTER : AR_REGIME_STREAM;
+}
 
 ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int32_t* perm,
               const float* w, const void* const* S, const void* residual, const void* gamma,
@@ -118,64 +242,35 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     if (overlap(r_out, r_res)) return AR_ERR_INVALID_ARG;
     if (!inplace && overlap(r_rout, r_res)) return AR_ERR_INVALID_ARG;
 
-    // Regime and launch plan.
+    // Regime and launch plan: a forced regime, else the table's rule for T,
+    // else (no rule, or no plan for it) the heuristic.
     const bool shared = S != nullptr;
-    int regime = ws->regime_force;
-    arf::ClusterPlan cplan{};
-    arf::StreamPlan splan{};
-    arf::SplitPlan xplan{};
-    if (regime == AR_REGIME_AUTO) {
-        // Measured on GB300 (bench.py sweep):
-        //  - light rows (at most 8 summands per 16-byte chunk, one load wave
-        //    per thread) below one row per two SMs: the one-shot kernel;
-        //  - heavy rows at the smallest T (one cluster per row fits in half
-        //    the SMs): the split kernel, fewest bulk copies per CTA;
-        //  - otherwise the streaming kernel (tiles over a cluster for small
-        //    T, whole rows for large T).
-        const int summands = (shared ? R : 0) + R * K;
-        if (summands <= 8 && 2 * T < ws->num_sms &&
-            arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &cplan))
-            regime = AR_REGIME_ONESHOT;
-        else if (summands > 8 && arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                                      ws->max_cluster_split, 0, &xplan))
-            regime = AR_REGIME_SPLIT;
-    }
-    if (regime == AR_REGIME_ONESHOT) {
-        if (!cplan.C && !arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &cplan))
-            return AR_ERR_UNSUPPORTED;
-    } else if (regime == AR_REGIME_SPLIT) {
-        if (!xplan.geo.C) {
-            // forced: the given cluster size, else the largest that fits
-            int C = ws->force_ctas_per_row;
-            if (C == 0)
-                for (int c = 16; c >= 2 && C == 0; c >>= 1)
-                    if (arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                             ws->max_cluster_split, c, &xplan))
-                        C = c;
-            if (C == 0 || !arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                                ws->max_cluster_split, C, &xplan))
-                return AR_ERR_UNSUPPORTED;
-        }
+    Plans pl;
+    int regime = 0;
+    if (ws->regime_force != AR_REGIME_AUTO) {
+        regime = plan_regime(ws, ws->regime_force, ws->force_ctas_per_row, R, K, H, shared, T, &pl);
+        if (!regime) return AR_ERR_UNSUPPORTED;
     } else {
-        int C = 0;  // automatic
-        if (regime == AR_REGIME_STREAM) C = 1;
-        if (regime == AR_REGIME_CLUSTER) {
-            C = ws->force_ctas_per_row;
-            if (C == 0) {
-                arf::StreamPlan probe{};
-                if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                           ws->max_cluster_stream, 0, ws->stage_bytes, &probe))
-                    return AR_ERR_UNSUPPORTED;
-                C = probe.geo.C > 1 ? probe.geo.C : 2;
+        for (int i = 0; i < ws->table_n; ++i)
+            if (T <= ws->table[i].max_tokens) {
+                if (ws->table[i].regime != AR_REGIME_AUTO)
+                    regime = plan_regime(ws, ws->table[i].regime, ws->table[i].ctas_per_row, R, K, H,
+                                         shared, T, &pl);
+                break;
             }
-        }
-        if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                   ws->max_cluster_stream, C, ws->stage_bytes, &splan))
-            return AR_ERR_UNSUPPORTED;
-        regime = splan.geo.C > 1 ? AR_REGIME_CLUSTER : AR_REGIME_STREAM;
+        if (!regime) regime = plan_heuristic(ws, R, K, H, shared, T, &pl);
+        if (!regime) return AR_ERR_UNSUPPORTED;
     }
+    const int ctas = regime == AR_REGIME_ONESHOT ? pl.c.C
+                     : regime == AR_REGIME_SPLIT ? pl.x.geo.C
+                     : regime == AR_REGIME_CLUSTER ? pl.s.geo.C
+                                                   : pl.s.grid;
 
-    if (ws->flags & AR_WS_DRY_RUN) return AR_VALIDATED;
+    if (ws->flags & AR_WS_DRY_RUN) {
+        ws->last_regime = regime;
+        ws->last_ctas = ctas;
+        return AR_VALIDATED;
+    }
 
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return AR_ERR_CUDA;
@@ -207,17 +302,12 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    int ctas;
-    if (regime == AR_REGIME_ONESHOT) {
-        e = arf::launch_cluster_rows(a, cplan, res_f32 != 0, s);
-        ctas = cplan.C;
-    } else if (regime == AR_REGIME_SPLIT) {
-        e = arf::launch_split_rows(a, xplan, res_f32 != 0, s);
-        ctas = xplan.geo.C;
-    } else {
-        e = arf::launch_stream_rows(a, splan, res_f32 != 0, s);
-        ctas = regime == AR_REGIME_CLUSTER ? splan.geo.C : splan.grid;
-    }
+    if (regime == AR_REGIME_ONESHOT)
+        e = arf::launch_cluster_rows(a, pl.c, res_f32 != 0, s);
+    else if (regime == AR_REGIME_SPLIT)
+        e = arf::launch_split_rows(a, pl.x, res_f32 != 0, s);
+    else
+        e = arf::launch_stream_rows(a, pl.s, res_f32 != 0, s);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ERR_CUDA;
@@ -255,8 +345,10 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
     ws->regime_force = AR_REGIME_AUTO;
     ws->force_ctas_per_row = 0;
     ws->stage_bytes = 0;
+    ws->producer_warps = 0;
     ws->last_regime = 0;
     ws->last_ctas = 0;
+    install_builtin_table(ws);
 
     if (flags & AR_WS_DRY_RUN) {
         ws->num_sms = kDryRunSms;
@@ -418,6 +510,28 @@ ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes) {
     return AR_OK;
 }
 
+ar_status ar_workspace_set_regime_table(ar_workspace* ws, const ar_regime_rule* rules, int n) {
+    if (!ws || !valid_table(rules, n)) return AR_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) ws->table[i] = rules[i];
+    ws->table_n = n;
+    return AR_OK;
+}
+
+ar_status ar_workspace_get_regime_table(const ar_workspace* ws, ar_regime_rule* rules, int cap,
+                                        int* n) {
+    if (!ws || !n || cap < 0 || (cap > 0 && !rules)) return AR_ERR_INVALID_ARG;
+    for (int i = 0; i < ws->table_n && i < cap; ++i) rules[i] = ws->table[i];
+    *n = ws->table_n;
+    return AR_OK;
+}
+
+ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps) {
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (warps < 0 || warps > 4) return AR_ERR_INVALID_ARG;
+    ws->producer_warps = warps;
+    return AR_OK;
+}
+
 int ar_workspace_last_regime(const ar_workspace* ws, int* ctas) {
     if (!ws) return 0;
     if (ctas) *ctas = ws->last_ctas;
@@ -549,6 +663,7 @@ ar_status ar_finalize_rmsnorm_noalloc(const void* const* expert_out, int64_t row
     ws.max_cluster_stream = d->max_cluster_stream;
     ws.max_cluster_split = d->max_cluster_split;
     ws.regime_force = AR_REGIME_AUTO;
+    install_builtin_table(&ws);
     ar_status v = run(&ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma,
                       weight_bias, eps, T, R, K, H, out, residual_out, residual_out_is_fp32,
                       stream, true);

@@ -321,21 +321,23 @@ struct StreamGeom {
     int seg_stride;   // bytes between the segments of a slot (>= tile bytes, multiple of 128)
     int C;            // CTAs per token row (cluster size); 1 = whole rows per CTA
     int tile_chunks;  // 16-byte column chunks per CTA tile (the row's last tile may be shorter)
+    int producers;    // producer warps (slot q is filled by warp q % producers)
 };
 
 struct StreamPlan {
     StreamGeom geo;
     int cpt;          // 16-byte chunks per consumer thread
-    int threads;      // producer warp + consumer warps
+    int threads;      // producer warps + consumer warps
     int smem;         // dynamic shared memory bytes
     int grid;         // CTAs (a multiple of C)
 };
 
 // Plan a stream_rows launch for T rows.  C = 0 picks the CTAs per row from T
 // and the SM count; C >= 1 forces it.  stage_bytes = 0 picks the slot size,
-// otherwise it is the target.  Returns false if no plan fits.
+// otherwise it is the target.  producers = 0 picks the producer warps (up to
+// four), otherwise it is the cap.  Returns false if no plan fits.
 bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
-                      int max_cluster, int C, int stage_bytes, StreamPlan* p);
+                      int max_cluster, int C, int stage_bytes, StreamPlan* p, int producers = 0);
 cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, bool res_f32,
                                cudaStream_t stream);
 cudaError_t stream_rows_set_attributes(int smem_optin);

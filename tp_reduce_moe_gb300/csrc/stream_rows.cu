@@ -7,11 +7,14 @@
 // thread-block cluster (C = 2..16, small T) -- and streams its tile of the
 // row's nseg segments through a ring of shared-memory slots:
 //
-//   * a producer warp issues one 1-D bulk async copy per segment
-//     (cp.async.bulk, the TMA engine's untiled form, L2 evict-first),
-//     completion counted as transaction bytes on the slot's `full` mbarrier;
-//     whole rows use one issuing lane, tiles use all 32 lanes so that the
-//     many small copies of a tile go out at once;
+//   * producer warps issue one 1-D bulk async copy per segment
+//     (cp.async.bulk, the TMA engine's untiled form, L2 evict-first), the
+//     copies of one slot from the lanes of one instruction, completion
+//     counted as transaction bytes on the slot's `full` mbarrier.  A bulk
+//     copy holds its issuing warp for about one memory latency (measured on
+//     GB300: ~0.6 us per instruction, whatever its size), so one warp alone
+//     fills one slot per latency; W producer warps take the slots
+//     round-robin and keep W slots in flight;
 //   * consumer warps fold each landed slot into fp32 accumulators held in
 //     registers (CPT 16-byte chunks per thread, U slots per step so several
 //     shared-memory loads are in flight), then release it on the slot's
@@ -44,7 +47,8 @@
 namespace arf {
 
 constexpr int kStreamMaxConsumers = 512;
-constexpr int kStreamMaxThreads = 32 + kStreamMaxConsumers;
+constexpr int kStreamMaxProducers = 4;
+constexpr int kStreamMaxThreads = 32 * kStreamMaxProducers + kStreamMaxConsumers;
 constexpr int kStreamMaxStages = 128;
 constexpr int kMaxCluster = 16;
 
@@ -93,7 +97,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int ncw = (blockDim.x >> 5) - 1;  // consumer warps
+    const int W = geo.producers;             // producer warps 0..W-1
+    const int ncw = (blockDim.x >> 5) - W;   // consumer warps
     const int C = CLUSTERED ? geo.C : 1;
     const uint32_t crank = CLUSTERED ? cluster_ctarank() : 0u;
     const int64_t first_row = blockIdx.x / C;
@@ -124,18 +129,21 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         cluster_wait_acquire();
     }
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        // One slot = up to P consecutive segments of one row, one bulk copy
-        // each, issued by lanes 0..cnt-1 and all counted on the slot's single
-        // `full` mbarrier (lane 0 arms it with the slot's total bytes).
+    if (warp < W) {
+        // ----------------------------------------------------------- producers
+        // The CTA's stages are numbered g = (row iteration) * nstage_row + j;
+        // stage g fills ring slot g % nst, and slot q belongs to producer warp
+        // q % W: each slot has one owner, which fills it in stage order (so
+        // its parity never runs more than one lap ahead of the consumers).  One slot = up to P consecutive segments
+        // of one row, one bulk copy each, issued by lanes 0..cnt-1 and all
+        // counted on the slot's single `full` mbarrier (lane 0 arms it with
+        // the slot's total bytes).
         const uint64_t pol = l2_evict_first_policy();
         const int64_t col = (int64_t)chunk0 * 8;
-        int slot = 0;
-        uint32_t phase = 0;
         bool ok = true;
         // Routing metadata one row ahead: lane k holds perm[t, k] of the row
-        // being issued and has the next row's value in flight.
+        // being issued and has the next row's value in flight (every
+        // producer warp keeps its own copy).
         int32_t raw_next = 0;
         float w_next = 0.0f;
         float gate_next = 0.0f;
@@ -144,13 +152,18 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
             w_next = __ldg(a.w + first_row * a.K + lane);
         }
         if (a.shared_gate && first_row < a.T) gate_next = __ldg(a.shared_gate + first_row);
-        for (int64_t t = first_row; t < a.T && ok; t += row_step) {
+        int64_t g0 = 0;  // stage number of the row's first stage
+        for (int64_t t = first_row; t < a.T && ok; t += row_step, g0 += nstage_row) {
             const int32_t raw = raw_next;
             const float my_w = w_next;
             const float s_coef = a.shared_gate ? 1.0f / (1.0f + expf(-gate_next)) : 1.0f;
             if (a.shared_gate && t + row_step < a.T) gate_next = __ldg(a.shared_gate + t + row_step);
-            int64_t my_row = -1;  // checked lazily, at the first routed stage
+            int64_t my_row = -1;  // checked lazily, at this warp's first routed stage
             for (int j = 0; j < nstage_row && ok; ++j) {
+                const int64_t g = g0 + j;
+                const int slot = (int)(g % nst);
+                if (slot % W != warp) continue;
+                const uint32_t phase = (uint32_t)((g / nst) & 1);
                 int s0, cnt;
                 stage_range(j, P, nS + 1, nseg, s0, cnt);
                 const int s = s0 + lane;
@@ -203,20 +216,16 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
                                  tile_bytes, smem_addr(&full[slot]), pol);
                     }
                 }
-                if (++slot == nst) {
-                    slot = 0;
-                    phase ^= 1u;
-                }
             }
-            if (my_row < 0 && lane < a.K && t + row_step < a.T) {  // row without routed stages
+            if (my_row < 0 && lane < a.K && t + row_step < a.T) {  // no routed stage of this row here
                 raw_next = __ldg(a.perm + (t + row_step) * a.K + lane);
                 w_next = __ldg(a.w + (t + row_step) * a.K + lane);
             }
         }
         // After an abort, wait (briefly, bounded) for every copy still landing
-        // in this CTA's shared memory before the CTA may exit.
+        // in this warp's slots before the CTA may exit.
         if (lane == 0 && *abort_flag) {
-            for (int j = 0; j < nst; ++j)
+            for (int j = warp; j < nst; j += W)
                 if (rec[j])
                     (void)mbar_wait_bounded(smem_addr(&full[j]), (uint32_t)(rec[j] - 1), nullptr,
                                             10000000ull);
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     }
 
     // -------------------------------------------------------------- consumers
-    const int ci = threadIdx.x - 32;
+    const int ci = threadIdx.x - 32 * W;
     const int nct = ncw * 32;
     int lch[CPT];
     bool valid[CPT];
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
             }
         }
         ss = warp_sum(ss);
-        if (lane == 0) red[par_row * 32 + (warp - 1)] = ss;
+        if (lane == 0) red[par_row * 32 + (warp - W)] = ss;
         named_barrier_sync(1, nct);
         float tot = 0.0f;
         for (int w = 0; w < ncw; ++w) tot += red[par_row * 32 + w];
@@ -406,12 +415,12 @@ static bool consumer_layout(int chunks, int* cpt, int* threads) {
     while (c < 4 && chunks > c * kStreamMaxConsumers) c <<= 1;
     if (chunks > c * kStreamMaxConsumers) return false;
     *cpt = c;
-    *threads = 32 * (ceil_div(ceil_div(chunks, c), 32) + 1);
+    *threads = 32 * ceil_div(ceil_div(chunks, c), 32);  // consumer threads
     return true;
 }
 
 bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
-                      int max_cluster, int C, int stage_bytes, StreamPlan* p) {
+                      int max_cluster, int C, int stage_bytes, StreamPlan* p, int producers) {
     const int chunks = H / 8;
     const int nseg = (shared ? R : 0) + 1 + R * K;
     if (chunks < 1 || T < 1) return false;
@@ -432,9 +441,12 @@ bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, 
     int cpt, threads;
     if (!consumer_layout(tile, &cpt, &threads)) return false;
     const int seg_stride = ceil_div(tile * 16, 128) * 128;
-    // Segments per slot: enough for a ~16 KB (tiles) / ~32 KB (whole rows)
-    // slot, at most one per producer lane, spread evenly over the row.
-    const int target = stage_bytes > 0 ? stage_bytes : (C == 1 ? 65536 : 16384);
+    // Segments per slot: enough for a ~64 KB slot, at most one per producer
+    // lane, spread evenly over the row.  Bulk copies are issued one slot per
+    // instruction and an instruction costs its warp about a memory latency
+    // whatever its size, so slots are made large (measured on GB300: 64 KB
+    // slots beat 16 KB ones for column tiles as well as whole rows).
+    const int target = stage_bytes > 0 ? stage_bytes : 65536;
     int P = target / seg_stride;
     if (P < 1) P = 1;
     if (P > 32) P = 32;
@@ -459,6 +471,11 @@ bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, 
         if (nst < 2) nst = 2;
     }
     if (nst < 2 || stream_ring_offset(nst) + nst * slot_bytes > smem_optin) return false;
+    // Producer warps: up to four (slot q is filled by warp q % W).
+    int W = nst < kStreamMaxProducers ? nst : kStreamMaxProducers;
+    if (producers > 0) W = producers < nst ? producers : nst;
+    if (W > kStreamMaxProducers || threads + 32 * W > kStreamMaxThreads) return false;
+    p->geo.producers = W;
     p->geo.nstages = nst;
     p->geo.slot_bytes = slot_bytes;
     p->geo.seg_per_stage = P;
@@ -466,7 +483,7 @@ bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, 
     p->geo.C = C;
     p->geo.tile_chunks = tile;
     p->cpt = cpt;
-    p->threads = threads;
+    p->threads = threads + 32 * W;
     p->smem = stream_ring_offset(nst) + nst * slot_bytes;
     if (C == 1) {
         p->grid = (int)(T < num_sms ? T : num_sms);

@@ -1,0 +1,186 @@
+"""Regime crossover tuning for one problem shape (R, K, H).
+
+The library has four launch regimes (whole-row streaming, tiled streaming over
+a cluster, the one-shot cluster kernel, the split-segment cluster kernel) and
+the best one depends on T and on the shape: the crossovers measured for one
+hidden size do not carry over to another.  ``tune`` times every regime (and
+every cluster size) through the public API on this GPU, L2-cold, at a ladder
+of token counts, and reduces the winners to the rule table that
+``ar_workspace_set_regime_table`` takes: ``[(max_tokens, regime,
+ctas_per_row), ...]`` in ascending ``max_tokens``; a call with T tokens runs
+the first rule with ``T <= max_tokens``.
+
+Timing: a CUDA graph of one call per input set, replayed; the sets are
+disjoint (each gathers only within its own block of expert rows) and together
+hold at least 3x the L2 cache, so every call reads HBM.  Input values are
+random (they do not affect the time); only their layout matters.
+
+    python -m tp_reduce_moe_gb300.tune --R 8 --K 8 --H 7168
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import statistics
+
+import torch
+
+from . import binding as arf
+
+DEFAULT_TOKENS = (1, 2, 4, 8, 12, 16, 24, 32, 48, 64, 96, 128, 192, 256)
+REGIME_NAME = {arf.AR_REGIME_AUTO: "auto", arf.AR_REGIME_CLUSTER: "cluster",
+               arf.AR_REGIME_STREAM: "stream", arf.AR_REGIME_ONESHOT: "oneshot",
+               arf.AR_REGIME_SPLIT: "split"}
+
+
+def candidates():
+    """Every (regime, ctas_per_row) the library accepts; 0 = its own choice."""
+    out = [(arf.AR_REGIME_STREAM, 0), (arf.AR_REGIME_ONESHOT, 0)]
+    out += [(arf.AR_REGIME_CLUSTER, c) for c in (2, 4, 8, 16)]
+    out += [(arf.AR_REGIME_SPLIT, c) for c in (2, 4, 8, 16)]
+    return out
+
+
+def problem_bytes(R: int, K: int, H: int, T: int, shared: bool = True) -> int:
+    """Algorithmic HBM bytes of one call with bf16 residual_out."""
+    return 2 * T * H * (R * K + (R if shared else 0) + 3)
+
+
+class _Inputs:
+    """n_sets disjoint input sets for T tokens, on `dev`."""
+
+    def __init__(self, R, K, H, T, shared, n_sets, dev, seed=0):
+        g = torch.Generator(device=dev).manual_seed(seed)
+        self.T, self.n = T, n_sets
+        rows = T * n_sets
+        bf = torch.bfloat16
+
+        def randn(*shape):
+            return torch.randn(*shape, generator=g, device=dev).to(bf)
+
+        self.E = [randn(rows * K, H) for _ in range(R)] if K else None
+        if K:
+            blocks = [torch.randperm(T * K, generator=g, device=dev) + i * T * K for i in range(n_sets)]
+            self.perm = torch.cat(blocks).view(rows, K).to(torch.int32)
+            self.w = torch.rand(rows, K, generator=g, device=dev)
+        self.S = [randn(rows, H) for _ in range(R)] if shared else None
+        self.residual = randn(rows, H)
+        self.gamma = (torch.rand(H, generator=g, device=dev) + 0.5).to(bf)
+        self.out = torch.empty(n_sets, T, H, dtype=bf, device=dev)
+        self.rout = torch.empty(n_sets, T, H, dtype=bf, device=dev)
+        self.rows_e = rows * K
+
+    def call(self, ws, i, eps, stream):
+        sl = slice(i * self.T, (i + 1) * self.T)
+        S = [x[sl] for x in self.S] if self.S is not None else None
+        if self.E is None:
+            arf.ar_rmsnorm(ws, S, self.residual[sl], self.gamma, 0.0, eps, out=self.out[i],
+                           residual_out=self.rout[i], stream=stream)
+        else:
+            arf.ar_finalize_rmsnorm(ws, self.E, self.perm[sl], self.w[sl], S, self.residual[sl],
+                                    self.gamma, 0.0, eps, out=self.out[i], residual_out=self.rout[i],
+                                    stream=stream, rows_e=self.rows_e)
+
+
+def time_regime(ws, inp: _Inputs, eps: float, regime: int, ctas: int, dev, reps: int = 3):
+    """Median µs per call of one forced (regime, ctas_per_row), or None when the
+    library has no plan for it.  Returns (us, regime_run, ctas_run)."""
+    arf.ar_workspace_set_regime(ws, regime)
+    arf.ar_workspace_set_cluster_size(ws, ctas)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    try:
+        with torch.cuda.stream(side):
+            for i in range(min(inp.n, 4)):
+                inp.call(ws, i, eps, side)
+    except arf.ArfuseError as e:
+        if e.status == arf.AR_ERR_UNSUPPORTED:
+            return None, regime, ctas
+        raise
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    ran = arf.ar_workspace_last_regime(ws)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream(dev)
+        for i in range(inp.n):
+            inp.call(ws, i, eps, cs)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    per = []
+    st = torch.cuda.current_stream(dev)
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        g.replay()
+        b.record(st)
+        torch.cuda.synchronize(dev)
+        per.append(a.elapsed_time(b) * 1e3 / inp.n)
+    del g
+    return statistics.median(per), ran[0], ran[1]
+
+
+def tune(R: int, K: int, H: int, tokens=DEFAULT_TOKENS, shared: bool = True, eps: float = 1e-6,
+         device: int = 0, cands=None, log=None):
+    """Time every candidate at every T; returns (rules, points).
+
+    rules: [(max_tokens, regime, ctas_per_row)], consecutive equal winners
+    merged; points: one dict per (T, candidate) with the measured µs.
+    """
+    dev = torch.device("cuda", device)
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    cands = list(cands or candidates())
+    points, winners = [], []
+    for T in sorted(set(int(t) for t in tokens)):
+        n_sets = int(min(4096, max(2, math.ceil(3 * l2 / problem_bytes(R, K, H, T, shared)))))
+        inp = _Inputs(R, K, H, T, shared, n_sets, dev)
+        ws = arf.ar_workspace_create(R, K, H, T, eps, device=device)
+        best = None
+        for regime, ctas in cands:
+            us, ran_regime, ran_ctas = time_regime(ws, inp, eps, regime, ctas, dev)
+            pt = {"T": T, "regime": REGIME_NAME[regime], "ctas_per_row": ctas, "us": us,
+                  "ran": [REGIME_NAME.get(ran_regime, "?"), ran_ctas]}
+            points.append(pt)
+            if log:
+                log(pt)
+            if us is not None and (best is None or us < best[0]):
+                best = (us, regime, ctas)
+        ws.destroy()
+        del inp
+        torch.cuda.empty_cache()
+        if best is not None:
+            winners.append((T, best[1], best[2]))
+    rules = []
+    for T, regime, ctas in winners:
+        if rules and rules[-1][1] == regime and rules[-1][2] == ctas:
+            rules[-1] = (T, regime, ctas)
+        else:
+            rules.append((T, regime, ctas))
+    return rules, points
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--R", type=int, required=True)
+    p.add_argument("--K", type=int, required=True)
+    p.add_argument("--H", type=int, required=True)
+    p.add_argument("--tokens", default=",".join(str(t) for t in DEFAULT_TOKENS))
+    p.add_argument("--no-shared", action="store_true", help="no shared-expert partials (K > 0 only)")
+    p.add_argument("--eps", type=float, default=1e-6)
+    p.add_argument("--device", type=int, default=0)
+    args = p.parse_args(argv)
+    shared = not args.no_shared or args.K == 0
+    rules, points = tune(args.R, args.K, args.H, [int(t) for t in args.tokens.split(",")],
+                         shared=shared, eps=args.eps, device=args.device)
+    print(json.dumps({"R": args.R, "K": args.K, "H": args.H, "shared": shared,
+                      "device": torch.cuda.get_device_name(args.device),
+                      "rules": [[t, REGIME_NAME[r], c] for t, r, c in rules],
+                      "points": points}))
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
