@@ -522,3 +522,34 @@ def test_regime_table_routes_calls(cfg, T, split_c):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 16), ("tiny", 400), ("ar_only", 128)])
+def test_tuning_controls_leave_results_unchanged(cfg, T):
+    """Producer warps and slot sizes change only who issues which bulk copy and
+    how copies are grouped, never the summation order: bitwise-identical
+    outputs for every setting, in both streaming regimes, and oracle parity."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        for regime, ctas in ((arf.AR_REGIME_STREAM, 0), (arf.AR_REGIME_CLUSTER, 4)):
+            arf.ar_workspace_set_cluster_size(ws, ctas)
+            base = None
+            for warps in (0, 1, 2, 3, 4):
+                for stage in (0, 4096, 32768):
+                    arf.ar_workspace_set_producer_warps(ws, warps)
+                    arf.ar_workspace_set_stage_bytes(ws, stage)
+                    out, r_out = run_gpu(ws, d, fp32=True, regime=regime)
+                    torch.cuda.synchronize()
+                    if base is None:
+                        base = (out.clone(), r_out.clone())
+                        check_bf16(out, ref["out"], f"{cfg} T={T} regime={regime} out")
+                        check_f32(r_out, ref["h"], ref["abs"], f"{cfg} T={T} regime={regime} residual_out")
+                    else:
+                        assert torch.equal(out, base[0]) and torch.equal(r_out, base[1]), \
+                            (regime, warps, stage)
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
