@@ -36,7 +36,8 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = ["CONFIGS", "Config", "make_inputs", "make_perm_decode_inputs",
-           "make_gate_logits", "bf16_bits", "problem_bytes"]
+           "make_gate_logits", "make_mhc_inputs", "MHC_SHAPES", "mhc_problem_bytes",
+           "bf16_bits", "problem_bytes"]
 
 
 @dataclass(frozen=True)
@@ -226,3 +227,38 @@ def make_perm_decode_inputs(R: int, K: int, H: int, T: int, hot_shift: int = 0,
     return dict(R=R, K=K, H=H, T=T, rows_e=rows_e, eps=1e-6, weight_bias=0.0,
                 E=E, perm=perm, w=w, S=S, residual=residual, gamma=gamma,
                 hot=hot, digits=D)
+
+
+# All-reduce + mHC residual write-back (hc_post): four residual streams, at
+# most 16 tokens in serving (sglang PR #42020, Summary and Scope; TP4 on the
+# page's MI355X runs).  Hidden sizes: 5120 (the other fused all-reduce +
+# hc_post the page mentions) and 6144 (GLM-5.x, sglang PR #37196, Known gaps).
+MHC_SHAPES = {"mhc_h5120": dict(R=4, H=5120, hc=4, Ts=(1, 2, 4, 8, 16)),
+              "mhc_h6144": dict(R=4, H=6144, hc=4, Ts=(1, 2, 4, 8, 16))}
+
+
+def mhc_problem_bytes(R: int, H: int, hc: int, T: int) -> int:
+    """Algorithmic HBM bytes of one all-reduce + hc_post call: R partials and hc
+    streams read, hc streams written (bf16; post/comb coefficients excluded)."""
+    return 2 * T * H * (R + 2 * hc)
+
+
+def make_mhc_inputs(R: int, H: int, hc: int, T: int, seed: int = 777, device="cpu"):
+    """Inputs for the all-reduce + mHC write-back.
+
+    partials P_r ~ N(0,1) and incoming streams x ~ N(0,1), both fp32 rounded to
+    bf16; post = 2*sigmoid(N(0,1)) in (0, 2); comb a doubly stochastic hc x hc
+    matrix per token (positive entries exp(N(0,1)), rows and columns
+    normalised alternately 20 times, in fp64, then fp32).  Draw order:
+    P_0..P_{R-1}, x, post logits, comb logits.
+    """
+    g = _gen(seed, device)
+    P = [_normal_bf16((T, H), 1.0, g, device) for _ in range(R)]
+    x = _normal_bf16((T * hc, H), 1.0, g, device).view(T, hc, H)
+    post = (2.0 * torch.sigmoid(torch.randn((T, hc), generator=g, device=device))).float()
+    m = torch.exp(torch.randn((T, hc, hc), generator=g, device=device)).double()
+    for _ in range(20):
+        m = m / m.sum(dim=2, keepdim=True)
+        m = m / m.sum(dim=1, keepdim=True)
+    comb = m.float().contiguous()
+    return dict(R=R, H=H, hc=hc, T=T, P=P, x=x.contiguous(), post=post.contiguous(), comb=comb)

@@ -57,6 +57,9 @@ def _bind(path: str):
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
         P, P, P, P, P, P, P, ctypes.c_double, ctypes.c_double, ctypes.c_int,
         P, P, P]
+    lib.oracle_ar_mhc_post.restype = ctypes.c_int
+    lib.oracle_ar_mhc_post.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                       P, P, P, P, P]
     lib.oracle_round_bf16.restype = ctypes.c_double
     lib.oracle_round_bf16.argtypes = [ctypes.c_double]
     lib.oracle_round_bf16_array.restype = None
@@ -194,3 +197,28 @@ def ar_rmsnorm_ref(partials, residual, gamma, weight_bias, eps,
     """fp64 oracle of the K = 0 case: sum of R partials + residual, RMSNorm."""
     return ar_finalize_rmsnorm_ref(None, None, None, partials, residual, gamma,
                                    weight_bias, eps, h_bf16_before_norm, want_abs)
+
+
+def ar_mhc_post_ref(partials, x, post, comb):
+    """fp64 oracle of the all-reduce + mHC residual write-back (hc_post).
+
+    partials: list of R arrays [T, H] (bf16 bits); x: [T, hc, H] (bf16 bits,
+    the incoming residual streams); post: float32 [T, hc]; comb: float32
+    [T, hc, hc].  Returns float64 out [T, hc, H] (unrounded):
+    out[t,i,j] = post[t,i] * sum_r P_r[t,j] + sum_k comb[t,i,k] * x[t,k,j].
+    PARITY UNPINNED: the pages do not define hc_post (see ar_oracle.c).
+    """
+    x = _u16(x)
+    T, hc, H = x.shape
+    partials = [_u16(p, (T, H)) for p in partials]
+    post = np.ascontiguousarray(post, dtype=np.float32)
+    comb = np.ascontiguousarray(comb, dtype=np.float32)
+    if post.shape != (T, hc) or comb.shape != (T, hc, hc):
+        raise ValueError(f"post {post.shape} / comb {comb.shape} do not match T={T}, hc={hc}")
+    out = np.empty((T, hc, H), np.float64)
+    tab = _ptr_table(partials)
+    rc = _load().oracle_ar_mhc_post(len(partials), H, hc, T, ctypes.cast(tab, ctypes.c_void_p),
+                                    _ptr(x), _ptr(post), _ptr(comb), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (rc={rc})")
+    return out

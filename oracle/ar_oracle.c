@@ -232,6 +232,55 @@ int oracle_ar_rmsnorm(int R, int H, int64_t T, const uint16_t *const *partials,
                                       eps, h_bf16, h_out, out, abs_terms);
 }
 
+/*
+ * All-reduce + mHC residual write-back ("hc_post").  sglang PR #42020 (ROCm
+ * aiter fused all-reduce + mHC hc_post for GLM-5.3-Flash), Summary and Scope:
+ * an mHC layer writes its FFN output back as two launches -- the FFN's
+ * tensor-parallel all-reduce, then hc_post, which reads the reduced output
+ * back and mixes it into the hc_mult = 4 residual streams -- and the fused
+ * kernel does both in one pass (at most 16 tokens in serving).
+ *
+ * The page gives no formula for the mix.  Reading taken here, the plainest
+ * one the page supports (a per-token linear mix of the reduced output and the
+ * incoming streams, as in hyper-connection write-backs):
+ *
+ *   y[t,j]     = sum_{r<R} P_r[t,j]                          (the all-reduce)
+ *   out[t,i,j] = post[t,i] * y[t,j] + sum_{k<hc} comb[t,i,k] * x[t,k,j]
+ *
+ * P_r bf16 [T, H]; x (incoming streams) bf16 [T, hc, H]; post fp32 [T, hc];
+ * comb fp32 [T, hc, hc] (row i mixes the streams into output stream i).
+ * PARITY UNPINNED against the pages (they do not define hc_post): the tests
+ * pin this code to the reading above only.  Every product is exact in
+ * binary64; the only roundings are the sums.
+ */
+int oracle_ar_mhc_post(int R, int H, int hc, int64_t T,
+                       const uint16_t *const *partials, const uint16_t *x,
+                       const float *post, const float *comb, double *out)
+{
+    if (R < 1 || H < 1 || hc < 1 || T < 0 || !partials || !x || !post ||
+        !comb || !out)
+        return ORACLE_BAD_ARG;
+    for (int r = 0; r < R; ++r)
+        if (!partials[r])
+            return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int j = 0; j < H; ++j) {
+            double y = 0.0;
+            for (int r = 0; r < R; ++r)
+                y += bf16_bits_to_double(partials[r][t * H + j]);
+            for (int i = 0; i < hc; ++i) {
+                double o = (double)post[t * hc + i] * y;
+                for (int k = 0; k < hc; ++k)
+                    o += (double)comb[(t * hc + i) * hc + k] *
+                         bf16_bits_to_double(x[(t * hc + k) * H + j]);
+                out[(t * hc + i) * H + j] = o;
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* Thread control for the timed CPU baseline (OpenMP over token rows). */
 int oracle_num_threads(void)
 {

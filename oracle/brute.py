@@ -63,3 +63,26 @@ def brute_ar_finalize_rmsnorm(E, perm, w, S, residual, gamma, weight_bias, eps,
         for j in range(H):
             out[t][j] = float(h[t][j] * (_fr_bf16(gamma[j]) + wb)) / root
     return h, out
+
+
+def brute_ar_mhc_post(partials, x, post, comb):
+    """Exact (Fraction) all-reduce + mHC write-back on tiny inputs.
+
+    partials: list over r of [T][H] bf16 bits; x: [T][hc][H] bits; post: [T][hc]
+    floats; comb: [T][hc][hc] floats.  Returns out[t][i][j] as Fractions:
+    post[t][i] * sum_r P_r[t][j] + sum_k comb[t][i][k] * x[t][k][j]
+    (the reading of hc_post stated in ar_oracle.c; parity unpinned).
+    """
+    T = len(x)
+    hc = len(x[0])
+    H = len(x[0][0])
+    out = [[[Fraction(0)] * H for _ in range(hc)] for _ in range(T)]
+    for t in range(T):
+        for j in range(H):
+            y = sum((_fr_bf16(p[t][j]) for p in partials), Fraction(0))
+            for i in range(hc):
+                o = Fraction(float(post[t][i])) * y
+                for k in range(hc):
+                    o += Fraction(float(comb[t][i][k])) * _fr_bf16(x[t][k][j])
+                out[t][i][j] = o
+    return out

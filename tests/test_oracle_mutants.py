@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 from tests import test_oracle as pins
+from tests import test_oracle_mhc as mhc_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ar_oracle.c")
 
@@ -35,6 +36,13 @@ MUTANTS = [
     ("shared gate dropped", "double s = g * bf16_bits_to_double(S[r][t * H + j]);",
      "double s = bf16_bits_to_double(S[r][t * H + j]);"),
     ("shared gate sign flipped", "1.0 / (1.0 + exp(-(double)gate[t]))", "1.0 / (1.0 + exp((double)gate[t]))"),
+    ("hc_post mix matrix transposed", "comb[(t * hc + i) * hc + k]", "comb[(t * hc + k) * hc + i]"),
+    ("hc_post reduced output dropped", "double o = (double)post[t * hc + i] * y;", "double o = 0.0;"),
+    ("hc_post post weight of stream 0 for all", "double o = (double)post[t * hc + i] * y;",
+     "double o = (double)post[t * hc] * y;"),
+    ("hc_post all-reduce over rank 0 only", "for (int r = 0; r < R; ++r)\n                y += bf16_bits_to_double(partials",
+     "for (int r = 0; r < 1; ++r)\n                y += bf16_bits_to_double(partials"),
+    ("hc_post streams of token 0", "bf16_bits_to_double(x[(t * hc + k) * H + j])", "bf16_bits_to_double(x[(0 * hc + k) * H + j])"),
 ]
 
 PINS = [
@@ -48,6 +56,12 @@ PINS = [
     pins.test_round_bf16_matches_fp32_to_bf16_for_fp32_values,
     lambda: [pins.test_gated_brute_force_2x4(R, K) for R, K in ((1, 1), (2, 2), (2, 0))],
     pins.test_gate_scales_only_the_shared_term,
+    lambda: [mhc_pins.test_mhc_brute_force(R, hc) for R, hc in ((1, 1), (2, 2), (2, 4), (3, 4))],
+    mhc_pins.test_mhc_identity_mix_returns_the_streams,
+    mhc_pins.test_mhc_pure_all_reduce_matches_the_main_oracle,
+    mhc_pins.test_mhc_single_stream_is_the_residual_add,
+    mhc_pins.test_mhc_stream_relabelling,
+    mhc_pins.test_mhc_hand_example,
 ]
 
 
