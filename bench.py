@@ -501,7 +501,61 @@ def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="r
                 res.append(sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T,
                                        *parse_regime(regime_name), mode=mode,
                                        gated=gated and cfg.K > 0))
+    from gen import MHC_SHAPES
+    for name, shp in MHC_SHAPES.items():
+        if only and name not in only and "mhc" not in only:
+            continue
+        for T in shp["Ts"]:
+            res.append(sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode))
     return res
+
+
+def sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode="rotate"):
+    """One T of the all-reduce + mHC write-back (ar_mhc_post), timed like the
+    main sweep: a CUDA graph of one call per disjoint input set (>= 3x L2)."""
+    from gen import make_mhc_inputs, mhc_problem_bytes
+    R, H, hc = shp["R"], shp["H"], shp["hc"]
+    b = mhc_problem_bytes(R, H, hc, T)
+    n_sets = 1 if mode == "warm" else int(min(8192, max(2, math.ceil(3 * l2 / b))))
+    inp = make_mhc_inputs(R, H, hc, T * n_sets, seed=5 + T, device=dev)
+    P, x, post, comb = inp["P"], inp["x"], inp["post"], inp["comb"]
+    out = torch.empty_like(x)
+    ws = arf.ar_workspace_create(R, 0, H, T, 1e-6, device=dev.index)
+
+    def call(i):
+        sl = slice(i * T, (i + 1) * T)
+        arf.ar_mhc_post(ws, [p[sl] for p in P], x[sl], post[sl], comb[sl], out=out[sl])
+
+    for i in range(min(n_sets, 4)):
+        call(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_sets):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize()
+    per = []
+    reps = 200 if mode == "warm" else 1
+    for _ in range(3):
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e.record(stream)
+        torch.cuda.synchronize()
+        per.append(a.elapsed_time(e) * 1e3 / (n_sets * reps))
+    us = statistics.median(per)
+    gbs = b / (us * 1e-6) / 1e9
+    err = arf.ar_workspace_device_error(ws)
+    del g, inp, out, P, x, post, comb
+    ws.destroy()
+    torch.cuda.empty_cache()
+    return {"workload": name, "R": R, "K": 0, "H": H, "hc": hc, "T": T, "us_per_call": round(us, 3),
+            "GBps": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4), "regime": "mhc_post",
+            "ctas": None, "forced": False, "calls_per_graph": n_sets, "mode": mode, "gated": False,
+            "device_error": err}
 
 
 def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0, mode="rotate",

@@ -294,6 +294,36 @@ ARFUSE_API ar_status ar_workspace_get_regime_table(const ar_workspace* ws, ar_re
                                                    int cap, int* n);
 
 /*
+ * ar_mhc_post -- the all-reduce + mHC residual write-back ("hc_post") in one
+ * launch.  sglang PR #42020 (Summary and Scope): an mHC layer writes its FFN
+ * output back as the FFN's tensor-parallel all-reduce followed by hc_post,
+ * which reads the reduced output back and mixes it into the hc_mult (four)
+ * residual streams; the fused kernel does both in one pass.  The page gives
+ * no formula for the mix; this entry point computes the per-token linear mix
+ *
+ *   y[t,j]     = sum_{r<R} partials[r][t,j]                       (fp32)
+ *   out[t,i,j] = post[t,i] * y[t,j] + sum_{k<hc} comb[t,i,k] * streams[t,k,j]
+ *
+ * rounded once to bf16.
+ *   ws            a workspace whose ranks equals R and hidden equals H (its
+ *                 top_k and eps are not used); T <= its max_tokens.
+ *   partials      host array[R] of device pointers, bf16 [T, H], 16-byte aligned.
+ *   streams       device bf16 [T, hc, H]: the incoming residual streams.
+ *   post          device fp32 [T, hc]; comb device fp32 [T, hc, hc] (row i
+ *                 mixes the incoming streams into outgoing stream i); 4-byte
+ *                 aligned.
+ *   hc            1 .. AR_MAX_HC_STREAMS.
+ *   streams_out   device bf16 [T, hc, H], 16-byte aligned; may be `streams`
+ *                 itself (in place), otherwise it must not overlap any input.
+ * T == 0 returns AR_OK without a launch.  Errors as for ar_rmsnorm; nothing
+ * is launched unless AR_OK is returned.
+ */
+#define AR_MAX_HC_STREAMS 8
+ARFUSE_API ar_status ar_mhc_post(ar_workspace* ws, const void* const* partials, int R,
+                                 const void* streams, const float* post, const float* comb,
+                                 int64_t T, int H, int hc, void* streams_out, void* stream);
+
+/*
  * ar_finalize_rmsnorm_noalloc -- the fused op for callers that cannot allocate
  * device memory.  (No counterpart on the pages: an addition of this library.)
  *

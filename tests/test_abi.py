@@ -328,3 +328,44 @@ def test_norm_bf16_h_flag_is_accepted(lib):
         assert Fake().call(lib, w) == arf.AR_VALIDATED
     finally:
         w.destroy()
+
+
+# ------------------------------------------------ all-reduce + mHC write-back
+def _mhc_call(lib, ws, **over):
+    a = iter(range(BASE, BASE + 64 * MB, MB))
+    f = dict(P=[next(a) for _ in range(R)], R=R, x=next(a), post=next(a), comb=next(a), T=4, H=H, hc=4,
+             out=next(a))
+    f.update(over)
+    P = (ctypes.c_void_p * len(f["P"]))(*f["P"]) if f["P"] is not None else None
+    return lib.ar_mhc_post(ctypes.c_void_p(ws.handle) if ws else None,
+                           ctypes.cast(P, ctypes.c_void_p) if P else None, f["R"], f["x"], f["post"],
+                           f["comb"], f["T"], f["H"], f["hc"], f["out"], None)
+
+
+def test_mhc_post_validation(lib, ws):
+    assert _mhc_call(lib, ws) == arf.AR_VALIDATED
+    x = BASE + 40 * MB
+    assert _mhc_call(lib, ws, x=x, out=x) == arf.AR_VALIDATED            # in place
+    assert _mhc_call(lib, ws, x=x, out=x + 16) == arf.AR_ERR_INVALID_ARG  # partial overlap
+    assert _mhc_call(lib, ws, T=0) == arf.AR_OK
+    assert _mhc_call(lib, ws, T=TMAX + 1) == arf.AR_ERR_CAPACITY
+    assert _mhc_call(lib, ws, R=R + 1, P=[BASE + i * MB for i in range(R + 1)]) == arf.AR_ERR_INVALID_ARG
+    assert _mhc_call(lib, ws, H=H + 8) == arf.AR_ERR_INVALID_ARG
+    for hc in (0, arf.AR_MAX_HC_STREAMS + 1):
+        assert _mhc_call(lib, ws, hc=hc) == arf.AR_ERR_INVALID_ARG
+    assert _mhc_call(lib, ws, hc=1) == arf.AR_VALIDATED
+    assert _mhc_call(lib, ws, hc=arf.AR_MAX_HC_STREAMS) == arf.AR_VALIDATED
+    for field in ("x", "out"):
+        assert _mhc_call(lib, ws, **{field: BASE + 50 * MB + 8}) == arf.AR_ERR_ALIGNMENT
+    for field in ("post", "comb"):
+        assert _mhc_call(lib, ws, **{field: BASE + 50 * MB + 2}) == arf.AR_ERR_ALIGNMENT
+    assert _mhc_call(lib, ws, P=[BASE + 8] + [BASE + (i + 1) * MB for i in range(R - 1)]) == arf.AR_ERR_ALIGNMENT
+    for field in ("x", "post", "comb", "out"):
+        assert _mhc_call(lib, ws, **{field: None}) == arf.AR_ERR_INVALID_ARG
+    assert _mhc_call(lib, ws, P=None) == arf.AR_ERR_INVALID_ARG
+    assert _mhc_call(lib, None) == arf.AR_ERR_INVALID_ARG
+    # the output overlapping a partial, post or comb
+    p0 = BASE + 30 * MB
+    assert _mhc_call(lib, ws, P=[p0] + [BASE + (i + 1) * MB for i in range(R - 1)], out=p0) == arf.AR_ERR_INVALID_ARG
+    assert _mhc_call(lib, ws, post=BASE + 41 * MB, out=BASE + 41 * MB) == arf.AR_ERR_INVALID_ARG
+    assert _mhc_call(lib, ws, comb=BASE + 42 * MB, out=BASE + 42 * MB) == arf.AR_ERR_INVALID_ARG

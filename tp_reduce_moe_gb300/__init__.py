@@ -15,4 +15,5 @@ from .binding import (  # noqa: F401
     ar_status_string, ar_workspace_create, ar_workspace_destroy, ar_workspace_device_error,
     ar_workspace_last_regime, ar_workspace_set_cluster_size, ar_workspace_set_regime,
     ar_workspace_set_producer_warps, ar_workspace_set_stage_bytes, load_library,
-    AR_MAX_REGIME_RULES, RegimeRule, ar_workspace_get_regime_table, ar_workspace_set_regime_table)
+    AR_MAX_REGIME_RULES, RegimeRule, ar_workspace_get_regime_table, ar_workspace_set_regime_table,
+    AR_MAX_HC_STREAMS, ar_mhc_post)

@@ -86,6 +86,8 @@ def load_library(path: str | None = None):
         lib.ar_workspace_set_stage_bytes.argtypes = [P, I]
         lib.ar_workspace_set_producer_warps.restype = I
         lib.ar_workspace_set_producer_warps.argtypes = [P, I]
+        lib.ar_mhc_post.restype = I
+        lib.ar_mhc_post.argtypes = [P, P, I, P, P, P, I64, I, I, P, P]
         lib.ar_workspace_set_regime_table.restype = I
         lib.ar_workspace_set_regime_table.argtypes = [P, P, I]
         lib.ar_workspace_get_regime_table.restype = I
@@ -346,3 +348,36 @@ def ar_rmsnorm(ws: Workspace, partials, residual, gamma, weight_bias: float, eps
         1 if residual_out_fp32 else 0, _stream_handle(stream, dev) if not ws.dry_run else None)
     _check(st, "ar_rmsnorm", ok=(AR_OK, AR_VALIDATED) if ws.dry_run else (AR_OK,))
     return out, residual_out
+
+
+AR_MAX_HC_STREAMS = 8
+
+
+def ar_mhc_post(ws: Workspace, partials, streams, post, comb, out=None, stream=None,
+                T: int | None = None, hc: int | None = None):
+    """All-reduce + mHC residual write-back: out[t,i] = post[t,i] * sum_r partials[r][t]
+    + sum_k comb[t,i,k] * streams[t,k].  partials: R bf16 [T, H]; streams bf16
+    [T, hc, H]; post fp32 [T, hc]; comb fp32 [T, hc, hc].  ``out`` may be
+    ``streams`` (in place).  Returns out."""
+    R, H = ws.R, ws.H
+    if len(partials) != R:
+        raise ValueError(f"partials has {len(partials)} entries, workspace has R={R}")
+    if T is None:
+        T = streams.shape[0]
+    if hc is None:
+        hc = streams.shape[1] if not isinstance(streams, int) else post.shape[1]
+    for r, p in enumerate(partials):
+        _need(p, torch.bfloat16, (T, H), f"partials[{r}]")
+    _need(streams, torch.bfloat16, (T, hc, H), "streams")
+    _need(post, torch.float32, (T, hc), "post")
+    _need(comb, torch.float32, (T, hc, hc), "comb")
+    dev = streams.device if not isinstance(streams, int) else None
+    if out is None:
+        out = torch.empty((T, hc, H), dtype=torch.bfloat16, device=dev)
+    _need(out, torch.bfloat16, (T, hc, H), "out")
+    arr = _ptr_array(partials)
+    st = load_library().ar_mhc_post(ctypes.c_void_p(ws.handle), ctypes.cast(arr, ctypes.c_void_p), int(R),
+                                    _ptr(streams), _ptr(post), _ptr(comb), int(T), int(H), int(hc),
+                                    _ptr(out), _stream_handle(stream, dev) if not ws.dry_run else None)
+    _check(st, "ar_mhc_post", ok=(AR_OK, AR_VALIDATED) if ws.dry_run else (AR_OK,))
+    return out

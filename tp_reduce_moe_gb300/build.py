@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build", "arfuse")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libarfuse.so")
 
-SOURCES = ["api.cu", "cluster_rows.cu", "stream_rows.cu", "split_rows.cu"]
+SOURCES = ["api.cu", "cluster_rows.cu", "stream_rows.cu", "split_rows.cu", "mhc_post.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

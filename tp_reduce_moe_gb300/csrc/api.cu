@@ -467,6 +467,53 @@ ar_status ar_rmsnorm(ar_workspace* ws, const void* const* partials, int R, const
                0, H, out, residual_out, residual_out_is_fp32, stream, false);
 }
 
+ar_status ar_mhc_post(ar_workspace* ws, const void* const* partials, int R, const void* streams,
+                      const float* post, const float* comb, int64_t T, int H, int hc,
+                      void* streams_out, void* stream) {
+    if (!ws || !partials) return AR_ERR_INVALID_ARG;
+    if (R < 1 || R > AR_MAX_RANKS || R != ws->R || H != ws->H) return AR_ERR_INVALID_ARG;
+    if (hc < 1 || hc > AR_MAX_HC_STREAMS) return AR_ERR_INVALID_ARG;
+    if (T < 0) return AR_ERR_INVALID_ARG;
+    if (T > ws->max_tokens) return AR_ERR_CAPACITY;
+    if (T == 0) return AR_OK;
+    if (!streams || !post || !comb || !streams_out) return AR_ERR_INVALID_ARG;
+    for (int r = 0; r < R; ++r)
+        if (!partials[r]) return AR_ERR_INVALID_ARG;
+    if (!aligned(streams, 16) || !aligned(streams_out, 16) || !aligned(post, 4) || !aligned(comb, 4))
+        return AR_ERR_ALIGNMENT;
+    for (int r = 0; r < R; ++r)
+        if (!aligned(partials[r], 16)) return AR_ERR_ALIGNMENT;
+    // The output may be the incoming streams exactly; otherwise it overlaps no input.
+    const Range r_out = range_of(streams_out, T * hc * H * 2);
+    const Range r_x = range_of(streams, T * hc * H * 2);
+    if (streams_out != streams && overlap(r_out, r_x)) return AR_ERR_INVALID_ARG;
+    if (overlap(r_out, range_of(post, T * hc * 4)) || overlap(r_out, range_of(comb, T * hc * hc * 4)))
+        return AR_ERR_INVALID_ARG;
+    for (int r = 0; r < R; ++r)
+        if (overlap(r_out, range_of(partials[r], T * H * 2))) return AR_ERR_INVALID_ARG;
+    if (ws->flags & AR_WS_DRY_RUN) return AR_VALIDATED;
+
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return AR_ERR_CUDA;
+    if (cur != ws->device) return AR_ERR_INVALID_ARG;
+    arf::MhcArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int r = 0; r < R; ++r) a.P[r] = static_cast<const uint16_t*>(partials[r]);
+    a.x = static_cast<const uint16_t*>(streams);
+    a.post = post;
+    a.comb = comb;
+    a.out = static_cast<uint16_t*>(streams_out);
+    a.T = T;
+    a.R = R;
+    a.H = H;
+    a.hc = hc;
+    if (arf::launch_mhc_post(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    return AR_OK;
+}
+
 ar_status ar_workspace_device_error(ar_workspace* ws, int* code) {
     if (!ws || !code) return AR_ERR_INVALID_ARG;
     *code = 0;

@@ -314,6 +314,18 @@ cudaError_t cluster_rows_set_attributes();
 constexpr int kSlotHeader = 128;
 
 // Geometry of one stream_rows launch (kernel parameter).
+// Arguments of the all-reduce + mHC write-back (mhc_post.cu).
+struct MhcArgs {
+    const uint16_t* P[16];  // R partials, bf16 [T, H]
+    const uint16_t* x;      // incoming streams, bf16 [T, hc, H]
+    const float* post;      // [T, hc]
+    const float* comb;      // [T, hc, hc]
+    uint16_t* out;          // outgoing streams, bf16 [T, hc, H] (may be x)
+    int64_t T;
+    int R, H, hc;
+};
+cudaError_t launch_mhc_post(const MhcArgs& a, cudaStream_t stream);
+
 struct StreamGeom {
     int nstages;      // ring slots
     int slot_bytes;   // bytes per slot: kSlotHeader + seg_per_stage * seg_stride
