@@ -105,9 +105,13 @@ typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
 
 /*
  * Create the workspace for one model: fixes ranks (R), top_k (K), hidden (H)
- * and eps, as the model's MoE layers share them.  Allocates a small device
- * block (the error word) on `device` and sets kernel attributes; call it once,
- * outside any stream capture.
+ * and eps, as the model's MoE layers share them.  Allocates its device memory
+ * on `device` -- the error word, and a scratch of one fp32 row of H plus one
+ * counter per SM for rows split over several CTAs (4.4 MB at H = 7168 on 152
+ * SMs) -- and sets kernel attributes; call it once, outside any stream
+ * capture.  A workspace serves one stream of calls at a time: calls that use
+ * the same workspace must be ordered on the GPU (one stream, or event
+ * ordering); concurrent callers need a workspace each.
  *   device      CUDA device ordinal (ignored with AR_WS_DRY_RUN)
  *   ranks       1 .. AR_MAX_RANKS
  *   top_k       0 .. AR_MAX_TOP_K (0: only ar_rmsnorm is meaningful)
@@ -246,6 +250,21 @@ ARFUSE_API ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes);
  * identical for every value.
  */
 ARFUSE_API ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps);
+
+/*
+ * Cap the split of whole-row streaming (AR_REGIME_STREAM) over its last,
+ * partial wave: with T mod SMs = n > 0 rows left for the last wave, each of
+ * those rows is split into up to m = min(max_parts, SMs / n) segment
+ * intervals on m CTAs, whose fp32 partial rows meet in the workspace scratch;
+ * the CTA that brings the last part sums the parts in part order and finishes
+ * the row (no CTA waits for another).  max_parts 0 or 1 never splits; 2 ..
+ * AR_MAX_SPLIT_PARTS caps m (default AR_MAX_SPLIT_PARTS).  Other values are
+ * AR_ERR_INVALID_ARG.  A split row's fp32 sum runs in another order than an
+ * unsplit one, so results move within rounding (deterministic for a given
+ * setting, T and GPU).
+ */
+#define AR_MAX_SPLIT_PARTS 8
+ARFUSE_API ar_status ar_workspace_set_split_rows(ar_workspace* ws, int max_parts);
 
 /* Regime (AR_REGIME_CLUSTER / _STREAM / _ONESHOT / _SPLIT) of the last
  * launched call (on a dry-run workspace: of the last validated call), 0

@@ -21,7 +21,8 @@ int main() {
     for (int sb : {0, 1024, 4096, 16384, 65536, 131072})
     for (int Cf = 0; Cf <= 16; Cf = Cf ? Cf * 2 : 1) {
       StreamPlan p;
-      if (!plan_stream_rows(R, K, H, sh, T, 152, 232448, 16, Cf, sb, &p)) {
+      const int split = (sb == 0 || sb == 65536) ? 8 : 0;  // split rows of the last wave
+      if (!plan_stream_rows(R, K, H, sh, T, 152, 232448, 16, Cf, sb, &p, 0, split)) {
         if (Cf == 0 || Cf == 1) { ++fails; printf("auto/stream plan failed H=%d R=%d K=%d T=%ld Cf=%d\n", H, R, K, T, Cf); }
         continue;
       }
@@ -35,6 +36,19 @@ int main() {
       if (p.grid % C) bad = true;
       if (p.threads > 640 || p.threads % 32) bad = true;
       if (g.nstages < 2) bad = true;
+      // split rows: whole rows fill complete waves, each split row's parts
+      // have a CTA each and at least one segment each
+      if (g.tail_parts < 1 || g.tail_parts > 8 || g.main_rows < 0 || g.main_rows > T) bad = true;
+      if (g.tail_parts > 1) {
+        if (C != 1 || !split) bad = true;
+        if (g.main_rows % p.grid) bad = true;
+        if ((T - g.main_rows) * g.tail_parts > p.grid) bad = true;
+        if (g.tail_parts > nseg) bad = true;
+        if (T < 152 && (g.main_rows != 0 || p.grid != T * g.tail_parts)) bad = true;
+        if (p.grid > 152) bad = true;
+        for (int q = 0; q < g.tail_parts; ++q)
+          if ((long)(q + 1) * nseg / g.tail_parts - (long)q * nseg / g.tail_parts < 1) bad = true;
+      } else if (g.main_rows != T) bad = true;
       // every producer warp owns at least one slot
       if (g.producers < 1 || g.producers > 4 || g.producers > g.nstages) bad = true;
       if (g.seg_per_stage < 1 || g.seg_per_stage > 32 || g.seg_per_stage > nseg) bad = true;

@@ -369,3 +369,12 @@ def test_mhc_post_validation(lib, ws):
     assert _mhc_call(lib, ws, P=[p0] + [BASE + (i + 1) * MB for i in range(R - 1)], out=p0) == arf.AR_ERR_INVALID_ARG
     assert _mhc_call(lib, ws, post=BASE + 41 * MB, out=BASE + 41 * MB) == arf.AR_ERR_INVALID_ARG
     assert _mhc_call(lib, ws, comb=BASE + 42 * MB, out=BASE + 42 * MB) == arf.AR_ERR_INVALID_ARG
+
+
+def test_split_rows_setter(lib, ws):
+    for n in (0, 1, 2, arf.AR_MAX_SPLIT_PARTS):
+        arf.ar_workspace_set_split_rows(ws, n)
+        assert Fake().call(lib, ws) == arf.AR_VALIDATED
+    for n in (-1, arf.AR_MAX_SPLIT_PARTS + 1):
+        with pytest.raises(arf.ArfuseError):
+            arf.ar_workspace_set_split_rows(ws, n)

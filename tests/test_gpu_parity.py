@@ -553,3 +553,36 @@ def test_tuning_controls_leave_results_unchanged(cfg, T):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+@pytest.mark.parametrize("cfg,T", [("tiny", 153), ("tiny", 170), ("tiny", 7), ("dsv3_decode", 16),
+                                   ("dsv3_decode", 64), ("glm_gemma", 16), ("ar_only", 40)])
+def test_split_rows_of_the_last_wave(cfg, T):
+    """Whole-row streaming with the last wave's rows split over several CTAs
+    (partial rows meet in the workspace scratch, the last arriving CTA
+    finishes the row): parity at every split cap, both residual_out types, and
+    back-to-back calls (the arrival counters must come back to zero)."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        grids = set()
+        for parts in (0, 2, 3, arf.AR_MAX_SPLIT_PARTS):
+            arf.ar_workspace_set_split_rows(ws, parts)
+            for fp32 in (False, True):
+                for rep in range(3):
+                    out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_STREAM)
+                    torch.cuda.synchronize()
+                    tag = f"split rows {cfg} T={T} parts<={parts} fp32={fp32} call {rep}"
+                    check_bf16(out, ref["out"], tag + " out")
+                    if fp32:
+                        check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+                    else:
+                        check_bf16(r_out, ref["h"], tag + " residual_out")
+            grids.add(arf.ar_workspace_last_regime(ws)[1])
+        if T < torch.cuda.get_device_properties(0).multi_processor_count:
+            assert len(grids) >= 2, grids   # the cap changed the launch (more CTAs per row)
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()

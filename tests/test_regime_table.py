@@ -65,7 +65,7 @@ def test_table_rules_are_followed(dsv3):
     assert dsv3.plan(3) == (arf.AR_REGIME_CLUSTER, 4)
     assert dsv3.plan(40) == (arf.AR_REGIME_CLUSTER, 4)
     regime, grid = dsv3.plan(41)
-    assert regime == arf.AR_REGIME_STREAM and grid == 41  # one CTA per row below the SM count
+    assert regime == arf.AR_REGIME_STREAM and grid == 41 * 3  # each row split over 152 // 41 CTAs
 
 
 def test_past_the_last_rule_and_auto_rules_use_the_heuristic(dsv3):
@@ -147,3 +147,17 @@ def test_k0_table_selects_oneshot_then_stream():
         assert s.plan(200)[0] == arf.AR_REGIME_STREAM
     finally:
         s.ws.destroy()
+
+
+def test_whole_row_streaming_splits_the_last_wave(dsv3):
+    """The last partial wave's rows go to several CTAs each: the grid grows to
+    cover the idle SMs (T < SMs: T * parts CTAs; T >= SMs: the SM count)."""
+    arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_STREAM)
+    assert dsv3.plan(16) == (arf.AR_REGIME_STREAM, 16 * 8)    # 8 parts per row
+    assert dsv3.plan(64) == (arf.AR_REGIME_STREAM, 128)       # 2 parts per row
+    assert dsv3.plan(100) == (arf.AR_REGIME_STREAM, 100)      # 152 // 100 = 1: whole rows
+    assert dsv3.plan(300) == (arf.AR_REGIME_STREAM, 152)
+    arf.ar_workspace_set_split_rows(dsv3.ws, 0)
+    assert dsv3.plan(16) == (arf.AR_REGIME_STREAM, 16)
+    arf.ar_workspace_set_split_rows(dsv3.ws, 3)
+    assert dsv3.plan(16) == (arf.AR_REGIME_STREAM, 48)

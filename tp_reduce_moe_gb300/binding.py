@@ -84,6 +84,8 @@ def load_library(path: str | None = None):
         lib.ar_workspace_set_regime.argtypes = [P, I]
         lib.ar_workspace_set_stage_bytes.restype = I
         lib.ar_workspace_set_stage_bytes.argtypes = [P, I]
+        lib.ar_workspace_set_split_rows.restype = I
+        lib.ar_workspace_set_split_rows.argtypes = [P, I]
         lib.ar_workspace_set_producer_warps.restype = I
         lib.ar_workspace_set_producer_warps.argtypes = [P, I]
         lib.ar_mhc_post.restype = I
@@ -199,6 +201,16 @@ def ar_workspace_get_regime_table(ws: Workspace):
            "ar_workspace_get_regime_table")
     return [(int(arr[i].max_tokens), int(arr[i].regime), int(arr[i].ctas_per_row))
             for i in range(min(n.value, AR_MAX_REGIME_RULES))]
+
+
+AR_MAX_SPLIT_PARTS = 8
+
+
+def ar_workspace_set_split_rows(ws: Workspace, max_parts: int) -> None:
+    """Cap how many CTAs share each row of whole-row streaming's last, partial
+    wave (0 or 1: never split; default AR_MAX_SPLIT_PARTS)."""
+    _check(load_library().ar_workspace_set_split_rows(ctypes.c_void_p(ws.handle), int(max_parts)),
+           "ar_workspace_set_split_rows")
 
 
 def ar_workspace_set_producer_warps(ws: Workspace, warps: int) -> None:

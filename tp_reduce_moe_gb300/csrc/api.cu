@@ -24,6 +24,9 @@ struct ar_workspace {
     float eps;
     unsigned flags;
     unsigned* d_err;  // device error word (AR_DEVERR_* bits)
+    unsigned* d_part;  // split-row counters [num_sms] (zero between calls), then fp32 scratch [num_sms, H]
+    bool split_ok;     // plans may split rows (the scratch exists, or a dry run plans as if it did)
+    int max_tail_parts;  // cap on the segment intervals of a split row (0 / 1: never split)
     int num_sms;
     int smem_optin;
     int max_cluster;  // largest co-schedulable cluster for the cluster kernel
@@ -46,6 +49,13 @@ constexpr int kDryRunSms = 152;          // GB300
 constexpr int kDryRunSmemOptin = 232448;  // 227 KB
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Split-row workspace: num_sms counters (rounded up to 256 bytes), then
+// num_sms fp32 rows of H.
+size_t part_counter_words(int num_sms) { return ((size_t)num_sms * 4 + 255) / 256 * 64; }
+size_t part_bytes(int num_sms, int H) {
+    return part_counter_words(num_sms) * 4 + (size_t)num_sms * H * 4;
+}
 
 struct Range {
     uintptr_t lo, hi;  // [lo, hi)
@@ -150,7 +160,7 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
             }
             if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
                                        ws->max_cluster_stream, C, ws->stage_bytes, &p->s,
-                                       ws->producer_warps))
+                                       ws->producer_warps, ws->split_ok ? ws->max_tail_parts : 0))
                 return 0;
             return p->s.geo.C > 1 ? AR_REGIME_CLUSTER : AR_REGIME_STREAM;
         }
@@ -174,7 +184,8 @@ int plan_heuristic(const ar_workspace* ws, int R, int K, int H, bool shared, int
                                              ws->max_cluster_split, 0, &p->x))
         return AR_REGIME_SPLIT;
     if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                               ws->max_cluster_stream, 0, ws->stage_bytes, &p->s, ws->producer_warps))
+                               ws->max_cluster_stream, 0, ws->stage_bytes, &p->s, ws->producer_warps,
+                               ws->split_ok ? ws->max_tail_parts : 0))
         return 0;
     return p->s.geo.C > 1 ? AR_REGIME_CLUSTER : AR_REGIME_STREAM;
 }
@@ -289,6 +300,10 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     a.out = out;
     a.residual_out = residual_out;
     a.err = ws->d_err;
+    if (ws->d_part) {
+        a.part_count = ws->d_part;
+        a.part_scratch = reinterpret_cast<float*>(ws->d_part + part_counter_words(ws->num_sms));
+    }
     a.T = T;
     a.rows_e = K > 0 ? rows_e : 0;
     a.R = R;
@@ -342,6 +357,9 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
     ws->eps = eps;
     ws->flags = flags;
     ws->d_err = nullptr;
+    ws->d_part = nullptr;
+    ws->split_ok = (flags & AR_WS_DRY_RUN) != 0;
+    ws->max_tail_parts = arf::kMaxTailParts;
     ws->regime_force = AR_REGIME_AUTO;
     ws->force_ctas_per_row = 0;
     ws->stage_bytes = 0;
@@ -403,8 +421,20 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
             if (arf::plan_split_rows(ranks, top_k, hidden, true, 1, ws->num_sms, ws->smem_optin, 16, c, &xp))
                 ws->max_cluster_split = arf::split_rows_max_cluster(xp.threads, xp.smem, xp.cpt);
     }
-    if (cudaMalloc(&ws->d_err, 256) != cudaSuccess || cudaMemset(ws->d_err, 0, 256) != cudaSuccess ||
-        cudaDeviceSynchronize() != cudaSuccess) {
+    if (cudaMalloc(&ws->d_err, 256) != cudaSuccess || cudaMemset(ws->d_err, 0, 256) != cudaSuccess) {
+        st = AR_ERR_CUDA;
+        goto fail;
+    }
+    {
+        // Split rows: one counter and one fp32 partial row per CTA of a whole-row grid.
+        const size_t bytes = part_bytes(ws->num_sms, hidden);
+        if (cudaMalloc(&ws->d_part, bytes) != cudaSuccess || cudaMemset(ws->d_part, 0, bytes) != cudaSuccess) {
+            st = AR_ERR_CUDA;
+            goto fail;
+        }
+        ws->split_ok = true;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) {
         st = AR_ERR_CUDA;
         goto fail;
     }
@@ -415,6 +445,7 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
 fail:
     (void)cudaGetLastError();
     if (ws->d_err) (void)cudaFree(ws->d_err);
+    if (ws->d_part) (void)cudaFree(ws->d_part);
     if (prev >= 0) (void)cudaSetDevice(prev);
     delete ws;
     return st;
@@ -426,7 +457,8 @@ ar_status ar_workspace_destroy(ar_workspace* ws) {
     if (ws->d_err) {
         int prev = -1;
         (void)cudaGetDevice(&prev);
-        if (cudaSetDevice(ws->device) != cudaSuccess || cudaFree(ws->d_err) != cudaSuccess)
+        if (cudaSetDevice(ws->device) != cudaSuccess || cudaFree(ws->d_err) != cudaSuccess ||
+            (ws->d_part && cudaFree(ws->d_part) != cudaSuccess))
             st = AR_ERR_CUDA;
         if (prev >= 0) (void)cudaSetDevice(prev);
     }
@@ -524,7 +556,11 @@ ar_status ar_workspace_device_error(ar_workspace* ws, int* code) {
     ar_status st = AR_OK;
     if (cudaSetDevice(ws->device) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
         cudaMemcpy(&v, ws->d_err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemset(ws->d_err, 0, sizeof v) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaMemset(ws->d_err, 0, sizeof v) != cudaSuccess ||
+        // a call cut short may have left split-row counters part-way: restart them
+        (v && ws->d_part &&
+         cudaMemset(ws->d_part, 0, part_counter_words(ws->num_sms) * sizeof(unsigned)) != cudaSuccess) ||
+        cudaDeviceSynchronize() != cudaSuccess) {
         (void)cudaGetLastError();
         st = AR_ERR_CUDA;
     }
@@ -569,6 +605,13 @@ ar_status ar_workspace_get_regime_table(const ar_workspace* ws, ar_regime_rule* 
     if (!ws || !n || cap < 0 || (cap > 0 && !rules)) return AR_ERR_INVALID_ARG;
     for (int i = 0; i < ws->table_n && i < cap; ++i) rules[i] = ws->table[i];
     *n = ws->table_n;
+    return AR_OK;
+}
+
+ar_status ar_workspace_set_split_rows(ar_workspace* ws, int max_parts) {
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (max_parts < 0 || max_parts > arf::kMaxTailParts) return AR_ERR_INVALID_ARG;
+    ws->max_tail_parts = max_parts;
     return AR_OK;
 }
 

@@ -37,6 +37,8 @@ struct RowArgs {
     void* out;                     // bf16 [T, H]
     void* residual_out;            // bf16 or fp32 [T, H]
     unsigned* err;                 // device error word
+    float* part_scratch;           // [grid, H] fp32 partial rows of split rows (streaming, C = 1)
+    unsigned* part_count;          // [grid] arrival counters of split rows (zero between calls)
     int64_t T;
     int64_t rows_e;
     int R, K, H;
@@ -334,6 +336,8 @@ struct StreamGeom {
     int C;            // CTAs per token row (cluster size); 1 = whole rows per CTA
     int tile_chunks;  // 16-byte column chunks per CTA tile (the row's last tile may be shorter)
     int producers;    // producer warps (slot q is filled by warp q % producers)
+    int64_t main_rows;  // rows [0, main_rows) whole, round-robin; the rest split (C = 1 only)
+    int tail_parts;     // segment intervals per split row (1: no split rows)
 };
 
 struct StreamPlan {
@@ -347,9 +351,15 @@ struct StreamPlan {
 // Plan a stream_rows launch for T rows.  C = 0 picks the CTAs per row from T
 // and the SM count; C >= 1 forces it.  stage_bytes = 0 picks the slot size,
 // otherwise it is the target.  producers = 0 picks the producer warps (up to
-// four), otherwise it is the cap.  Returns false if no plan fits.
+// four), otherwise it is the cap.  max_tail_parts >= 2 lets whole-row plans
+// (C = 1) split the rows of a last, partial wave over up to that many CTAs
+// each (their partial rows meet in a workspace scratch of num_sms rows of H
+// fp32 and num_sms counters); 0 or 1 never splits.  Returns false if no plan
+// fits.
+constexpr int kMaxTailParts = 8;
 bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
-                      int max_cluster, int C, int stage_bytes, StreamPlan* p, int producers = 0);
+                      int max_cluster, int C, int stage_bytes, StreamPlan* p, int producers = 0,
+                      int max_tail_parts = 0);
 cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, bool res_f32,
                                cudaStream_t stream);
 cudaError_t stream_rows_set_attributes(int smem_optin);

@@ -81,6 +81,24 @@ __device__ __forceinline__ void stage_range(int j, int P, int nsr, int nseg, int
     }
 }
 
+// Stages of the segment interval [a, b) of a split row: its perm-free
+// segments (s < nsr) in stages of at most P, then its routed ones.
+__device__ __forceinline__ int part_stage_count(int P, int nsr, int a, int b) {
+    const int lo = min(b, nsr) - a, hi = b - max(a, nsr);
+    return (lo > 0 ? (lo + P - 1) / P : 0) + (hi > 0 ? (hi + P - 1) / P : 0);
+}
+__device__ __forceinline__ void part_stage_range(int j, int P, int nsr, int a, int b, int& s0, int& cnt) {
+    const int lo = min(b, nsr) - a;
+    const int first = lo > 0 ? (lo + P - 1) / P : 0;
+    if (j < first) {
+        s0 = a + j * P;
+        cnt = min(P, min(b, nsr) - s0);
+    } else {
+        s0 = max(a, nsr) + (j - first) * P;
+        cnt = min(P, b - s0);
+    }
+}
+
 template <int CPT, int U, bool RES_F32, bool CLUSTERED>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     stream_rows_kernel(const __grid_constant__ RowArgs a, const StreamGeom geo) {
@@ -92,6 +110,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     float* xslot = reinterpret_cast<float*>(xbar + 2);            // [2][kMaxCluster]
     float* red = xslot + 2 * kMaxCluster;                         // [2][32]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 64);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(red + 65);
     uint8_t* rec = reinterpret_cast<uint8_t*>(red + 68);          // [nst]
     uint8_t* ring = smem + stream_ring_offset(nst);
 
@@ -111,6 +130,13 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     const int nseg = nS + 1 + a.R * a.K;
     const int P = geo.seg_per_stage;
     const int nstage_row = (nS + 1 + P - 1) / P + (a.R * a.K + P - 1) / P;
+    // Whole rows [0, main_rows) go round-robin; with split rows (C = 1 only)
+    // each row of the last, partial wave is cut into `parts` segment
+    // intervals, one per CTA (CTA b takes part b % parts of row
+    // main_rows + b / parts), handled after the CTA's whole rows.
+    const int64_t main_rows = CLUSTERED ? a.T : geo.main_rows;
+    const int parts = CLUSTERED ? 1 : geo.tail_parts;
+    const bool has_part = !CLUSTERED && parts > 1 && (int64_t)blockIdx.x < (a.T - main_rows) * parts;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -121,6 +147,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         mbar_init(smem_addr(&xbar[0]), (uint32_t)C);
         mbar_init(smem_addr(&xbar[1]), (uint32_t)C);
         *abort_flag = 0;
+        *last_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -147,17 +174,17 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         int32_t raw_next = 0;
         float w_next = 0.0f;
         float gate_next = 0.0f;
-        if (lane < a.K && first_row < a.T) {
+        if (lane < a.K && first_row < main_rows) {
             raw_next = __ldg(a.perm + first_row * a.K + lane);
             w_next = __ldg(a.w + first_row * a.K + lane);
         }
-        if (a.shared_gate && first_row < a.T) gate_next = __ldg(a.shared_gate + first_row);
+        if (a.shared_gate && first_row < main_rows) gate_next = __ldg(a.shared_gate + first_row);
         int64_t g0 = 0;  // stage number of the row's first stage
-        for (int64_t t = first_row; t < a.T && ok; t += row_step, g0 += nstage_row) {
+        for (int64_t t = first_row; t < main_rows && ok; t += row_step, g0 += nstage_row) {
             const int32_t raw = raw_next;
             const float my_w = w_next;
             const float s_coef = a.shared_gate ? 1.0f / (1.0f + expf(-gate_next)) : 1.0f;
-            if (a.shared_gate && t + row_step < a.T) gate_next = __ldg(a.shared_gate + t + row_step);
+            if (a.shared_gate && t + row_step < main_rows) gate_next = __ldg(a.shared_gate + t + row_step);
             int64_t my_row = -1;  // checked lazily, at this warp's first routed stage
             for (int j = 0; j < nstage_row && ok; ++j) {
                 const int64_t g = g0 + j;
@@ -173,7 +200,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
                 if (s0 > nS) {  // routed stage
                     if (my_row < 0) {
                         my_row = lane < a.K ? checked_row(raw, a.rows_e, a.err) : 0;
-                        if (lane < a.K && t + row_step < a.T) {
+                        if (lane < a.K && t + row_step < main_rows) {
                             raw_next = __ldg(a.perm + (t + row_step) * a.K + lane);
                             w_next = __ldg(a.w + (t + row_step) * a.K + lane);
                         }
@@ -217,9 +244,74 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
                     }
                 }
             }
-            if (my_row < 0 && lane < a.K && t + row_step < a.T) {  // no routed stage of this row here
+            if (my_row < 0 && lane < a.K && t + row_step < main_rows) {  // no routed stage of this row here
                 raw_next = __ldg(a.perm + (t + row_step) * a.K + lane);
                 w_next = __ldg(a.w + (t + row_step) * a.K + lane);
+            }
+        }
+        if (has_part && ok) {
+            // This CTA's part of a split row: segments [pa, pb) of row t,
+            // through the same ring, after the whole rows.
+            const int64_t t = main_rows + blockIdx.x / parts;
+            const int pa = (int)((int64_t)(blockIdx.x % parts) * nseg / parts);
+            const int pb = (int)((int64_t)(blockIdx.x % parts + 1) * nseg / parts);
+            const int nsr = nS + 1;
+            int64_t my_row = 0;
+            float my_w = 0.0f;
+            if (lane < a.K) {
+                my_w = __ldg(a.w + t * a.K + lane);
+                if (pb > nsr) my_row = checked_row(__ldg(a.perm + t * a.K + lane), a.rows_e, a.err);
+            }
+            const float s_coef = shared_coef(a, t);
+            const int nstage = part_stage_count(P, nsr, pa, pb);
+            for (int j = 0; j < nstage && ok; ++j) {
+                const int64_t g = g0 + j;
+                const int slot = (int)(g % nst);
+                if (slot % W != warp) continue;
+                const uint32_t phase = (uint32_t)((g / nst) & 1);
+                int s0, cnt;
+                part_stage_range(j, P, nsr, pa, pb, s0, cnt);
+                const int s = s0 + lane;
+                const int e = s - nsr;
+                int64_t row_k = 0;
+                float w_k = 1.0f;
+                if (s0 >= nsr) {
+                    const int k = (lane < cnt) ? e / a.R : 0;
+                    row_k = __shfl_sync(0xffffffffu, my_row, k);
+                    w_k = __shfl_sync(0xffffffffu, my_w, k);
+                }
+                int go = 0;
+                if (lane == 0) {
+                    if (*abort_flag) {
+                        go = 0;
+                    } else if (mbar_wait_bounded(smem_addr(&empty[slot]), phase ^ 1u, abort_flag)) {
+                        go = 1;
+                    } else {
+                        if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+                        *abort_flag = 1;
+                    }
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                } else {
+                    uint8_t* sbase = ring + (size_t)slot * geo.slot_bytes;
+                    if (lane < cnt)
+                        reinterpret_cast<float*>(sbase)[lane] = e >= 0 ? w_k : (s < nS ? s_coef : 1.0f);
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(smem_addr(&full[slot]), (uint32_t)cnt * tile_bytes);
+                        rec[slot] = (uint8_t)(1u + phase);
+                    }
+                    if (lane < cnt) {
+                        const uint16_t* src;
+                        if (s < nS) src = a.S[s] + t * H + col;
+                        else if (s == nS) src = a.residual + t * H + col;
+                        else src = a.E[e % a.R] + row_k * H + col;
+                        bulk_g2s(smem_addr(sbase + kSlotHeader + (size_t)lane * geo.seg_stride), src,
+                                 tile_bytes, smem_addr(&full[slot]), pol);
+                    }
+                }
             }
         }
         // After an abort, wait (briefly, bounded) for every copy still landing
@@ -261,7 +353,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     int par_row = 0;
     uint32_t xph = 0u;  // bit p: phase of xbar[p] to wait for next
     bool ok = true;
-    for (int64_t t = first_row; t < a.T; t += row_step) {
+    for (int64_t t = first_row; t < main_rows; t += row_step) {
         float acc[CPT][8];
 #pragma unroll
         for (int m = 0; m < CPT; ++m)
@@ -347,7 +439,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
             for (int rk = 0; rk < C; ++rk) tot += xs[rk];
             // After the last row's push, arrive on the exit barrier now and
             // wait at the end: no CTA leaves while a peer may still push into it.
-            if (t + row_step >= a.T) cluster_arrive_release();
+            if (t + row_step >= main_rows) cluster_arrive_release();
         }
         const float inv = rsqrtf(tot / (float)H + a.eps);
 #pragma unroll
@@ -366,6 +458,134 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         if (first_row >= a.T) cluster_arrive_release();  // a cluster without rows
         cluster_wait_acquire();
     }
+    if (!CLUSTERED && has_part) {
+        // This CTA's part of a split row: accumulate its segments, publish the
+        // fp32 partial row, count the parts in; the CTA that brings the last
+        // part sums all of them in part order (a fixed order, whichever CTA
+        // finishes last) and finishes the row.  No CTA waits for another.
+        const int64_t t = main_rows + blockIdx.x / parts;
+        const int pa = (int)((int64_t)(blockIdx.x % parts) * nseg / parts);
+        const int pb = (int)((int64_t)(blockIdx.x % parts + 1) * nseg / parts);
+        const int nsr = nS + 1;
+        float acc[CPT][8];
+#pragma unroll
+        for (int m = 0; m < CPT; ++m)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[m][j] = 0.0f;
+        const int nstage = part_stage_count(P, nsr, pa, pb);
+        for (int j = 0; j < nstage; ++j) {
+            int s0, cnt;
+            part_stage_range(j, P, nsr, pa, pb, s0, cnt);
+            if (ok && !mbar_wait_bounded(smem_addr(&full[slot]), phase, abort_flag)) {
+                ok = false;
+                if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            const uint8_t* base = ring + (size_t)slot * geo.slot_bytes;
+            const float* coef = reinterpret_cast<const float*>(base);
+            const uint8_t* seg = base + kSlotHeader;
+            for (int i0 = 0; i0 < cnt; i0 += U) {
+                float cf[U];
+                uint4 v[U][CPT];
+#pragma unroll
+                for (int u = 0; u < U; ++u) cf[u] = i0 + u < cnt ? coef[i0 + u] : 0.0f;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int m = 0; m < CPT; ++m)
+                        if (i0 + u < cnt && valid[m])
+                            v[u][m] = reinterpret_cast<const uint4*>(seg + (size_t)(i0 + u) * geo.seg_stride)[lch[m]];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int m = 0; m < CPT; ++m)
+                        if (i0 + u < cnt && valid[m]) {
+                            float f[8];
+                            bf16x8_to_f32(v[u][m], f);
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj) acc[m][jj] = fmaf(cf[u], f[jj], acc[m][jj]);
+                        }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty[slot]));
+            if (++slot == nst) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        }
+        float* mine = a.part_scratch + (int64_t)blockIdx.x * H;
+#pragma unroll
+        for (int m = 0; m < CPT; ++m)
+            if (valid[m]) {
+                float4* q = reinterpret_cast<float4*>(mine + (int64_t)lch[m] * 8);
+                __stcg(q, make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]));
+                __stcg(q + 1, make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]));
+            }
+        __threadfence();
+        named_barrier_sync(1, nct);
+        if (ci == 0) {
+            unsigned* count = a.part_count + blockIdx.x / parts;
+            const unsigned prev = atomicAdd(count, 1u);
+            const int last = prev == (unsigned)(parts - 1);
+            if (last) *count = 0u;  // every part has arrived: ready for the next call
+            __threadfence();
+            *last_flag = last;
+        }
+        named_barrier_sync(1, nct);
+        if (!*last_flag) return;
+        const int64_t first_part = (int64_t)(blockIdx.x / parts) * parts;
+        const int my_part = (int)(blockIdx.x % parts);
+#pragma unroll
+        for (int m = 0; m < CPT; ++m) {
+            if (!valid[m]) continue;
+            float sum[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sum[j] = 0.0f;
+            for (int p = 0; p < parts; ++p) {
+                if (p == my_part) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sum[j] += acc[m][j];
+                } else {
+                    const float4* q = reinterpret_cast<const float4*>(
+                        a.part_scratch + (first_part + p) * H + (int64_t)lch[m] * 8);
+                    const float4 x0 = __ldcg(q), x1 = __ldcg(q + 1);
+                    sum[0] += x0.x; sum[1] += x0.y; sum[2] += x0.z; sum[3] += x0.w;
+                    sum[4] += x1.x; sum[5] += x1.y; sum[6] += x1.z; sum[7] += x1.w;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[m][j] = sum[j];
+        }
+        // the row's epilogue, as for whole rows
+        float ss = 0.0f;
+#pragma unroll
+        for (int m = 0; m < CPT; ++m) {
+            if (valid[m]) {
+                store_residual8<RES_F32>(a.residual_out, t * H + (int64_t)(chunk0 + lch[m]) * 8, acc[m]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    acc[m][j] = norm_input(acc[m][j], a.norm_bf16_h);
+                    ss = fmaf(acc[m][j], acc[m][j], ss);
+                }
+            }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) red[par_row * 32 + (warp - W)] = ss;
+        named_barrier_sync(1, nct);
+        float tot = 0.0f;
+        for (int w = 0; w < ncw; ++w) tot += red[par_row * 32 + w];
+        const float inv = rsqrtf(tot / (float)H + a.eps);
+#pragma unroll
+        for (int m = 0; m < CPT; ++m) {
+            if (valid[m]) {
+                float o[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = acc[m][j] * inv * gw[m][j];
+                st_global16(reinterpret_cast<uint16_t*>(a.out) + t * H + (int64_t)(chunk0 + lch[m]) * 8,
+                            f32x8_to_bf16x8(o));
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -379,8 +599,9 @@ struct KernelTable {
             case 3: return stream_rows_kernel<1, kU, true, CL>;
             case 4: return stream_rows_kernel<2, kU, false, CL>;
             case 5: return stream_rows_kernel<2, kU, true, CL>;
-            case 8: return stream_rows_kernel<4, kU, false, CL>;
-            case 9: return stream_rows_kernel<4, kU, true, CL>;
+            // four chunks per thread: two segments per step keep the loads in registers
+            case 8: return stream_rows_kernel<4, 2, false, CL>;
+            case 9: return stream_rows_kernel<4, 2, true, CL>;
         }
         return nullptr;
     }
@@ -420,7 +641,8 @@ static bool consumer_layout(int chunks, int* cpt, int* threads) {
 }
 
 bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
-                      int max_cluster, int C, int stage_bytes, StreamPlan* p, int producers) {
+                      int max_cluster, int C, int stage_bytes, StreamPlan* p, int producers,
+                      int max_tail_parts) {
     const int chunks = H / 8;
     const int nseg = (shared ? R : 0) + 1 + R * K;
     if (chunks < 1 || T < 1) return false;
@@ -485,8 +707,24 @@ bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, 
     p->cpt = cpt;
     p->threads = threads + 32 * W;
     p->smem = stream_ring_offset(nst) + nst * slot_bytes;
+    p->geo.main_rows = T;
+    p->geo.tail_parts = 1;
     if (C == 1) {
         p->grid = (int)(T < num_sms ? T : num_sms);
+        // The last wave (T mod num_sms rows; all rows when T < num_sms) would
+        // leave SMs idle: split each of its rows into m segment intervals on
+        // m CTAs, m = the largest that fits beside the others, capped.
+        const int64_t tail = T % num_sms;
+        if (max_tail_parts >= 2 && tail > 0) {
+            int64_t m = num_sms / tail;
+            if (m > max_tail_parts) m = max_tail_parts;
+            if (m > nseg) m = nseg;
+            if (m >= 2) {
+                p->geo.main_rows = T - tail;
+                p->geo.tail_parts = (int)m;
+                if (T < num_sms) p->grid = (int)(tail * m);
+            }
+        }
     } else {
         const int per_sm = smem_optin / p->smem > 0 ? smem_optin / p->smem : 1;
         int64_t clusters = ((int64_t)num_sms * per_sm) / C;
