@@ -263,6 +263,17 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
     return r;
 }
 
+// Store 4 bytes into a peer CTA's shared memory (addresses from
+// map_shared_rank) as an asynchronous store that completes as 4 transaction
+// bytes on the peer's mbarrier: no release fence, so it does not wait for the
+// issuing thread's earlier global stores; the value is visible to whoever
+// observes the barrier's phase complete.
+__device__ __forceinline__ void st_async_remote_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }

@@ -10,9 +10,11 @@
 // shared memory: every CTA sends slice j of its partial row to CTA j with one
 // bulk copy (shared -> peer shared, the TMA engine), completing on CTA j's
 // receive mbarrier; CTA c then sums its C received slices locally (fixed rank
-// order), which is h for column tile c.  The tile sums of squares are pushed
-// into every peer with a remote mbarrier arrive; each CTA normalises and
-// stores its tile.
+// order), which is h for column tile c.  The tile sums of squares go to
+// every peer as asynchronous remote stores (st.async) counted as transaction
+// bytes on the peer's barrier -- no release fence, so they do not wait for
+// the residual_out stores just issued; each CTA normalises and stores its
+// tile.
 //
 //   producer warp: shared partials + residual copies go out at once (they
 //     need no routing metadata) on mbarrier 0; the routed copies follow as
@@ -85,11 +87,13 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         mbar_init(smem_addr(&bar[0]), 1);
         mbar_init(smem_addr(&bar[1]), 1);
         mbar_init(smem_addr(rbar), 1);
-        mbar_init(smem_addr(ssbar), (uint32_t)C);
+        mbar_init(smem_addr(ssbar), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        // every source CTA sends this tile's slice of its partial row
+        // every source CTA sends this tile's slice of its partial row, and its
+        // tile's sum of squares (4 bytes)
         mbar_arrive_expect_tx(smem_addr(rbar), (uint32_t)(C * ntile_c * 32));
+        mbar_arrive_expect_tx(smem_addr(ssbar), (uint32_t)C * 4u);
     }
     __syncthreads();
     // barrier A, arrive: this CTA's mbarriers exist
@@ -103,18 +107,20 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         const bool mine = i < ns;
         const bool is_sr = mine && i < nsr_c;
         const uint32_t dst = smem_addr(segbuf + (size_t)i * geo.seg_stride);
-        // 1. perm-independent copies, at once
-        if (is_sr) {
-            const uint16_t* src = s < nS ? a.S[s] + t * H : a.residual + t * H;
-            bulk_g2s(dst, src, row_bytes, smem_addr(&bar[0]), pol);
-        }
-        // 2. routing metadata -> routed copies
+        // 1. routing metadata requested first (a bulk-copy instruction
+        //    holds the warp for about a memory latency), then the
+        //    perm-independent copies, at once
         int32_t raw = 0;
         float wv = 0.0f;
         if (lane < a.K) {
             raw = __ldg(a.perm + t * a.K + lane);
             wv = __ldg(a.w + t * a.K + lane);
         }
+        if (is_sr) {
+            const uint16_t* src = s < nS ? a.S[s] + t * H : a.residual + t * H;
+            bulk_g2s(dst, src, row_bytes, smem_addr(&bar[0]), pol);
+        }
+        // 2. routed copies
         const int64_t rowv = lane < a.K ? checked_row(raw, a.rows_e, a.err) : 0;
         const int e = s - nsr;
         const int k = (mine && !is_sr) ? e / a.R : 0;
@@ -256,10 +262,10 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         float tot = 0.0f;
         for (int w = 0; w < ncw; ++w) tot += red[w];
         // push this tile's sum of squares into every peer's slot c
-        if (ci < C) {
-            st_shared_cluster_f32(map_shared_rank(smem_addr(ss_slots + c), (uint32_t)ci), tot);
-            mbar_arrive_remote(map_shared_rank(smem_addr(ssbar), (uint32_t)ci));
-        }
+        // (asynchronous remote stores counted on the peer's barrier)
+        if (ci < C)
+            st_async_remote_f32(map_shared_rank(smem_addr(ss_slots + c), (uint32_t)ci), tot,
+                                map_shared_rank(smem_addr(ssbar), (uint32_t)ci));
         if (ok2 && !mbar_wait_bounded<true>(smem_addr(ssbar), 0u, abort_flag)) {
             if (!*abort_flag) atomicOr(a.err, kErrTimeout);
             *abort_flag = 1;

@@ -22,9 +22,10 @@
 //   * after a row's last segment the consumers finish the row on chip: store
 //     residual_out, reduce the sum of squares (warp shuffle + one named
 //     barrier), and -- for tiles -- push the CTA's partial into every peer's
-//     shared memory with a remote mbarrier arrive (distributed shared
-//     memory), then scale by rsqrt(mean + eps) * (gamma + weight_bias) and
-//     store out.  The ring keeps streaming the next row meanwhile.
+//     shared memory as an asynchronous remote store (st.async, distributed
+//     shared memory) counted as transaction bytes on the peer's barrier,
+//     then scale by rsqrt(mean + eps) * (gamma + weight_bias) and store out.
+//     The ring keeps streaming the next row meanwhile.
 //
 // Every input byte is read once and every output byte written once.  Rows
 // go round-robin over persistent CTAs (C = 1) or clusters (C > 1).
@@ -144,8 +145,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
             mbar_init(smem_addr(&empty[s]), (uint32_t)ncw);
             rec[s] = 0;
         }
-        mbar_init(smem_addr(&xbar[0]), (uint32_t)C);
-        mbar_init(smem_addr(&xbar[1]), (uint32_t)C);
+        mbar_init(smem_addr(&xbar[0]), 1);  // + C * 4 bytes of peer partials per row
+        mbar_init(smem_addr(&xbar[1]), 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_mbar_init();
@@ -421,12 +422,13 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         for (int w = 0; w < ncw; ++w) tot += red[par_row * 32 + w];
         if (CLUSTERED) {
             // Push this CTA's partial into every peer (lane rk -> peer rk, all
-            // at once), then wait for all C partials of the row.
+            // at once, asynchronous stores that count as transaction bytes on
+            // the peer's barrier), then wait for all C partials of the row.
             const uint32_t xb = smem_addr(&xbar[par_row]);
+            if (ci == 0) mbar_arrive_expect_tx(xb, (uint32_t)C * 4u);
             if (ci < C) {
                 const uint32_t mine = smem_addr(&xslot[par_row * kMaxCluster + crank]);
-                st_shared_cluster_f32(map_shared_rank(mine, (uint32_t)ci), tot);
-                mbar_arrive_remote(map_shared_rank(xb, (uint32_t)ci));
+                st_async_remote_f32(map_shared_rank(mine, (uint32_t)ci), tot, map_shared_rank(xb, (uint32_t)ci));
             }
             if (ok && !mbar_wait_bounded<true>(xb, (xph >> par_row) & 1u, abort_flag)) {
                 ok = false;
