@@ -254,8 +254,8 @@ ARFUSE_API ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps
 /*
  * Cap the split of whole-row streaming (AR_REGIME_STREAM) over its last,
  * partial wave: with T mod SMs = n > 0 rows left for the last wave, each of
- * those rows is split into up to m = min(max_parts, SMs / n) segment
- * intervals on m CTAs, whose fp32 partial rows meet in the workspace scratch;
+ * those rows is split into up to m = min(max_parts, SMs / n, segments / 8)
+ * segment intervals on m CTAs, whose fp32 partial rows meet in the workspace scratch;
  * the CTA that brings the last part sums the parts in part order and finishes
  * the row (no CTA waits for another).  max_parts 0 or 1 never splits; 2 ..
  * AR_MAX_SPLIT_PARTS caps m (default AR_MAX_SPLIT_PARTS).  Other values are

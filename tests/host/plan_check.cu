@@ -43,7 +43,7 @@ int main() {
         if (C != 1 || !split) bad = true;
         if (g.main_rows % p.grid) bad = true;
         if ((T - g.main_rows) * g.tail_parts > p.grid) bad = true;
-        if (g.tail_parts > nseg) bad = true;
+        if (g.tail_parts > nseg / 8) bad = true;
         if (T < 152 && (g.main_rows != 0 || p.grid != T * g.tail_parts)) bad = true;
         if (p.grid > 152) bad = true;
         for (int q = 0; q < g.tail_parts; ++q)

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import tp_reduce_moe_gb300 as arf
-from gen import CONFIGS, make_inputs, make_perm_decode_inputs
+from gen import CONFIGS, Config, make_inputs, make_perm_decode_inputs
 from tests._util import check_bf16, check_f32, oracle_args, run_oracle
 
 pytestmark = pytest.mark.gpu
@@ -555,8 +555,13 @@ def test_tuning_controls_leave_results_unchanged(cfg, T):
         ws.destroy()
 
 
-@pytest.mark.parametrize("cfg,T", [("tiny", 153), ("tiny", 170), ("tiny", 7), ("dsv3_decode", 16),
-                                   ("dsv3_decode", 64), ("glm_gemma", 16), ("ar_only", 40)])
+# a small heavy-row shape (37 segments per row: up to four parts) for split-row tests
+SPLIT_CFG = Config("split_small", 9, R=4, K=8, H=512, Ts=(160,), eps=1e-6, weights="softmax")
+
+
+@pytest.mark.parametrize("cfg,T", [(SPLIT_CFG, 153), (SPLIT_CFG, 170), (SPLIT_CFG, 7), ("dsv3_decode", 16),
+                                   ("dsv3_decode", 64), ("glm_gemma", 16)],
+                         ids=["small-T153", "small-T170", "small-T7", "dsv3-T16", "dsv3-T64", "glm-T16"])
 def test_split_rows_of_the_last_wave(cfg, T):
     """Whole-row streaming with the last wave's rows split over several CTAs
     (partial rows meet in the workspace scratch, the last arriving CTA
@@ -574,7 +579,7 @@ def test_split_rows_of_the_last_wave(cfg, T):
                 for rep in range(3):
                     out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_STREAM)
                     torch.cuda.synchronize()
-                    tag = f"split rows {cfg} T={T} parts<={parts} fp32={fp32} call {rep}"
+                    tag = f"split rows {getattr(cfg, 'name', cfg)} T={T} parts<={parts} fp32={fp32} call {rep}"
                     check_bf16(out, ref["out"], tag + " out")
                     if fp32:
                         check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")

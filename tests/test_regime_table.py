@@ -161,3 +161,14 @@ def test_whole_row_streaming_splits_the_last_wave(dsv3):
     assert dsv3.plan(16) == (arf.AR_REGIME_STREAM, 16)
     arf.ar_workspace_set_split_rows(dsv3.ws, 3)
     assert dsv3.plan(16) == (arf.AR_REGIME_STREAM, 48)
+
+
+def test_light_rows_are_never_split():
+    """Three segments per row (K = 0): a split part would hold a single segment."""
+    s = Shape(2, 0, 7168)
+    try:
+        arf.ar_workspace_set_regime(s.ws, arf.AR_REGIME_STREAM)
+        assert s.plan(1) == (arf.AR_REGIME_STREAM, 1)
+        assert s.plan(192) == (arf.AR_REGIME_STREAM, 152)
+    finally:
+        s.ws.destroy()

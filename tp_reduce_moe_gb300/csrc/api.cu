@@ -69,7 +69,8 @@ Range range_of(const void* p, int64_t bytes) {
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
 // Regime tables measured on GB300 (tp_reduce_moe_gb300.tune: every regime and
-// cluster size, L2-cold, T = 1..256), installed for these shapes at create.
+// cluster size, L2-cold, T = 1..256; ties within noise merged into the
+// neighbouring rule), installed for these shapes at create.
 struct BuiltinTable {
     int R, K, H, n;
     ar_regime_rule rules[6];
@@ -87,10 +88,8 @@ const BuiltinTable kBuiltinTables[] = {
     {8, 8, 6144, 5,
      {{4, AR_REGIME_SPLIT, 16}, {12, AR_REGIME_SPLIT, 8}, {32, AR_REGIME_CLUSTER, 8},
       {64, AR_REGIME_CLUSTER, 4}, {256, AR_REGIME_STREAM, 0}}},
-    // H = 8192, top-10, TP8
-    {8, 10, 8192, 4,
-     {{4, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 2},
-      {256, AR_REGIME_STREAM, 0}}},
+    // H = 8192, top-10, TP8 (from T = 48 whole rows, the last wave's rows split)
+    {8, 10, 8192, 3, {{4, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {256, AR_REGIME_STREAM, 0}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0)
     {2, 0, 7168, 2, {{96, AR_REGIME_ONESHOT, 0}, {256, AR_REGIME_STREAM, 0}}},
 };

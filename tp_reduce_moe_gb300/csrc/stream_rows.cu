@@ -52,6 +52,7 @@ constexpr int kStreamMaxProducers = 4;
 constexpr int kStreamMaxThreads = 32 * kStreamMaxProducers + kStreamMaxConsumers;
 constexpr int kStreamMaxStages = 128;
 constexpr int kMaxCluster = 16;
+constexpr int kMinPartSegs = 8;  // segments per part of a split row, at least
 
 // Shared-memory header: full[n], empty[n], xbar[2] mbarriers; xslot[2][16]
 // (pushed partial sums of squares), red[2][32] (per-warp partials), the abort
@@ -716,11 +717,13 @@ bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, 
         // The last wave (T mod num_sms rows; all rows when T < num_sms) would
         // leave SMs idle: split each of its rows into m segment intervals on
         // m CTAs, m = the largest that fits beside the others, capped.
+        // Parts keep at least kMinPartSegs segments: a light row (K = 0 has
+        // three) gains nothing from splitting and pays the parts' reduction.
         const int64_t tail = T % num_sms;
         if (max_tail_parts >= 2 && tail > 0) {
             int64_t m = num_sms / tail;
             if (m > max_tail_parts) m = max_tail_parts;
-            if (m > nseg) m = nseg;
+            if (m > nseg / kMinPartSegs) m = nseg / kMinPartSegs;
             if (m >= 2) {
                 p->geo.main_rows = T - tail;
                 p->geo.tail_parts = (int)m;
