@@ -71,6 +71,27 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float f[8]) {
     }
 }
 
+// acc[0..7] += c * (the 8 bf16 of v), as four packed fp32x2 fused
+// multiply-adds (fma.rn.f32x2: two independent round-to-nearest FMAs, so the
+// result is bit-identical to eight scalar fmaf).  Decoding a bf16 pair costs
+// one shift and one mask, so a pair of elements takes three instructions
+// instead of four.
+__device__ __forceinline__ void fma_bf16x8(float acc[8], float c, const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
+        asm("{\n\t.reg .b64 a2, x2, c2;\n\t"
+            "mov.b64 a2, {%0, %1};\n\t"
+            "mov.b64 x2, {%2, %3};\n\t"
+            "mov.b64 c2, {%4, %4};\n\t"
+            "fma.rn.f32x2 a2, c2, x2, a2;\n\t"
+            "mov.b64 {%0, %1}, a2;\n\t}"
+            : "+f"(acc[2 * q]), "+f"(acc[2 * q + 1])
+            : "f"(lo), "f"(hi), "f"(c));
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // round to nearest even
     return *reinterpret_cast<uint32_t*>(&p);
@@ -165,6 +186,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns();
+
+// After a wait has run out (an error path only): keep the CTA resident for
+// `ns` nanoseconds so that asynchronous copies and stores still in flight to
+// or from its shared memory land before it exits.
+__device__ __forceinline__ void grace_period(unsigned long long ns) {
+    const unsigned long long t0 = global_timer_ns();
+    for (unsigned it = 0; it < 1000000u && global_timer_ns() - t0 < ns; ++it) __nanosleep(1000);
 }
 
 __device__ __forceinline__ unsigned long long global_timer_ns() {

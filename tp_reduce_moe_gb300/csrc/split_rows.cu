@@ -24,13 +24,14 @@
 //     locally, send its slices; wait for the C slices of this tile; local sums;
 //     push the tile's sum of squares; wait for the C sums; normalise; store.
 //
-// Cluster barrier A (arrived on right after the mbarriers are initialised,
+// One cluster barrier (arrived on right after the mbarriers are initialised,
 // waited on just before the first send) keeps peers from signalling a
-// barrier that does not exist yet; barrier B (arrived on once everything
-// expected has been received, waited on at exit) keeps every CTA resident
-// until the copies reading its shared memory have landed.  Every mbarrier
-// wait is bounded (arf::mbar_wait_bounded); both cluster barriers are reached
-// unconditionally by every thread.
+// barrier that does not exist yet.  None is needed at exit: a CTA sends its
+// sum of squares only after it has received every slice, so once a CTA holds
+// all C sums, every copy that reads its partial row has landed and nothing
+// more will be written into it.  Every mbarrier wait is bounded
+// (arf::mbar_wait_bounded); after one runs out, the CTA waits a bounded grace
+// period for copies in flight before it exits.
 //
 // Operation: sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and
 // wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
@@ -155,13 +156,14 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                 if (!*abort_flag) atomicOr(a.err, kErrTimeout);
                 *abort_flag = 1;
             }
-            for (int i0 = i_begin; i0 < i_end; i0 += 4) {
-                float cf[4];
-                uint4 v[4][CPT];
+            constexpr int SU = CPT >= 4 ? 2 : 4;  // segments per step (loads in registers)
+            for (int i0 = i_begin; i0 < i_end; i0 += SU) {
+                float cf[SU];
+                uint4 v[SU][CPT];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) cf[u] = i0 + u < i_end ? coef[i0 + u] : 0.0f;
+                for (int u = 0; u < SU; ++u) cf[u] = i0 + u < i_end ? coef[i0 + u] : 0.0f;
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < SU; ++u)
 #pragma unroll
                     for (int m = 0; m < CPT; ++m) {
                         const int ch = ci + m * nct;
@@ -169,15 +171,12 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                             v[u][m] = reinterpret_cast<const uint4*>(segbuf + (size_t)(i0 + u) * geo.seg_stride)[ch];
                     }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < SU; ++u)
 #pragma unroll
                     for (int m = 0; m < CPT; ++m) {
                         const int ch = ci + m * nct;
                         if (i0 + u < i_end && ch < chunks) {
-                            float f[8];
-                            bf16x8_to_f32(v[u][m], f);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) acc[m][j] = fmaf(cf[u], f[j], acc[m][j]);
+                            fma_bf16x8(acc[m], cf[u], v[u][m]);
                         }
                     }
             }
@@ -262,8 +261,10 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         float tot = 0.0f;
         for (int w = 0; w < ncw; ++w) tot += red[w];
         // push this tile's sum of squares into every peer's slot c
-        // (asynchronous remote stores counted on the peer's barrier)
-        if (ci < C)
+        // (asynchronous remote stores counted on the peer's barrier) -- only
+        // once every slice has arrived, which is what lets the receivers
+        // exit without a cluster barrier
+        if (ci < C && ok2)
             st_async_remote_f32(map_shared_rank(smem_addr(ss_slots + c), (uint32_t)ci), tot,
                                 map_shared_rank(smem_addr(ssbar), (uint32_t)ci));
         if (ok2 && !mbar_wait_bounded<true>(smem_addr(ssbar), 0u, abort_flag)) {
@@ -271,11 +272,6 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             *abort_flag = 1;
         }
     }
-
-    // ---- barrier B, arrive: everything this CTA expects has arrived (so the
-    // copies that read its partial row have landed in their targets' memory)
-    __syncwarp();
-    cluster_arrive_release();
 
     float total = 0.0f;
     for (int r = 0; r < C; ++r) total += reinterpret_cast<volatile float*>(ss_slots)[r];
@@ -294,16 +290,16 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                        pack_bf16x2(hq[m].z * inv * g2, hq[m].w * inv * g3));
     }
 
-    // After an abort, copies may still be landing: wait (briefly) for both
-    // barriers before the CTA may exit.
+    // After an abort, copies may still be landing in or reading from this
+    // CTA's shared memory: wait (bounded) for its barriers, then a grace
+    // period, before the CTA may exit.
     if (threadIdx.x == 0 && *abort_flag) {
         if (nsr_c > 0) (void)mbar_wait_bounded(smem_addr(&bar[0]), 0u, nullptr, 10000000ull);
         if (ns > nsr_c) (void)mbar_wait_bounded(smem_addr(&bar[1]), 0u, nullptr, 10000000ull);
         (void)mbar_wait_bounded(smem_addr(rbar), 0u, nullptr, 10000000ull);
+        (void)mbar_wait_bounded<true>(smem_addr(ssbar), 0u, nullptr, 10000000ull);
+        grace_period(1000000ull);
     }
-    // ---- barrier B, wait: no CTA leaves while a peer may still read it
-    __syncwarp();
-    cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------------ host side

@@ -33,9 +33,10 @@
 // Every wait is bounded (arf::mbar_wait_bounded): a wait that runs out sets
 // the workspace error word and an abort flag, later waits are skipped (rows
 // are left unfinished, never hung), and the producer waits (bounded again)
-// for its own copies in flight before the CTA exits.  A clustered CTA ends
-// with a cluster barrier so that no CTA leaves while a peer may still write
-// into its shared memory.
+// for its own copies in flight before the CTA exits.  A clustered CTA needs
+// no exit barrier: it leaves only after every peer's partial of its last row
+// has arrived, so no peer writes into it afterwards (after an abort it waits
+// a bounded grace period instead).
 //
 // Operation: sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and
 // wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
@@ -324,11 +325,6 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
                     (void)mbar_wait_bounded(smem_addr(&full[j]), (uint32_t)(rec[j] - 1), nullptr,
                                             10000000ull);
         }
-        __syncwarp();
-        if (CLUSTERED) {
-            cluster_arrive_release();
-            cluster_wait_acquire();
-        }
         return;
     }
 
@@ -389,10 +385,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
 #pragma unroll
                     for (int m = 0; m < CPT; ++m)
                         if (i0 + u < cnt && valid[m]) {
-                            float f[8];
-                            bf16x8_to_f32(v[u][m], f);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) acc[m][j] = fmaf(cf[u], f[j], acc[m][j]);
+                            fma_bf16x8(acc[m], cf[u], v[u][m]);
                         }
             }
             __syncwarp();
@@ -440,9 +433,6 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
             const volatile float* xs = xslot + par_row * kMaxCluster;
             tot = 0.0f;
             for (int rk = 0; rk < C; ++rk) tot += xs[rk];
-            // After the last row's push, arrive on the exit barrier now and
-            // wait at the end: no CTA leaves while a peer may still push into it.
-            if (t + row_step >= main_rows) cluster_arrive_release();
         }
         const float inv = rsqrtf(tot / (float)H + a.eps);
 #pragma unroll
@@ -457,10 +447,11 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         }
         par_row ^= 1;
     }
-    if (CLUSTERED) {
-        if (first_row >= a.T) cluster_arrive_release();  // a cluster without rows
-        cluster_wait_acquire();
-    }
+    // No exit barrier for clusters: a CTA leaves after it has received every
+    // peer's partial of its last row, so nothing more is written into it (and
+    // it reads nothing remote).  After an abort, a bounded grace period lets
+    // peers' pushes still in flight land first.
+    if (CLUSTERED && ci == 0 && *abort_flag) grace_period(1000000ull);
     if (!CLUSTERED && has_part) {
         // This CTA's part of a split row: accumulate its segments, publish the
         // fp32 partial row, count the parts in; the CTA that brings the last
@@ -503,10 +494,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
 #pragma unroll
                     for (int m = 0; m < CPT; ++m)
                         if (i0 + u < cnt && valid[m]) {
-                            float f[8];
-                            bf16x8_to_f32(v[u][m], f);
-#pragma unroll
-                            for (int jj = 0; jj < 8; ++jj) acc[m][jj] = fmaf(cf[u], f[jj], acc[m][jj]);
+                            fma_bf16x8(acc[m], cf[u], v[u][m]);
                         }
             }
             __syncwarp();
