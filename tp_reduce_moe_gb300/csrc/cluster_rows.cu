@@ -35,8 +35,9 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
     __shared__ int64_t s_row[kMaxTopK];
     __shared__ float s_w[kMaxTopK];
     __shared__ float s_warp[32];
-    __shared__ float s_part;   // this CTA's sum of squares, read by its peers
-    __shared__ float s_total;  // the row's sum of squares
+    __shared__ float s_parts[16];  // every CTA's sum of squares, pushed in by the CTAs
+    __shared__ __align__(8) uint64_t s_bar;  // C * 4 bytes of pushed sums
+    __shared__ int s_abort;
 
     const int tid = threadIdx.x;
     const int64_t t = blockIdx.x / C;
@@ -50,6 +51,22 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
     const int nS = a.has_shared ? a.R : 0;
     const int NT = active ? nS + a.R * a.K : 0;
     const int64_t rowoff = t * H + col;
+
+    // The exchange barrier exists (and expects its C pushed sums) before any
+    // peer may push: cluster barrier arrived on here, waited on before the push.
+    if (tid == 0) {
+        mbar_init(smem_addr(&s_bar), 1);
+        s_abort = 0;
+        fence_mbar_init();
+        mbar_arrive_expect_tx(smem_addr(&s_bar), (uint32_t)C * 4u);
+    }
+    if (C > 1) {
+        __syncthreads();
+        cluster_arrive_release();
+    }
+    // gamma, requested now (it is needed only at the end)
+    uint4 gv = make_uint4(0, 0, 0, 0);
+    if (g == 0 && active) gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + col));
 
     for (int k = tid; k < a.K; k += blockDim.x) {
         s_row[k] = checked_row(a.perm[t * a.K + k], a.rows_e, a.err);
@@ -132,37 +149,45 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
     ss = warp_sum(ss);
     if ((tid & 31) == 0) s_warp[tid >> 5] = ss;
     __syncthreads();
-    if (tid == 0) {
-        float tot = 0.0f;
-        const int nw = (blockDim.x + 31) >> 5;
-        for (int w = 0; w < nw; ++w) tot += s_warp[w];
-        s_part = tot;
-        s_total = tot;
-    }
+    float total;
     if (C > 1) {
-        cluster_arrive_release();
-        cluster_wait_acquire();
-        if (tid == 0) {
-            const uint32_t mine = smem_addr(&s_part);
+        // Thread rk (and rk + blockDim, ...) sums the CTA's warps and pushes
+        // the CTA's sum into peer rk (asynchronous remote stores counted on
+        // the peer's barrier);
+        // every thread waits for the C sums of the row.  No exit barrier:
+        // the pushes are the only remote accesses, and a CTA leaves only
+        // after every peer's push into it has landed.
+        cluster_wait_acquire();  // every peer's barrier exists
+        if (tid < C) {  // a block may have fewer threads than the cluster has CTAs
             float tot = 0.0f;
-            for (int rk = 0; rk < C; ++rk) tot += ld_shared_cluster_f32(map_shared_rank(mine, rk));
-            s_total = tot;
+            const int nw = (blockDim.x + 31) >> 5;
+            for (int w = 0; w < nw; ++w) tot += s_warp[w];
+            for (int rk = tid; rk < C; rk += blockDim.x)
+                st_async_remote_f32(map_shared_rank(smem_addr(&s_parts[c]), (uint32_t)rk), tot,
+                                    map_shared_rank(smem_addr(&s_bar), (uint32_t)rk));
         }
-        __syncwarp();
-        cluster_arrive_release();  // this CTA is done reading its peers
+        if (!mbar_wait_bounded<true>(smem_addr(&s_bar), 0u, reinterpret_cast<volatile int*>(&s_abort))) {
+            if (!s_abort) atomicOr(a.err, kErrTimeout);
+            s_abort = 1;
+        }
+        total = 0.0f;
+        for (int rk = 0; rk < C; ++rk) total += reinterpret_cast<volatile float*>(s_parts)[rk];
+    } else {
+        total = 0.0f;
+        const int nw = (blockDim.x + 31) >> 5;
+        for (int w = 0; w < nw; ++w) total += s_warp[w];
     }
-    __syncthreads();
 
     if (g == 0 && active) {
-        const float inv = rsqrtf(s_total / (float)H + a.eps);
-        const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma + col);
+        const float inv = rsqrtf(total / (float)H + a.eps);
         float gf[8], o[8];
         bf16x8_to_f32(gv, gf);
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j] = h[j] * inv * (gf[j] + a.weight_bias);
         st_global16(reinterpret_cast<uint16_t*>(a.out) + rowoff, f32x8_to_bf16x8(o));
     }
-    if (C > 1) cluster_wait_acquire();  // no CTA leaves while a peer may read it
+    // after a wait that ran out: let pushes still in flight land first
+    if (C > 1 && tid == 0 && s_abort) grace_period(1000000ull);
 }
 
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }

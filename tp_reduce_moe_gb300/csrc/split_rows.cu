@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     const size_t slice = (size_t)tile * 8;  // floats per source slice
     float4 hq[CPT];
     bool hv[CPT];
+    uint2 gpre[CPT];  // gamma of this thread's items, requested before the exchanges
     float ss = 0.0f;
     bool ok2 = true;
     if (warp > 0 && !mbar_wait_bounded(smem_addr(rbar), 0u, abort_flag)) {
@@ -230,7 +231,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         const int q = ci + m * nct;
         hv[m] = warp > 0 && q < 2 * ntile;
         hq[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        gpre[m] = make_uint2(0, 0);
         if (!hv[m]) continue;
+        gpre[m] = __ldg(reinterpret_cast<const uint2*>(a.gamma + (int64_t)tile0 * 8 + (int64_t)q * 4));
         const float* src = recv + (size_t)q * 4;
         for (int r = 0; r < C; ++r) {
             const float4 x = *reinterpret_cast<const float4*>(src + r * slice);
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     for (int m = 0; m < CPT; ++m) {
         if (!hv[m]) continue;
         const int64_t col = (int64_t)tile0 * 8 + (int64_t)(ci + m * nct) * 4;
-        const uint2 gv = *reinterpret_cast<const uint2*>(a.gamma + col);
+        const uint2 gv = gpre[m];
         const float g0 = __uint_as_float(gv.x << 16) + wb, g1 = __uint_as_float(gv.x & 0xffff0000u) + wb;
         const float g2 = __uint_as_float(gv.y << 16) + wb, g3 = __uint_as_float(gv.y & 0xffff0000u) + wb;
         *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + t * H + col) =
