@@ -89,6 +89,10 @@ def parse():
                    help="comma list of regimes timed in the sweep (same tokens as --regime)")
     p.add_argument("--sweep-only", default="",
                    help="comma list of workloads to sweep (default: all)")
+    p.add_argument("--pdl", action="store_true",
+                   help="headline and e2e workspaces launch with programmatic dependent launch")
+    p.add_argument("--sweep-pdl", choices=["off", "on", "both"], default="both",
+                   help="sweep points without / with programmatic dependent launch (AR_WS_PDL)")
     p.add_argument("--sweep-mode", choices=["rotate", "scatter", "warm"], default="rotate",
                    help="rotate: L2-cold, each call gathers within its own expert block; "
                         "scatter: L2-cold, gathers spread over all sets' rows; "
@@ -312,7 +316,8 @@ def main_ours(args):
     R, K, H = cfg.R, cfg.K, cfg.H
     # weak scaling: every rank draws and reduces its own T token rows
     d = make_inputs(cfg, T, seed=rank_seed(cfg.index, T, rank), device=dev)
-    ws = arf.ar_workspace_create(R, K, H, T, cfg.eps, device=local)
+    ws = arf.ar_workspace_create(R, K, H, T, cfg.eps, device=local,
+                                 flags=arf.AR_WS_PDL if args.pdl else 0)
     force, csize = parse_regime(args.regime)
     arf.ar_workspace_set_regime(ws, force)
     arf.ar_workspace_set_cluster_size(ws, csize)
@@ -394,7 +399,8 @@ def main_ours(args):
     if not args.no_sweep and rank == 0:
         sweep = run_sweep(arf, torch, dev, stream, peak, args.sweep_regimes.split(","),
                           [w for w in args.sweep_only.split(",") if w], args.sweep_mode,
-                          gated=args.gated)
+                          gated=args.gated,
+                          pdls={"off": (False,), "on": (True,), "both": (False, True)}[args.sweep_pdl])
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
@@ -411,6 +417,7 @@ def main_ours(args):
                 "config": headline_config(args.workload, T, world),
                 "us_per_call": round(1e3 * ms_per_step, 3),
                 "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas, "gated": bool(args.gated),
+                "pdl": bool(args.pdl),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps, "clocks": clocks.summary(), "sweep": sweep}
         print(json.dumps(line), flush=True)
@@ -482,7 +489,7 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
 
 
 def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate",
-              gated=False):
+              gated=False, pdls=(False,)):
     """µs/call vs T for every workload: L2-cold by rotating through disjoint
     input sets (>= 3x L2 in total; each set gathers only within its own block
     of expert rows, like successive layers), timed by replaying a CUDA graph
@@ -498,19 +505,21 @@ def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="r
             if name == "prefill" and T == HEADLINE[1]:
                 continue
             for regime_name in regimes:
-                res.append(sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T,
-                                       *parse_regime(regime_name), mode=mode,
-                                       gated=gated and cfg.K > 0))
+                for pdl in pdls:
+                    res.append(sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T,
+                                           *parse_regime(regime_name), mode=mode,
+                                           gated=gated and cfg.K > 0, pdl=pdl))
     from gen import MHC_SHAPES
     for name, shp in MHC_SHAPES.items():
         if only and name not in only and "mhc" not in only:
             continue
         for T in shp["Ts"]:
-            res.append(sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode))
+            for pdl in pdls:
+                res.append(sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode, pdl))
     return res
 
 
-def sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode="rotate"):
+def sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode="rotate", pdl=False):
     """One T of the all-reduce + mHC write-back (ar_mhc_post), timed like the
     main sweep: a CUDA graph of one call per disjoint input set (>= 3x L2)."""
     from gen import make_mhc_inputs, mhc_problem_bytes
@@ -520,7 +529,7 @@ def sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode="rotat
     inp = make_mhc_inputs(R, H, hc, T * n_sets, seed=5 + T, device=dev)
     P, x, post, comb = inp["P"], inp["x"], inp["post"], inp["comb"]
     out = torch.empty_like(x)
-    ws = arf.ar_workspace_create(R, 0, H, T, 1e-6, device=dev.index)
+    ws = arf.ar_workspace_create(R, 0, H, T, 1e-6, device=dev.index, flags=arf.AR_WS_PDL if pdl else 0)
 
     def call(i):
         sl = slice(i * T, (i + 1) * T)
@@ -555,11 +564,11 @@ def sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode="rotat
     return {"workload": name, "R": R, "K": 0, "H": H, "hc": hc, "T": T, "us_per_call": round(us, 3),
             "GBps": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4), "regime": "mhc_post",
             "ctas": None, "forced": False, "calls_per_graph": n_sets, "mode": mode, "gated": False,
-            "device_error": err}
+            "pdl": pdl, "device_error": err}
 
 
 def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0, mode="rotate",
-                gated=False):
+                gated=False, pdl=False):
     """One (workload, T, regime) point of the sweep."""
     from gen import make_gate_logits, make_inputs, problem_bytes
     b = problem_bytes(cfg.R, cfg.K, cfg.H, T)
@@ -568,7 +577,8 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
         n_sets = 1
     big = make_inputs(cfg, T * n_sets, seed=11 + T, device=dev,
                       perm_blocks=n_sets if mode == "rotate" else 1)
-    ws = arf.ar_workspace_create(cfg.R, cfg.K, cfg.H, T, cfg.eps, device=dev.index)
+    ws = arf.ar_workspace_create(cfg.R, cfg.K, cfg.H, T, cfg.eps, device=dev.index,
+                                 flags=arf.AR_WS_PDL if pdl else 0)
     arf.ar_workspace_set_regime(ws, force)
     arf.ar_workspace_set_cluster_size(ws, csize)
     outs = torch.empty((n_sets, T, cfg.H), dtype=torch.bfloat16, device=dev)
@@ -630,7 +640,7 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
             "frac_of_hbm_peak": round(gbs / peak, 4),
             "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas,
             "forced": force != 0, "calls_per_graph": n_sets, "mode": mode, "gated": gated,
-            "device_error": err}
+            "pdl": pdl, "device_error": err}
 
 
 def main():

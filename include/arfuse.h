@@ -83,6 +83,7 @@ typedef enum ar_status {
 /* ar_workspace_create() flags. */
 #define AR_WS_DRY_RUN 0x1u      /* no GPU state: calls validate, then return AR_VALIDATED   */
 #define AR_WS_NORM_BF16_H 0x2u  /* the norm reads h rounded to bf16, as a bf16 residual_out  */
+#define AR_WS_PDL 0x4u          /* launch with programmatic dependent launch (see below)      */
                                 /* stores it (default: the unrounded fp32 sum)              */
 
 /* Bits of the device error word (ar_workspace_device_error). */
@@ -118,7 +119,16 @@ typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
  *   hidden      8 .. AR_MAX_HIDDEN, a multiple of 8
  *   max_tokens  largest T any call may pass (>= 1)
  *   eps         RMSNorm epsilon every call must repeat
- *   flags       0, or AR_WS_DRY_RUN and/or AR_WS_NORM_BF16_H
+ *   flags       0, or any of AR_WS_DRY_RUN, AR_WS_NORM_BF16_H, AR_WS_PDL.
+ *               AR_WS_PDL launches every kernel with programmatic dependent
+ *               launch (cudaLaunchAttributeProgrammaticStreamSerialization):
+ *               the launch may begin while the previous kernel in the stream
+ *               is still running, and the kernel waits (griddepcontrol.wait)
+ *               for that kernel to complete and flush its memory before its
+ *               first global memory access, so results and stream order are
+ *               unchanged; launch latency overlaps the previous kernel.  Every
+ *               kernel also signals its own dependents as soon as it starts
+ *               (kernels launched without the attribute are not affected).
  *   out         host pointer that receives the handle (set to NULL on error)
  * Errors: AR_ERR_INVALID_ARG (out NULL, max_tokens < 1, eps < 0 or not
  * finite), AR_ERR_ALIGNMENT (hidden % 8), AR_ERR_UNSUPPORTED (limits above,

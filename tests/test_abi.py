@@ -378,3 +378,14 @@ def test_split_rows_setter(lib, ws):
     for n in (-1, arf.AR_MAX_SPLIT_PARTS + 1):
         with pytest.raises(arf.ArfuseError):
             arf.ar_workspace_set_split_rows(ws, n)
+
+
+def test_pdl_flag_is_accepted(lib):
+    w = arf.ar_workspace_create(R, K, H, TMAX, EPS, flags=arf.AR_WS_DRY_RUN | arf.AR_WS_PDL)
+    try:
+        assert Fake().call(lib, w) == arf.AR_VALIDATED
+    finally:
+        w.destroy()
+    h = ctypes.c_void_p()
+    assert lib.ar_workspace_create(0, R, K, H, TMAX, EPS, arf.AR_WS_DRY_RUN | 0x8, ctypes.byref(h)) == \
+        arf.AR_ERR_INVALID_ARG

@@ -591,3 +591,33 @@ def test_split_rows_of_the_last_wave(cfg, T):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 4), ("dsv3_decode", 64), ("ar_only", 16), ("prefill", 3)])
+def test_pdl_chain_reads_the_previous_calls_output(cfg, T):
+    """With AR_WS_PDL, calls launched back to back without a host sync, each
+    reading the previous call's residual_out as its residual: every call must
+    see its input complete (griddepcontrol.wait before the first global
+    access).  Each step is checked against the oracle run on the residual the
+    GPU actually fed it."""
+    inp = make_inputs(cfg, T)
+    ws = arf.ar_workspace_create(inp["R"], inp["K"], inp["H"], T, inp["eps"], device=0, flags=arf.AR_WS_PDL)
+    try:
+        d = to_dev(inp)
+        steps = 5
+        res = [d["residual"].clone()] + [torch.empty_like(d["residual"]) for _ in range(steps)]
+        outs = [torch.empty_like(d["residual"]) for _ in range(steps)]
+        for n in range(steps):
+            dn = dict(d)
+            dn["residual"] = res[n]
+            run_gpu(ws, dn, out=outs[n], residual_out=res[n + 1])
+        torch.cuda.synchronize()
+        assert arf.ar_workspace_device_error(ws) == 0
+        for n in range(steps):
+            step = dict(inp)
+            step["residual"] = res[n].cpu()
+            ref = run_oracle(step)
+            check_bf16(outs[n], ref["out"], f"pdl chain {cfg} T={T} step {n} out")
+            check_bf16(res[n + 1], ref["h"], f"pdl chain {cfg} T={T} step {n} residual_out")
+    finally:
+        ws.destroy()

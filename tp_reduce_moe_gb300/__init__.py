@@ -11,7 +11,7 @@ from .binding import (  # noqa: F401
     AR_ERR_DEVICE_CHECK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_MAX_HIDDEN, AR_MAX_RANKS,
     AR_MAX_TOP_K, AR_OK, AR_REGIME_AUTO, AR_REGIME_CLUSTER, AR_REGIME_ONESHOT, AR_REGIME_SPLIT, AR_REGIME_STREAM,
     AR_VALIDATED,
-    AR_WS_DRY_RUN, AR_WS_NORM_BF16_H, LIB_PATH, ArfuseError, Workspace, ar_finalize_rmsnorm, ar_rmsnorm,
+    AR_WS_DRY_RUN, AR_WS_NORM_BF16_H, AR_WS_PDL, LIB_PATH, ArfuseError, Workspace, ar_finalize_rmsnorm, ar_rmsnorm,
     ar_status_string, ar_workspace_create, ar_workspace_destroy, ar_workspace_device_error,
     ar_workspace_last_regime, ar_workspace_set_cluster_size, ar_workspace_set_regime,
     ar_workspace_set_producer_warps, ar_workspace_set_stage_bytes, load_library,

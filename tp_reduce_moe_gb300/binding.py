@@ -29,6 +29,7 @@ AR_VALIDATED = 7
 
 AR_WS_DRY_RUN = 0x1
 AR_WS_NORM_BF16_H = 0x2
+AR_WS_PDL = 0x4
 AR_DEVERR_PERM_RANGE = 0x1
 AR_DEVERR_TIMEOUT = 0x2
 AR_REGIME_AUTO = 0

@@ -316,12 +316,13 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    const bool pdl = (ws->flags & AR_WS_PDL) != 0;
     if (regime == AR_REGIME_ONESHOT)
-        e = arf::launch_cluster_rows(a, pl.c, res_f32 != 0, s);
+        e = arf::launch_cluster_rows(a, pl.c, res_f32 != 0, s, pdl);
     else if (regime == AR_REGIME_SPLIT)
-        e = arf::launch_split_rows(a, pl.x, res_f32 != 0, s);
+        e = arf::launch_split_rows(a, pl.x, res_f32 != 0, s, pdl);
     else
-        e = arf::launch_stream_rows(a, pl.s, res_f32 != 0, s);
+        e = arf::launch_stream_rows(a, pl.s, res_f32 != 0, s, pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ERR_CUDA;
@@ -340,7 +341,7 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
     if (!out) return AR_ERR_INVALID_ARG;
     *out = nullptr;
     if (max_tokens < 1 || !(eps >= 0.0f) || eps > 3.0e38f) return AR_ERR_INVALID_ARG;
-    if ((flags & ~(AR_WS_DRY_RUN | AR_WS_NORM_BF16_H)) != 0) return AR_ERR_INVALID_ARG;
+    if ((flags & ~(AR_WS_DRY_RUN | AR_WS_NORM_BF16_H | AR_WS_PDL)) != 0) return AR_ERR_INVALID_ARG;
     if (hidden < 8 || hidden % 8 != 0) return hidden < 8 ? AR_ERR_UNSUPPORTED : AR_ERR_ALIGNMENT;
     if (ranks < 1 || ranks > AR_MAX_RANKS || top_k < 0 || top_k > AR_MAX_TOP_K ||
         hidden > AR_MAX_HIDDEN || max_tokens > kMaxTokensLimit)
@@ -538,7 +539,8 @@ ar_status ar_mhc_post(ar_workspace* ws, const void* const* partials, int R, cons
     a.R = R;
     a.H = H;
     a.hc = hc;
-    if (arf::launch_mhc_post(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    if (arf::launch_mhc_post(a, static_cast<cudaStream_t>(stream), (ws->flags & AR_WS_PDL) != 0) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ERR_CUDA;
     }

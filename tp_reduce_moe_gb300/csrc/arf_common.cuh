@@ -294,6 +294,15 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
     return r;
 }
 
+// Programmatic dependent launch.  Every kernel lets the next kernel in the
+// stream start launching as soon as it starts (launch_dependents), and waits
+// (griddepcontrol.wait) for the previous kernel to complete and flush its
+// memory before its first global memory access: with the launch attribute,
+// launch latency and prologue overlap the previous kernel's tail; without
+// it both instructions return at once.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Store 4 bytes into a peer CTA's shared memory (addresses from
 // map_shared_rank) as an asynchronous store that completes as 4 transaction
 // bytes on the peer's mbarrier: no release fence, so it does not wait for the
@@ -350,7 +359,7 @@ bool plan_cluster_rows(int R, int K, int H, bool shared, int max_c, int64_t T, i
                        ClusterPlan* p);
 int cluster_rows_max_cluster(int threads, int smem, bool res_f32);
 cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res_f32,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool pdl = false);
 cudaError_t cluster_rows_set_attributes();
 
 // Each ring slot starts with a header holding the coefficient of each of its
@@ -368,7 +377,7 @@ struct MhcArgs {
     int64_t T;
     int R, H, hc;
 };
-cudaError_t launch_mhc_post(const MhcArgs& a, cudaStream_t stream);
+cudaError_t launch_mhc_post(const MhcArgs& a, cudaStream_t stream, bool pdl = false);
 
 struct StreamGeom {
     int nstages;      // ring slots
@@ -403,7 +412,7 @@ bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, 
                       int max_cluster, int C, int stage_bytes, StreamPlan* p, int producers = 0,
                       int max_tail_parts = 0);
 cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, bool res_f32,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool pdl = false);
 cudaError_t stream_rows_set_attributes(int smem_optin);
 // Largest cluster (<= 16) co-schedulable for a clustered plan of this shape.
 int stream_rows_max_cluster(int threads, int smem, int cpt);
@@ -430,7 +439,7 @@ struct SplitPlan {
 bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
                      int max_cluster, int C, SplitPlan* p);
 cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32,
-                              cudaStream_t stream);
+                              cudaStream_t stream, bool pdl = false);
 cudaError_t split_rows_set_attributes(int smem_optin);
 int split_rows_max_cluster(int threads, int smem, int cpt);
 

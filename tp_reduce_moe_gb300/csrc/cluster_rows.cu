@@ -31,6 +31,7 @@ template <bool RES_F32>
 __global__ void __launch_bounds__(kClusterMaxThreads, 1)
     cluster_rows_kernel(const __grid_constant__ RowArgs a, int C, int nch, int G) {
     extern __shared__ __align__(16) uint8_t dyn_smem[];
+    pdl_trigger();
     float4* red = reinterpret_cast<float4*>(dyn_smem);  // [G-1][2][nch]
     __shared__ int64_t s_row[kMaxTopK];
     __shared__ float s_w[kMaxTopK];
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
         __syncthreads();
         cluster_arrive_release();
     }
+    pdl_wait();  // no global memory access before this point
     // gamma, requested now (it is needed only at the end)
     uint4 gv = make_uint4(0, 0, 0, 0);
     if (g == 0 && active) gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + col));
@@ -263,9 +265,14 @@ int cluster_rows_max_cluster(int threads, int smem, bool res_f32) {
 }
 
 cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res_f32,
-                                cudaStream_t stream) {
-    cudaLaunchAttribute attr[1];
+                                cudaStream_t stream, bool pdl) {
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = cluster_config(p, a.T, stream, attr);
+    if (pdl) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
+    }
     if (res_f32)
         return cudaLaunchKernelEx(&cfg, cluster_rows_kernel<true>, a, p.C, p.nch, p.G);
     return cudaLaunchKernelEx(&cfg, cluster_rows_kernel<false>, a, p.C, p.nch, p.G);

@@ -32,6 +32,8 @@ constexpr int kMhcMaxStreams = 8;
 template <int HC>
 __global__ void __launch_bounds__(kMhcThreads)
     mhc_post_kernel(const __grid_constant__ MhcArgs a) {
+    pdl_trigger();
+    pdl_wait();  // no global memory access before this point
     __shared__ float s_post[kMhcMaxStreams];
     __shared__ float s_comb[kMhcMaxStreams * kMhcMaxStreams];
     const int hc = HC > 0 ? HC : a.hc;
@@ -95,17 +97,21 @@ __global__ void __launch_bounds__(kMhcThreads)
     }
 }
 
-cudaError_t launch_mhc_post(const MhcArgs& a, cudaStream_t stream) {
+cudaError_t launch_mhc_post(const MhcArgs& a, cudaStream_t stream, bool pdl) {
     const int chunks = a.H / 8;
     const int per_token = (chunks + kMhcThreads - 1) / kMhcThreads;
     const int64_t grid = a.T * per_token;
     if (grid < 1 || grid > 0x7fffffff) return cudaErrorInvalidValue;
-    if (a.hc == 4) {
-        mhc_post_kernel<4><<<(unsigned)grid, kMhcThreads, 0, stream>>>(a);
-    } else {
-        mhc_post_kernel<0><<<(unsigned)grid, kMhcThreads, 0, stream>>>(a);
-    }
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kMhcThreads);
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return a.hc == 4 ? cudaLaunchKernelEx(&cfg, mhc_post_kernel<4>, a) : cudaLaunchKernelEx(&cfg, mhc_post_kernel<0>, a);
 }
 
 }  // namespace arf

@@ -55,6 +55,7 @@ template <int CPT, bool RES_F32>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     split_rows_kernel(const __grid_constant__ RowArgs a, const SplitGeom geo) {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_trigger();
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     uint64_t* rbar = bar + 2;
     uint64_t* ssbar = bar + 3;
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     __syncthreads();
     // barrier A, arrive: this CTA's mbarriers exist
     cluster_arrive_release();
+    pdl_wait();  // no global memory access before this point
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -402,11 +404,12 @@ int split_rows_max_cluster(int threads, int smem, int cpt) {
     return 1;
 }
 
-cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32, cudaStream_t stream) {
+cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32, cudaStream_t stream,
+                              bool pdl) {
     const void* k = split_kernel_for(p.cpt, res_f32);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3((unsigned)p.threads);
     cfg.dynamicSmemBytes = (size_t)p.smem;
@@ -415,8 +418,10 @@ cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32
     attr[0].val.clusterDim.x = (unsigned)p.geo.C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     void* args[] = {const_cast<RowArgs*>(&a), const_cast<SplitGeom*>(&p.geo)};
     return cudaLaunchKernelExC(&cfg, k, args);
 }

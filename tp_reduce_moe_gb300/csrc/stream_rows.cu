@@ -106,6 +106,7 @@ template <int CPT, int U, bool RES_F32, bool CLUSTERED>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     stream_rows_kernel(const __grid_constant__ RowArgs a, const StreamGeom geo) {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_trigger();
     const int nst = geo.nstages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + nst;
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // no global memory access before this point
     if (CLUSTERED) {  // every peer's barriers exist before anyone pushes
         cluster_arrive_release();
         cluster_wait_acquire();
@@ -750,24 +752,31 @@ int stream_rows_max_cluster(int threads, int smem, int cpt) {
 }
 
 cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, bool res_f32,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool pdl) {
     const bool clustered = p.geo.C > 1;
     const void* k = kernel_for(p.cpt, res_f32, clustered);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3((unsigned)p.threads);
     cfg.dynamicSmemBytes = (size_t)p.smem;
     cfg.stream = stream;
+    int na = 0;
     if (clustered) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)p.geo.C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.geo.C;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = na;
     void* args[] = {const_cast<RowArgs*>(&a), const_cast<StreamGeom*>(&p.geo)};
     return cudaLaunchKernelExC(&cfg, k, args);
 }
