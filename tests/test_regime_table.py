@@ -82,7 +82,7 @@ def test_past_the_last_rule_and_auto_rules_use_the_heuristic(dsv3):
 def test_rule_without_a_plan_falls_back(dsv3):
     arf.ar_workspace_set_regime_table(dsv3.ws, [])
     h1 = dsv3.plan(1)
-    # 81 segments over a 2-CTA split cluster is 41 per CTA: beyond the split
+    # 73 segments over a 2-CTA split cluster is 37 per CTA: beyond the split
     # kernel's 32 producer lanes, so the rule has no plan
     arf.ar_workspace_set_regime_table(dsv3.ws, [(4, arf.AR_REGIME_SPLIT, 2)])
     assert dsv3.plan(1) == h1
