@@ -314,29 +314,9 @@ __device__ __forceinline__ void st_async_remote_f32(uint32_t remote_addr, float 
                  : "memory");
 }
 
-__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 
-// Arrive on an mbarrier of a peer CTA (address from map_shared_rank); the
-// release orders this thread's earlier stores (e.g. st_shared_cluster_f32)
-// before the arrival.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
 
-__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, float4 v) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
-                 "f"(v.z), "f"(v.w)
-                 : "memory");
-}
 
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
 
 // Named barrier over a subset of the CTA's warps (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
