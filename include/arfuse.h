@@ -262,6 +262,23 @@ ARFUSE_API ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes);
 ARFUSE_API ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps);
 
 /*
+ * Column groups per row of the split kernel (AR_REGIME_SPLIT): 1, 2, 4 or 8;
+ * 0 (the default) picks the most groups that leave a plan, each group at least
+ * 128 16-byte chunks wide.  With G groups the C CTAs of a row form G groups
+ * of C/G; each group covers 1/G of the row's columns, its CTAs deal the row's
+ * segments among themselves (bulk copies of 1/G of a row each) and
+ * reduce-scatter only their group's columns, which cuts the distributed-
+ * shared-memory exchange G-fold for G-fold more, smaller copies.  A forced
+ * value that does not split the cluster into groups of at least two CTAs
+ * leaves the split regime without a plan (AR_ERR_UNSUPPORTED when the regime
+ * is forced).  Other values are AR_ERR_INVALID_ARG.  A tuning control:
+ * residual_out equals, bit for bit, that of a split over C/G CTAs without
+ * groups (the same segments per CTA, the same slice order); out differs from
+ * it only through the summation order of the tile sums of squares.
+ */
+ARFUSE_API ar_status ar_workspace_set_split_column_groups(ar_workspace* ws, int groups);
+
+/*
  * Cap the split of whole-row streaming (AR_REGIME_STREAM) over its last,
  * partial wave: with T mod SMs = n > 0 rows left for the last wave, each of
  * those rows is split into up to m = min(max_parts, SMs / n, segments / 8)

@@ -78,30 +78,40 @@ int main() {
       if (bad) { ++fails; if (fails < 20) printf("BAD H=%d R=%d K=%d sh=%d T=%ld Cf=%d -> C=%d tile=%d nst=%d slot=%d thr=%d smem=%d grid=%d\n", H,R,K,sh,T,Cf,C,g.tile_chunks,g.nstages,g.slot_bytes,p.threads,p.smem,p.grid); }
     }
   }
-  // split plans (one row per cluster, segments dealt round-robin)
-  for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts) {
+  // split plans (one row per cluster, segments dealt round-robin within a
+  // column group)
+  for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts)
+  for (int G = 1; G <= 8; G *= 2) {
     if (K == 0 && !sh) continue;
     for (int Cf = 0; Cf <= 16; Cf = Cf ? Cf * 2 : 2) {
       SplitPlan p;
-      if (!plan_split_rows(R, K, H, sh, T, 152, 232448, 16, Cf, &p)) continue;
+      if (!plan_split_rows(R, K, H, sh, T, 152, 232448, 16, Cf, &p, G)) continue;
       ++checks;
       const auto& g = p.geo;
-      const int chunks = H / 8, nseg = (sh ? R : 0) + 1 + R * K, C = g.C;
+      const int chunks = H / 8, nseg = (sh ? R : 0) + 1 + R * K, C = g.C, Cs = g.Cs;
       bool bad = false;
       if (p.smem > 232448 || p.grid != T * C || p.threads > 544 || p.threads % 32) bad = true;
+      if (Cs < 2 || C != Cs * G || g.group_chunks * G < chunks || (G - 1) * g.group_chunks >= chunks) bad = true;
       const int consumers = p.threads - 32;
-      if ((long)consumers * p.cpt < chunks) bad = true;       // partial row fully covered
-      if (2 * g.tile_chunks > p.cpt * consumers) bad = true;  // <= CPT float4 items per thread
-      if (g.seg_stride < H * 2 || g.seg_stride % 128 || g.part_bytes < C * g.tile_chunks * 32) bad = true;
+      if ((long)consumers * p.cpt < g.group_chunks) bad = true;  // partial row of a group fully covered
+      if (2 * g.tile_chunks > p.cpt * consumers) bad = true;     // <= CPT float4 items per thread
+      if (g.seg_stride < g.group_chunks * 16 || g.seg_stride % 128 || g.part_bytes < Cs * g.tile_chunks * 32) bad = true;
+      if (g.row_f32_bytes < g.group_chunks * 32) bad = true;
+      long covered = 0;
       for (int c = 0; c < C; ++c) {
-        const int ns = (nseg - c + C - 1) / C;
-        if (ns < 1 || ns > 32) bad = true;
-        if (1024 + g.part_bytes + g.row_f32_bytes + (long)ns * g.seg_stride > p.smem) bad = true;
-        if (g.row_f32_bytes < chunks * 32) bad = true;
-        if ((long)ns * H * 2 >= (1 << 20)) bad = true;        // mbarrier transaction count
-        if (std::min(g.tile_chunks, chunks - c * g.tile_chunks) < 1) bad = true;
+        const int grp = c / Cs, cs = c % Cs;
+        const int g0 = grp * g.group_chunks, gchunks = std::min(g.group_chunks, chunks - g0);
+        const int ns = (nseg - cs + Cs - 1) / Cs;
+        if (gchunks < 1 || ns < 1 || ns > 32) bad = true;
+        if (1024 + g.part_bytes + std::max<long>(g.row_f32_bytes, (long)ns * g.seg_stride) > p.smem) bad = true;
+        if ((long)ns * gchunks * 16 >= (1 << 20)) bad = true;   // mbarrier transaction count
+        const int ntile = std::min(g.tile_chunks, gchunks - cs * g.tile_chunks);
+        if (ntile < 1) bad = true;                               // every CTA owns a tile
+        if ((long)Cs * ntile * 32 > g.part_bytes) bad = true;
+        covered += ntile;
       }
-      if (bad) { ++fails; if (fails < 20) printf("BAD split H=%d R=%d K=%d sh=%d T=%ld Cf=%d\n", H, R, K, sh, T, Cf); }
+      if (covered != chunks) bad = true;                         // tiles partition the row
+      if (bad) { ++fails; if (fails < 20) printf("BAD split H=%d R=%d K=%d sh=%d T=%ld Cf=%d G=%d\n", H, R, K, sh, T, Cf, G); }
     }
   }
   // show the automatic plans for the workloads

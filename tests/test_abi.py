@@ -380,6 +380,16 @@ def test_split_rows_setter(lib, ws):
             arf.ar_workspace_set_split_rows(ws, n)
 
 
+def test_split_column_groups_setter(lib, ws):
+    for n in (0, 1, 2, 4, 8):
+        arf.ar_workspace_set_split_column_groups(ws, n)
+        assert Fake().call(lib, ws) == arf.AR_VALIDATED
+    for n in (-1, 3, 6, 16):
+        with pytest.raises(arf.ArfuseError):
+            arf.ar_workspace_set_split_column_groups(ws, n)
+    arf.ar_workspace_set_split_column_groups(ws, 0)
+
+
 def test_pdl_flag_is_accepted(lib):
     w = arf.ar_workspace_create(R, K, H, TMAX, EPS, flags=arf.AR_WS_DRY_RUN | arf.AR_WS_PDL)
     try:

@@ -501,6 +501,57 @@ def test_every_split_cluster_size(cfg, T):
         ws.destroy()
 
 
+@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 4), ("glm_gemma", 3), ("prefill", 2), ("tiny", 4)])
+def test_split_column_groups(cfg, T):
+    """Split plans with column groups: C CTAs in G groups of C/G.  Every column
+    is summed exactly as by the C/G-CTA split without groups (the same
+    segments per CTA, the same slice order), so residual_out is bitwise
+    identical to it; out differs from it only through the order of the tile
+    sums of squares.  Oracle parity for every plan that fits."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        base = {}
+        arf.ar_workspace_set_split_column_groups(ws, 1)
+        for c in (2, 4, 8, 16):
+            arf.ar_workspace_set_cluster_size(ws, c)
+            try:
+                out, r_out = run_gpu(ws, d, fp32=True, regime=arf.AR_REGIME_SPLIT)
+            except arf.ArfuseError as e:
+                assert e.status == arf.AR_ERR_UNSUPPORTED
+                continue
+            torch.cuda.synchronize()
+            check_bf16(out, ref["out"], f"split {cfg} T={T} C={c} one group out")
+            check_f32(r_out, ref["h"], ref["abs"], f"split {cfg} T={T} C={c} one group residual_out")
+            base[c] = (out.clone(), r_out.clone())
+        ran = 0
+        for groups in (2, 4, 8):
+            arf.ar_workspace_set_split_column_groups(ws, groups)
+            for c in (4, 8, 16):
+                arf.ar_workspace_set_cluster_size(ws, c)
+                try:
+                    out, r_out = run_gpu(ws, d, fp32=True, regime=arf.AR_REGIME_SPLIT)
+                except arf.ArfuseError as e:
+                    assert e.status == arf.AR_ERR_UNSUPPORTED
+                    continue
+                torch.cuda.synchronize()
+                ran += 1
+                tag = f"split {cfg} T={T} C={c} groups={groups}"
+                assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_SPLIT, c), tag
+                check_bf16(out, ref["out"], tag + " out")
+                check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+                if c // groups in base:
+                    assert torch.equal(r_out, base[c // groups][1]), tag
+                    assert (out.float() - base[c // groups][0].float()).abs().max().item() < 0.05, tag
+        assert ran >= 2
+        arf.ar_workspace_set_split_column_groups(ws, 0)
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
+
+
 @pytest.mark.parametrize("cfg,T,split_c", [("glm_gemma", 8, 8), ("tiny", 4, 4)])
 def test_regime_table_routes_calls(cfg, T, split_c):
     """AR_REGIME_AUTO under a regime table runs the rule's regime and cluster

@@ -172,3 +172,22 @@ def test_light_rows_are_never_split():
         assert s.plan(192) == (arf.AR_REGIME_STREAM, 152)
     finally:
         s.ws.destroy()
+
+
+def test_split_column_groups_need_two_ctas_per_group(dsv3):
+    """Forced column groups must leave groups of at least two CTAs whose share
+    of the row's 73 segments fits the producer's 32 lanes; otherwise the
+    forced split regime has no plan."""
+    arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_SPLIT)
+    arf.ar_workspace_set_cluster_size(dsv3.ws, 16)
+    for groups in (0, 1, 2, 4):
+        arf.ar_workspace_set_split_column_groups(dsv3.ws, groups)
+        assert dsv3.plan(4) == (arf.AR_REGIME_SPLIT, 16)
+    arf.ar_workspace_set_split_column_groups(dsv3.ws, 8)    # 2 CTAs per group: 37 segments each
+    with pytest.raises(arf.ArfuseError) as e:
+        dsv3.plan(4)
+    assert e.value.status == arf.AR_ERR_UNSUPPORTED
+    arf.ar_workspace_set_cluster_size(dsv3.ws, 4)
+    arf.ar_workspace_set_split_column_groups(dsv3.ws, 4)    # one CTA per group
+    with pytest.raises(arf.ArfuseError):
+        dsv3.plan(1)

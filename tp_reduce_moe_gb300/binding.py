@@ -89,6 +89,8 @@ def load_library(path: str | None = None):
         lib.ar_workspace_set_split_rows.argtypes = [P, I]
         lib.ar_workspace_set_producer_warps.restype = I
         lib.ar_workspace_set_producer_warps.argtypes = [P, I]
+        lib.ar_workspace_set_split_column_groups.restype = I
+        lib.ar_workspace_set_split_column_groups.argtypes = [P, I]
         lib.ar_mhc_post.restype = I
         lib.ar_mhc_post.argtypes = [P, P, I, P, P, P, I64, I, I, P, P]
         lib.ar_workspace_set_regime_table.restype = I
@@ -212,6 +214,12 @@ def ar_workspace_set_split_rows(ws: Workspace, max_parts: int) -> None:
     wave (0 or 1: never split; default AR_MAX_SPLIT_PARTS)."""
     _check(load_library().ar_workspace_set_split_rows(ctypes.c_void_p(ws.handle), int(max_parts)),
            "ar_workspace_set_split_rows")
+
+
+def ar_workspace_set_split_column_groups(ws: Workspace, groups: int) -> None:
+    """Column groups per row of the split kernel (1, 2, 4, 8; tuning); 0 = automatic."""
+    _check(load_library().ar_workspace_set_split_column_groups(ctypes.c_void_p(ws.handle), int(groups)),
+           "ar_workspace_set_split_column_groups")
 
 
 def ar_workspace_set_producer_warps(ws: Workspace, warps: int) -> None:

@@ -36,6 +36,7 @@ struct ar_workspace {
     int force_ctas_per_row;  // 0: automatic
     int stage_bytes;         // 0: automatic
     int producer_warps;      // 0: automatic
+    int split_groups;        // column groups per row of the split kernel; 0: automatic
     int last_regime;
     int last_ctas;
     int table_n;  // rules in `table` (0: heuristic only)
@@ -69,27 +70,28 @@ Range range_of(const void* p, int64_t bytes) {
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
 // Regime tables measured on GB300 (tp_reduce_moe_gb300.tune: every regime and
-// cluster size, L2-cold, T = 1..256; ties within noise merged into the
-// neighbouring rule), installed for these shapes at create.
+// cluster size, L2-cold, T = 1..128, whole-row streaming beyond; ties within
+// noise merged into the neighbouring rule), installed for these shapes at
+// create.
 struct BuiltinTable {
     int R, K, H, n;
     ar_regime_rule rules[6];
 };
 const BuiltinTable kBuiltinTables[] = {
     // DeepSeek-V3 decode, TP8 (H = 7168, top-8)
-    {8, 8, 7168, 5,
-     {{4, AR_REGIME_SPLIT, 16}, {12, AR_REGIME_SPLIT, 8}, {32, AR_REGIME_CLUSTER, 8},
-      {64, AR_REGIME_CLUSTER, 4}, {256, AR_REGIME_STREAM, 0}}},
+    {8, 8, 7168, 4,
+     {{16, AR_REGIME_SPLIT, 16}, {24, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 4},
+      {256, AR_REGIME_STREAM, 0}}},
     // DeepSeek-V3 decode, TP4
-    {4, 8, 7168, 5,
-     {{4, AR_REGIME_SPLIT, 16}, {12, AR_REGIME_SPLIT, 8}, {16, AR_REGIME_CLUSTER, 8},
-      {64, AR_REGIME_CLUSTER, 4}, {256, AR_REGIME_STREAM, 0}}},
+    {4, 8, 7168, 4,
+     {{12, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_SPLIT, 8}, {64, AR_REGIME_CLUSTER, 4},
+      {256, AR_REGIME_STREAM, 0}}},
     // GLM-style decode, TP8 (H = 6144, top-8)
-    {8, 8, 6144, 5,
-     {{4, AR_REGIME_SPLIT, 16}, {12, AR_REGIME_SPLIT, 8}, {32, AR_REGIME_CLUSTER, 8},
-      {64, AR_REGIME_CLUSTER, 4}, {256, AR_REGIME_STREAM, 0}}},
+    {8, 8, 6144, 4,
+     {{16, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 4},
+      {256, AR_REGIME_STREAM, 0}}},
     // H = 8192, top-10, TP8 (from T = 48 whole rows, the last wave's rows split)
-    {8, 10, 8192, 3, {{4, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {256, AR_REGIME_STREAM, 0}}},
+    {8, 10, 8192, 3, {{12, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {256, AR_REGIME_STREAM, 0}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0)
     {2, 0, 7168, 2, {{96, AR_REGIME_ONESHOT, 0}, {256, AR_REGIME_STREAM, 0}}},
 };
@@ -129,6 +131,9 @@ struct Plans {
     arf::SplitPlan x{};
 };
 
+// Column groups of a split plan (0: the planner's choice).
+int split_groups(const ar_workspace* ws) { return ws->split_groups; }
+
 // Plan `regime` with `ctas` CTAs per row (0: the regime's own choice).
 // Returns the regime that will run (a streaming plan reports CLUSTER when its
 // rows are split over a cluster, STREAM otherwise), 0 when there is no plan.
@@ -143,7 +148,7 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
             // the given cluster size, else the largest that fits
             for (int c = ctas ? ctas : 16; c >= 2; c = ctas ? 0 : c >> 1)
                 if (arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                         ws->max_cluster_split, c, &p->x))
+                                         ws->max_cluster_split, c, &p->x, split_groups(ws)))
                     return AR_REGIME_SPLIT;
             return 0;
         case AR_REGIME_STREAM:
@@ -170,7 +175,7 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
 // The built-in choice (measured on GB300 with bench.py's sweep):
 //  - light rows (at most 8 summands per 16-byte chunk, one load wave per
 //    thread) below one row per two SMs: the one-shot kernel;
-//  - heavy rows at the smallest T (one cluster per row fits in half the
+//  - heavy rows at small T (one cluster per row in three quarters of the
 //    SMs): the split kernel, fewest bulk copies per CTA;
 //  - otherwise the streaming kernel (tiles over a cluster for small T, whole
 //    rows for large T).
@@ -180,7 +185,7 @@ int plan_heuristic(const ar_workspace* ws, int R, int K, int H, bool shared, int
         arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c))
         return AR_REGIME_ONESHOT;
     if (summands > 8 && arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                             ws->max_cluster_split, 0, &p->x))
+                                             ws->max_cluster_split, 0, &p->x, split_groups(ws)))
         return AR_REGIME_SPLIT;
     if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
                                ws->max_cluster_stream, 0, ws->stage_bytes, &p->s, ws->producer_warps,
@@ -613,6 +618,13 @@ ar_status ar_workspace_set_split_rows(ar_workspace* ws, int max_parts) {
     if (!ws) return AR_ERR_INVALID_ARG;
     if (max_parts < 0 || max_parts > arf::kMaxTailParts) return AR_ERR_INVALID_ARG;
     ws->max_tail_parts = max_parts;
+    return AR_OK;
+}
+
+ar_status ar_workspace_set_split_column_groups(ar_workspace* ws, int groups) {
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (groups < 0 || groups > 8 || (groups & (groups - 1))) return AR_ERR_INVALID_ARG;
+    ws->split_groups = groups;
     return AR_OK;
 }
 

@@ -399,10 +399,12 @@ int stream_rows_max_cluster(int threads, int smem, int cpt);
 
 // Geometry of one split_rows launch (kernel parameter).
 struct SplitGeom {
-    int C;            // CTAs per row (cluster size); CTA c copies segments c, c+C, ...
+    int C;            // CTAs per row (cluster size) = Cs * column groups
+    int Cs;           // CTAs per column group; CTA c = g*Cs + cs copies segments cs, cs+Cs, ...
+    int group_chunks;  // 16-byte chunks of a column group (the last group may be shorter)
     int seg_stride;   // bytes between segment buffers in shared memory
-    int part_bytes;   // bytes of the fp32 receive buffer (C slices of a column tile)
-    int row_f32_bytes;  // bytes of the CTA's own fp32 partial row
+    int part_bytes;   // bytes of the fp32 receive buffer (Cs slices of a column tile)
+    int row_f32_bytes;  // bytes of the CTA's fp32 partial row (over the segment buffers)
     int tile_chunks;  // 16-byte chunks of the column tile each CTA finishes
 };
 
@@ -415,9 +417,10 @@ struct SplitPlan {
 };
 
 // Plan a split_rows launch (one row per cluster); C = 0 picks the largest
-// cluster that fits.  Returns false if no plan fits.
+// cluster that fits; `groups` column groups per row (they must divide C; 0
+// picks the most that fit).  Returns false if no plan fits.
 bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
-                     int max_cluster, int C, SplitPlan* p);
+                     int max_cluster, int C, SplitPlan* p, int groups = 1);
 cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32,
                               cudaStream_t stream, bool pdl = false);
 cudaError_t split_rows_set_attributes(int smem_optin);

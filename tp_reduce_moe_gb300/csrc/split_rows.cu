@@ -1,35 +1,40 @@
 // split_rows.cu -- decode-latency kernel: one token row per thread-block
-// cluster, the row's segments dealt round-robin to the cluster's C CTAs.
+// cluster, the row's segments dealt round-robin over the cluster's CTAs.
 //
 // At decode sizes a row is nseg = R*(K+1)+1 segments of H bf16 (~1 MB) and
 // the TMA engine completes a bulk copy every ~50 ns whatever its size, so the
-// number of copies per CTA -- not the bytes -- sets the time.  Here CTA c of
-// the cluster copies only segments c, c+C, c+2C, ... (~nseg/C full-width rows,
-// all in flight at once), accumulates them into a full-width fp32 partial
-// row, and the cluster then reduce-scatters the partials through distributed
-// shared memory: every CTA sends slice j of its partial row to CTA j with one
-// bulk copy (shared -> peer shared, the TMA engine), completing on CTA j's
-// receive mbarrier; CTA c then sums its C received slices locally (fixed rank
-// order), which is h for column tile c.  The tile sums of squares go to
-// every peer as asynchronous remote stores (st.async) counted as transaction
-// bytes on the peer's barrier -- no release fence, so they do not wait for
-// the residual_out stores just issued; each CTA normalises and stores its
-// tile.
+// number of copies per CTA -- not the bytes -- sets the time.  The C CTAs of
+// the cluster form G column groups of Cs = C/G CTAs; group g covers 1/G of the
+// row's columns.  CTA cs of a group copies only segments cs, cs+Cs, ... of
+// its group's columns (~nseg/Cs copies, all in flight at once), accumulates
+// them into an fp32 partial row of the group's columns, and the group then
+// reduce-scatters the partials through distributed shared memory: every CTA
+// sends slice j of its partial row to CTA j of its group with one bulk copy
+// (shared -> peer shared, the TMA engine), completing on that CTA's receive
+// mbarrier; each CTA then sums its Cs received slices locally (fixed rank
+// order), which is h for its column tile.  The tile sums of squares go to
+// every CTA of the cluster as asynchronous remote stores (st.async) counted
+// as transaction bytes on the peer's barrier -- no release fence, so they do
+// not wait for the residual_out stores just issued; each CTA normalises and
+// stores its tile.  Groups cut the bytes through the cluster exchange G-fold
+// for G-fold more, smaller copies: measured at DeepSeek-V3 sizes (C = 16,
+// T = 1) 6.3 us with one group, 5.1 us with four.
 //
 //   producer warp: shared partials + residual copies go out at once (they
 //     need no routing metadata) on mbarrier 0; the routed copies follow as
 //     soon as perm arrives, on mbarrier 1; per-segment coefficients go into
 //     a shared-memory table published by the same barrier phases.
 //   consumers: fold the CTA's segments into registers, write the partial row
-//     locally, send its slices; wait for the C slices of this tile; local sums;
-//     push the tile's sum of squares; wait for the C sums; normalise; store.
+//     over the spent segment buffers, send its slices; wait for the Cs slices
+//     of this tile; local sums; push the tile's sum of squares; wait for the
+//     C sums; normalise; store.
 //
 // One cluster barrier (arrived on right after the mbarriers are initialised,
 // waited on just before the first send) keeps peers from signalling a
 // barrier that does not exist yet.  None is needed at exit: a CTA sends its
 // sum of squares only after it has received every slice, so once a CTA holds
-// all C sums, every copy that reads its partial row has landed and nothing
-// more will be written into it.  Every mbarrier wait is bounded
+// all C sums (its group peers' among them), every copy that reads its partial
+// row has landed and nothing more will be written into it.  Every mbarrier wait is bounded
 // (arf::mbar_wait_bounded); after one runs out, the CTA waits a bounded grace
 // period for copies in flight before it exits.
 //
@@ -37,6 +42,8 @@
 // wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
 // 1-2; sglang PR #37104 "perf(mtp): fuse trailing TP all-reduce with final
 // RMSNorm", Changes.
+#include <algorithm>
+
 #include "arf_common.cuh"
 
 namespace arf {
@@ -45,12 +52,14 @@ constexpr int kSplitMaxSegs = 32;       // segments per CTA (one producer lane e
 constexpr int kSplitMaxConsumers = 512;
 constexpr int kSplitMaxThreads = 32 + kSplitMaxConsumers;
 constexpr int kSplitHeader = 1024;      // barriers, coefficient table, partial sums, flags
+constexpr int kSplitMinGroupChunks = 128;  // automatic column groups: at least 2 KB per copy
 
 // Header layout (bytes): 0 bar[2] (segment loads), 16 rbar (slices received),
 // 24 ssbar (sums of squares received); 32 coef[32] f32; 160 red[32] f32;
 // 288 ss slots [16] f32 (one per source CTA); 352 abort flag; 1024 receive
-// buffer [C][tile_chunks*8] f32 (slice of every source CTA's partial row);
-// then the partial row [chunks*8] f32 and the segment buffers at seg_stride.
+// buffer [Cs][tile_chunks*8] f32 (slice of every source CTA's partial row);
+// then the segment buffers at seg_stride, which the partial row
+// [group_chunks*8] f32 reuses once the segments are folded in.
 template <int CPT, bool RES_F32>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     split_rows_kernel(const __grid_constant__ RowArgs a, const SplitGeom geo) {
@@ -64,27 +73,35 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     float* ss_slots = reinterpret_cast<float*>(smem + 288);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 352);
     float* recv = reinterpret_cast<float*>(smem + kSplitHeader);
-    float* part = reinterpret_cast<float*>(smem + kSplitHeader + geo.part_bytes);
-    uint8_t* segbuf = smem + kSplitHeader + geo.part_bytes + geo.row_f32_bytes;
+    uint8_t* segbuf = smem + kSplitHeader + geo.part_bytes;
+    // the CTA's fp32 partial row reuses the segment buffers once every
+    // consumer is done with them
+    float* part = reinterpret_cast<float*>(segbuf);
 
     const int C = geo.C;
+    const int Cs = geo.Cs;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int ncw = (blockDim.x >> 5) - 1;
     const uint32_t c = cluster_ctarank();
+    const int grp = (int)c / Cs;        // column group of this CTA
+    const int cs = (int)c - grp * Cs;   // rank within the group
     const int64_t t = blockIdx.x / C;
     const int H = a.H;
-    const int chunks = H / 8;
-    const uint32_t row_bytes = (uint32_t)H * 2u;
+    // this CTA's column group: chunks [g0, g0 + chunks) of the row
+    const int g0 = grp * geo.group_chunks;
+    const int chunks = min(geo.group_chunks, H / 8 - g0);
+    const int64_t col0 = (int64_t)g0 * 8;           // first element of the group
+    const uint32_t row_bytes = (uint32_t)chunks * 16u;  // bytes of a segment's group
     const int nS = a.has_shared ? a.R : 0;
     const int nsr = nS + 1;                          // shared partials + residual
     const int nseg = nsr + a.R * a.K;
-    // Segments of this CTA: s = c + i*C, i < ns; the first nsr_c need no perm.
-    const int ns = (nseg - (int)c + C - 1) / C;
-    const int nsr_c = (nsr > (int)c) ? (nsr - 1 - (int)c) / C + 1 : 0;
+    // Segments of this CTA: s = cs + i*Cs, i < ns; the first nsr_c need no perm.
+    const int ns = (nseg - cs + Cs - 1) / Cs;
+    const int nsr_c = (nsr > cs) ? (nsr - 1 - cs) / Cs + 1 : 0;
 
     const int tile = geo.tile_chunks;
-    const int ntile_c = min(tile, chunks - (int)c * tile);  // chunks of this CTA's tile
+    const int ntile_c = min(tile, chunks - cs * tile);  // chunks of this CTA's tile
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&bar[0]), 1);
         mbar_init(smem_addr(&bar[1]), 1);
@@ -92,9 +109,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         mbar_init(smem_addr(ssbar), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        // every source CTA sends this tile's slice of its partial row, and its
-        // tile's sum of squares (4 bytes)
-        mbar_arrive_expect_tx(smem_addr(rbar), (uint32_t)(C * ntile_c * 32));
+        // every CTA of the group sends this tile's slice of its partial row,
+        // and every CTA of the cluster its tile's sum of squares (4 bytes)
+        mbar_arrive_expect_tx(smem_addr(rbar), (uint32_t)(Cs * ntile_c * 32));
         mbar_arrive_expect_tx(smem_addr(ssbar), (uint32_t)C * 4u);
     }
     __syncthreads();
@@ -106,7 +123,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         // ------------------------------------------------------------ producer
         const uint64_t pol = l2_evict_first_policy();
         const int i = lane;
-        const int s = (int)c + i * C;
+        const int s = cs + i * Cs;
         const bool mine = i < ns;
         const bool is_sr = mine && i < nsr_c;
         const uint32_t dst = smem_addr(segbuf + (size_t)i * geo.seg_stride);
@@ -120,7 +137,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             wv = __ldg(a.w + t * a.K + lane);
         }
         if (is_sr) {
-            const uint16_t* src = s < nS ? a.S[s] + t * H : a.residual + t * H;
+            const uint16_t* src = (s < nS ? a.S[s] + t * H : a.residual + t * H) + col0;
             bulk_g2s(dst, src, row_bytes, smem_addr(&bar[0]), pol);
         }
         // 2. routed copies
@@ -130,7 +147,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         const int64_t row_k = __shfl_sync(0xffffffffu, rowv, k);
         const float w_k = __shfl_sync(0xffffffffu, wv, k);
         if (mine && !is_sr)
-            bulk_g2s(dst, a.E[e % a.R] + row_k * H, row_bytes, smem_addr(&bar[1]), pol);
+            bulk_g2s(dst, a.E[e % a.R] + row_k * H + col0, row_bytes, smem_addr(&bar[1]), pol);
         // 3. coefficients, then arm both barriers (a phase needs lane 0's
         //    arrival as well as the bytes, so it cannot complete early)
         if (mine) coef[i] = is_sr ? (s < nS ? shared_coef(a, t) : 1.0f) : w_k;
@@ -183,7 +200,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                     }
             }
         }
-        // The partial row, locally; made visible to the bulk-copy engine.
+        // The partial row, locally (over the spent segment buffers); made
+        // visible to the bulk-copy engine.
+        named_barrier_sync(1, nct);
 #pragma unroll
         for (int m = 0; m < CPT; ++m) {
             const int ch = ci + m * nct;
@@ -200,20 +219,22 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     // ---- barrier A, wait: every peer's receive barrier exists
     __syncwarp();
     cluster_wait_acquire();
-    // send slice j of the partial row to CTA j (one bulk copy each)
-    if (warp == 1 && lane < C) {
+    // send slice j of the group's partial row to CTA j of the group (one
+    // bulk copy each)
+    if (warp == 1 && lane < Cs) {
         const int j = lane;
         const int nj = min(tile, chunks - j * tile);
-        bulk_s2cluster(map_shared_rank(smem_addr(recv + ((size_t)c * tile) * 8), (uint32_t)j),
+        const uint32_t peer = (uint32_t)(grp * Cs + j);
+        bulk_s2cluster(map_shared_rank(smem_addr(recv + ((size_t)cs * tile) * 8), peer),
                        smem_addr(part + (size_t)j * tile * 8), (uint32_t)nj * 32u,
-                       map_shared_rank(smem_addr(rbar), (uint32_t)j));
+                       map_shared_rank(smem_addr(rbar), peer));
     }
 
     // ---- this CTA's column tile: the C received slices summed locally, in
     // rank order.  Work item q = one float4 (half a 16-byte bf16 chunk); a
     // consumer thread owns items ci + m*nct (m < CPT, enough since a tile is
     // at most half the row).
-    const int tile0 = (int)c * tile;
+    const int tile0 = g0 + cs * tile;  // first chunk of this CTA's tile in the row
     const int ntile = ntile_c;
     const int ci = threadIdx.x - 32;
     const int nct = ncw * 32;
@@ -237,7 +258,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         if (!hv[m]) continue;
         gpre[m] = __ldg(reinterpret_cast<const uint2*>(a.gamma + (int64_t)tile0 * 8 + (int64_t)q * 4));
         const float* src = recv + (size_t)q * 4;
-        for (int r = 0; r < C; ++r) {
+        for (int r = 0; r < Cs; ++r) {
             const float4 x = *reinterpret_cast<const float4*>(src + r * slice);
             hq[m].x += x.x;
             hq[m].y += x.y;
@@ -311,51 +332,72 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 static int ceil_div_s(int a, int b) { return (a + b - 1) / b; }
 
 bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
-                     int max_cluster, int C, SplitPlan* p) {
+                     int max_cluster, int C, SplitPlan* p, int groups) {
     const int chunks = H / 8;
     const int nseg = (shared ? R : 0) + 1 + R * K;
-    if (chunks < 2 || T < 1) return false;
-    const int seg_stride = ceil_div_s(H * 2, 128) * 128;
-    auto recv_bytes = [&](int c) { return ceil_div_s(c * ceil_div_s(chunks, c) * 32, 128) * 128; };
-    const int row_f32 = ceil_div_s(chunks * 32, 128) * 128;
-    auto fits = [&](int c) {
-        if (c < 2 || c > 16 || c > max_cluster || c > nseg) return false;
-        const int ns = ceil_div_s(nseg, c);
-        if (ns > kSplitMaxSegs) return false;
-        const int tile = ceil_div_s(chunks, c);
-        if ((c - 1) * tile >= chunks) return false;
-        int cpt_c = 1;
-        while (cpt_c < 4 && chunks > cpt_c * kSplitMaxConsumers) cpt_c <<= 1;
-        const int consumers_c = ceil_div_s(ceil_div_s(chunks, cpt_c), 32) * 32;
-        if (2 * tile > cpt_c * consumers_c) return false;  // <= CPT items per thread
-        return kSplitHeader + recv_bytes(c) + row_f32 + ns * seg_stride <= smem_optin;
-    };
-    if (C <= 0) {
-        // Automatic: the largest cluster that fits with at most one CTA per
-        // two SMs over all rows (measured: beyond that the tiled streaming
-        // kernel is faster); no plan otherwise.
-        C = 0;
-        for (int c = 16; c >= 2; c >>= 1)
-            if (fits(c) && (int64_t)c * T * 2 <= num_sms) {
-                C = c;
-                break;
-            }
-        if (!C) return false;
+    if (chunks < 2 || T < 1 || groups < 0) return false;
+    if (groups == 0) {
+        // Automatic: the most column groups (of at least kSplitMinGroupChunks
+        // chunks) that leave a plan -- fewer bytes through the cluster
+        // exchange; measured at DeepSeek-V3 and GLM sizes, four groups of a
+        // 16-CTA cluster beat one group by 1.1 us at T = 1.
+        for (int g = 8; g > 1; g >>= 1)
+            if (ceil_div_s(chunks, g) >= kSplitMinGroupChunks &&
+                plan_split_rows(R, K, H, shared, T, num_sms, smem_optin, max_cluster, C, p, g))
+                return true;
+        groups = 1;
     }
-    if (!fits(C)) return false;
-    int cpt = 1;
-    while (cpt < 4 && chunks > cpt * kSplitMaxConsumers) cpt <<= 1;
-    if (chunks > cpt * kSplitMaxConsumers) return false;
-    const int consumers = ceil_div_s(ceil_div_s(chunks, cpt), 32) * 32;
-    p->geo.C = C;
-    p->geo.seg_stride = seg_stride;
-    p->geo.part_bytes = recv_bytes(C);
-    p->geo.row_f32_bytes = row_f32;
-    p->geo.tile_chunks = ceil_div_s(chunks, C);
-    p->cpt = cpt;
-    p->threads = 32 + consumers;
-    p->smem = kSplitHeader + recv_bytes(C) + row_f32 + ceil_div_s(nseg, C) * seg_stride;
-    p->grid = (int)(T * C);
+    // Column groups of gch chunks (the last one may be shorter); Cs = C /
+    // groups CTAs per group deal the row's segments and reduce-scatter the
+    // group's columns.
+    const int gch = ceil_div_s(chunks, groups);
+    const int last = chunks - (groups - 1) * gch;
+    auto make = [&](int c, SplitPlan* q) {
+        if (c < 2 || c > 16 || c > max_cluster || c % groups || last < 1) return false;
+        const int cs = c / groups;
+        if (cs < 2 || cs > nseg) return false;
+        const int ns = ceil_div_s(nseg, cs);
+        if (ns > kSplitMaxSegs) return false;
+        const int tile = ceil_div_s(gch, cs);
+        if ((cs - 1) * tile >= last) return false;  // every CTA owns a tile, the shortest group too
+        int cpt = 1;
+        while (cpt < 4 && gch > cpt * kSplitMaxConsumers) cpt <<= 1;
+        if (gch > cpt * kSplitMaxConsumers) return false;
+        const int consumers = ceil_div_s(ceil_div_s(gch, cpt), 32) * 32;
+        if (2 * tile > cpt * consumers) return false;  // <= CPT items per thread
+        const int seg_stride = ceil_div_s(gch * 16, 128) * 128;
+        const int recv = ceil_div_s(cs * tile * 32, 128) * 128;
+        const int row_f32 = ceil_div_s(gch * 32, 128) * 128;
+        const int smem = kSplitHeader + recv + std::max(row_f32, ns * seg_stride);
+        if (smem > smem_optin) return false;
+        q->geo.C = c;
+        q->geo.Cs = cs;
+        q->geo.group_chunks = gch;
+        q->geo.seg_stride = seg_stride;
+        q->geo.part_bytes = recv;
+        q->geo.row_f32_bytes = row_f32;
+        q->geo.tile_chunks = tile;
+        q->cpt = cpt;
+        q->threads = 32 + consumers;
+        q->smem = smem;
+        q->grid = (int)(T * c);
+        return true;
+    };
+    SplitPlan q{};
+    if (C <= 0) {
+        // Automatic: the largest cluster that fits with its CTAs over all
+        // rows on at most three quarters of the SMs (measured: beyond that
+        // clusters stop being co-resident and the tiled streaming kernel is
+        // faster); no plan otherwise.
+        for (int c = 16; c >= 2; c >>= 1)
+            if ((int64_t)c * T * 4 <= (int64_t)num_sms * 3 && make(c, &q)) {
+                *p = q;
+                return true;
+            }
+        return false;
+    }
+    if (!make(C, &q)) return false;
+    *p = q;
     return true;
 }
 
