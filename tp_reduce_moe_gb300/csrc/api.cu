@@ -80,7 +80,7 @@ struct BuiltinTable {
 const BuiltinTable kBuiltinTables[] = {
     // DeepSeek-V3 decode, TP8 (H = 7168, top-8)
     {8, 8, 7168, 4,
-     {{16, AR_REGIME_SPLIT, 16}, {24, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 4},
+     {{16, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 4},
       {256, AR_REGIME_STREAM, 0}}},
     // DeepSeek-V3 decode, TP4
     {4, 8, 7168, 4,
