@@ -552,6 +552,53 @@ def test_split_column_groups(cfg, T):
         ws.destroy()
 
 
+SPLIT_EDGE = [
+    # (R, K, H, T, shared): column groups of unequal width
+    (3, 5, 264, 3, True),       # 33 chunks: groups of 17 + 16, 9 + 9 + 9 + 6, ...
+    (2, 3, 2056, 5, True),      # 257 chunks: eight groups of 33, the last of 26
+    (4, 2, 12296, 2, True),     # 1537 chunks: four groups of 385, the last of 382
+    (1, 6, 1032, 4, False),     # 129 chunks, no shared partials
+]
+
+
+@pytest.mark.parametrize("R,K,H,T,shared", SPLIT_EDGE,
+                         ids=[f"R{a}K{b}H{c}T{d}S{int(e)}" for a, b, c, d, e in SPLIT_EDGE])
+def test_split_column_groups_ragged(R, K, H, T, shared):
+    """Forced column groups on widths that do not divide evenly: oracle parity
+    for every (cluster size, groups) with a plan, both residual_out types."""
+    from gen import Config
+    cfg = Config("split_edge", 98, R=R, K=K, H=H, Ts=(T,), eps=1e-6, weights="softmax",
+                 has_shared=shared)
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp, max_tokens=T)
+    ran = 0
+    try:
+        d = to_dev(inp)
+        for groups in (2, 4, 8):
+            arf.ar_workspace_set_split_column_groups(ws, groups)
+            for c in (4, 8, 16):
+                arf.ar_workspace_set_cluster_size(ws, c)
+                for fp32 in (False, True):
+                    try:
+                        out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_SPLIT)
+                    except arf.ArfuseError as e:
+                        assert e.status == arf.AR_ERR_UNSUPPORTED
+                        continue
+                    torch.cuda.synchronize()
+                    ran += 1
+                    tag = f"split edge R={R} K={K} H={H} T={T} C={c} groups={groups} fp32={fp32}"
+                    check_bf16(out, ref["out"], tag + " out")
+                    if fp32:
+                        check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+                    else:
+                        check_bf16(r_out, ref["h"], tag + " residual_out")
+        assert ran >= 4
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
+
+
 @pytest.mark.parametrize("cfg,T,split_c", [("glm_gemma", 8, 8), ("tiny", 4, 4)])
 def test_regime_table_routes_calls(cfg, T, split_c):
     """AR_REGIME_AUTO under a regime table runs the rule's regime and cluster
