@@ -316,8 +316,10 @@ ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
  * 2..16.  A call past the last rule, or one whose rule has no launch plan for
  * it (a cluster size the device cannot co-schedule, a row too long for the
  * split kernel), runs the heuristic.  A regime forced with
- * ar_workspace_set_regime takes precedence over the table.  Results are
- * identical under every table.
+ * ar_workspace_set_regime takes precedence over the table.  Every regime
+ * meets the same accuracy bound; each sums in its own fixed order, so a
+ * table changes results only within rounding, and a given table gives the
+ * same bits on every call.
  *
  * ar_workspace_create installs a table measured on GB300 when (ranks, top_k,
  * hidden) is one of the shapes the library carries one for, else none.

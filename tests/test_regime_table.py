@@ -3,8 +3,8 @@
 A dry-run workspace plans every call and records the regime it would launch
 (ar_workspace_last_regime) without touching a device, so the table's lookup,
 its precedence rules and its fallback to the heuristic can be checked here;
-results under every table are identical, which the GPU parity tests check
-for each regime.
+every regime meets the oracle tolerances, which the GPU parity tests check
+for each regime and for calls routed by a table.
 """
 import pytest
 
