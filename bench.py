@@ -4,7 +4,7 @@
 One step = one call of the whole fused path (routed gather-sum, shared add,
 rank sum, residual add, RMSNorm) on one batch of synthetic input.  The
 headline workload is the bandwidth-bound prefill shape: R = 8 rank partials,
-K = 10 routed experts per token, H = 8192, T = 8192 tokens per GPU (12.3 GB of
+K = 10 routed experts per token, H = 8192, T = 8192 tokens per GPU (12.2 GB of
 algorithmic traffic per call, far larger than the 129 MB L2, so no flush is
 needed between calls).  Inputs are drawn on the device with a seeded
 generator (gen.make_inputs); nothing is read from disk.

@@ -501,7 +501,8 @@ def test_every_split_cluster_size(cfg, T):
         ws.destroy()
 
 
-@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 4), ("glm_gemma", 3), ("prefill", 2), ("tiny", 4)])
+@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 4), ("glm_gemma", 3), ("prefill", 2), ("tiny", 4),
+                                   ("dsv3_decode", 48)])
 def test_split_column_groups(cfg, T):
     """Split plans with column groups: C CTAs in G groups of C/G.  Every column
     is summed exactly as by the C/G-CTA split without groups (the same
