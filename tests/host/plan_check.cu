@@ -7,6 +7,7 @@
 // mbarrier transaction count.  The automatic plan must exist for every shape.
 #include "stream_rows.cu"
 #include "split_rows.cu"
+#include "cluster_rows.cu"
 #include <cstdio>
 #include <cstdlib>
 using namespace arf;
@@ -113,6 +114,21 @@ int main() {
       if (covered != chunks) bad = true;                         // tiles partition the row
       if (bad) { ++fails; if (fails < 20) printf("BAD split H=%d R=%d K=%d sh=%d T=%ld Cf=%d G=%d\n", H, R, K, sh, T, Cf, G); }
     }
+  }
+  // one-shot plans (one cluster per row, every load of a thread in flight)
+  for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts)
+  for (int mc = 1; mc <= 16; mc *= 2) {
+    if (K == 0 && !sh) continue;
+    ClusterPlan p;
+    if (!plan_cluster_rows(R, K, H, sh, mc, T, 152, &p)) continue;
+    ++checks;
+    const int chunks = H / 8, NT = (sh ? R : 0) + R * K;
+    bool bad = false;
+    if (p.C < 1 || p.C > mc || p.threads != p.nch * p.G || p.threads > 768) bad = true;
+    if ((long)p.nch * p.C < chunks || p.nch > chunks) bad = true;                // every chunk has a CTA
+    if ((long)p.G * p.maxt < NT || (p.maxt != 2 && p.maxt != 8)) bad = true;     // every term has a load slot
+    if (p.smem != (p.G - 1) * 2 * p.nch * 16) bad = true;
+    if (bad) { ++fails; if (fails < 20) printf("BAD oneshot H=%d R=%d K=%d sh=%d T=%ld mc=%d\n", H, R, K, sh, T, mc); }
   }
   // show the automatic plans for the workloads
   struct W { const char* n; int R, K, H; bool sh; long T[8]; } ws[] = {

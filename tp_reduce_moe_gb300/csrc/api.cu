@@ -93,7 +93,7 @@ const BuiltinTable kBuiltinTables[] = {
     // H = 8192, top-10, TP8 (from T = 48 whole rows, the last wave's rows split)
     {8, 10, 8192, 3, {{12, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {256, AR_REGIME_STREAM, 0}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0)
-    {2, 0, 7168, 2, {{96, AR_REGIME_ONESHOT, 0}, {256, AR_REGIME_STREAM, 0}}},
+    {2, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0}}},
 };
 
 bool valid_regime(int r) {
@@ -174,15 +174,17 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
 
 // The built-in choice (measured on GB300 with bench.py's sweep):
 //  - light rows (at most 8 summands per 16-byte chunk, one load wave per
-//    thread) below one row per two SMs: the one-shot kernel;
+//    thread) below one row per two SMs, and rows of at most 2 summands (the
+//    40-register variant) up to 1.5 rows per SM: the one-shot kernel;
 //  - heavy rows at small T (one cluster per row in three quarters of the
 //    SMs): the split kernel, fewest bulk copies per CTA;
 //  - otherwise the streaming kernel (tiles over a cluster for small T, whole
 //    rows for large T).
 int plan_heuristic(const ar_workspace* ws, int R, int K, int H, bool shared, int64_t T, Plans* p) {
     const int summands = (shared ? R : 0) + R * K;
-    if (summands <= 8 && 2 * T < ws->num_sms &&
-        arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c))
+    const bool light = (summands <= 8 && 2 * T < ws->num_sms) ||
+                       (summands <= 2 && 2 * T <= 3 * (int64_t)ws->num_sms);
+    if (light && arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c))
         return AR_REGIME_ONESHOT;
     if (summands > 8 && arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
                                              ws->max_cluster_split, 0, &p->x, split_groups(ws)))

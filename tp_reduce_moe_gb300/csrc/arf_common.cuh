@@ -330,6 +330,7 @@ struct ClusterPlan {
     int G;    // thread groups splitting the term list
     int threads;
     int smem;  // dynamic shared memory bytes
+    int maxt;  // loads per thread the kernel instantiation holds (2, 4 or 8)
 };
 
 // Kernel plan for the small-T regime; returns false if (R, K, H, shared) has

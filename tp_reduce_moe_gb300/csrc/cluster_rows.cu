@@ -27,8 +27,8 @@ constexpr int kClusterMaxThreads = 768;
 // row may be ragged).  blockDim.x = nch * G.  Term q of a thread group:
 // q < nS is shared partial S_q; otherwise e = q - nS selects slot k = e / R
 // of rank r = e % R.
-template <bool RES_F32>
-__global__ void __launch_bounds__(kClusterMaxThreads, 1)
+template <bool RES_F32, int MAXT>
+__global__ void __launch_bounds__(kClusterMaxThreads, MAXT <= 2 ? 2 : 1)
     cluster_rows_kernel(const __grid_constant__ RowArgs a, int C, int nch, int G) {
     extern __shared__ __align__(16) uint8_t dyn_smem[];
     pdl_trigger();
@@ -76,11 +76,11 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
     }
 
     // Pass 1: loads that do not depend on the routing metadata.
-    uint4 v[kClusterMaxTerms];
-    float coef[kClusterMaxTerms];
+    uint4 v[MAXT];
+    float coef[MAXT];
     const float s_coef = shared_coef(a, t);
 #pragma unroll
-    for (int m = 0; m < kClusterMaxTerms; ++m) {
+    for (int m = 0; m < MAXT; ++m) {
         const int q = g + m * G;
         if (q < nS && q < NT) {
             v[m] = ld_stream16(a.S[q] + rowoff);
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
 
     // Pass 2: the routed (gathered) expert rows.
 #pragma unroll
-    for (int m = 0; m < kClusterMaxTerms; ++m) {
+    for (int m = 0; m < MAXT; ++m) {
         const int q = g + m * G;
         if (q >= nS && q < NT) {
             const int e = q - nS;
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
 #pragma unroll
-    for (int m = 0; m < kClusterMaxTerms; ++m) {
+    for (int m = 0; m < MAXT; ++m) {
         if (g + m * G < NT) {
             float f[8];
             bf16x8_to_f32(v[m], f);
@@ -192,21 +192,21 @@ __global__ void __launch_bounds__(kClusterMaxThreads, 1)
     if (C > 1 && tid == 0 && s_abort) grace_period(1000000ull);
 }
 
-static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+static int ceil_div_c(int a, int b) { return (a + b - 1) / b; }
 
 bool plan_cluster_rows(int R, int K, int H, bool shared, int max_c, int64_t T, int num_sms,
                        ClusterPlan* p) {
     const int chunks = H / 8;
     const int NT = (shared ? R : 0) + R * K;
     if (NT < 1 || chunks < 1) return false;
-    const int G = ceil_div(NT, kClusterMaxTerms);
+    const int G = ceil_div_c(NT, kClusterMaxTerms);
     if (G > kClusterMaxThreads) return false;
     // Enough CTAs to cover the GPU about twice over.
     int want = 1;
     while (want < 16 && (int64_t)want * T < 2LL * num_sms) want <<= 1;
     int best = 0, largest = 0;
     for (int C = 1; C <= 16 && C <= max_c && C <= chunks; C <<= 1) {
-        const int nch = ceil_div(chunks, C);
+        const int nch = ceil_div_c(chunks, C);
         if (nch * G > kClusterMaxThreads) continue;
         largest = C;
         if (!best && C >= want) best = C;
@@ -214,21 +214,36 @@ bool plan_cluster_rows(int R, int K, int H, bool shared, int max_c, int64_t T, i
     if (!best) best = largest;
     if (!best) return false;
     p->C = best;
-    p->nch = ceil_div(chunks, best);
+    p->nch = ceil_div_c(chunks, best);
     p->G = G;
+    // loads per thread, rounded up to an instantiated bound: at most two
+    // (light rows, e.g. the K = 0 all-reduce of two partials) fits 40
+    // registers, so twice the CTAs are resident per SM
+    const int terms = ceil_div_c(NT, G);
+    p->maxt = terms <= 2 ? 2 : kClusterMaxTerms;
     p->threads = p->nch * G;
     p->smem = (G - 1) * 2 * p->nch * (int)sizeof(float4);
     return true;
 }
 
+// The kernel instantiation for (residual_out type, loads per thread).
+static const void* cluster_kernel_for(bool res_f32, int maxt) {
+    if (maxt == 2) return res_f32 ? reinterpret_cast<const void*>(cluster_rows_kernel<true, 2>)
+                                  : reinterpret_cast<const void*>(cluster_rows_kernel<false, 2>);
+    if (maxt == kClusterMaxTerms)
+        return res_f32 ? reinterpret_cast<const void*>(cluster_rows_kernel<true, kClusterMaxTerms>)
+                       : reinterpret_cast<const void*>(cluster_rows_kernel<false, kClusterMaxTerms>);
+    return nullptr;
+}
+
 cudaError_t cluster_rows_set_attributes() {
-    cudaError_t e;
-    e = cudaFuncSetAttribute(cluster_rows_kernel<false>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(cluster_rows_kernel<true>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    return e;
+    for (int f = 0; f < 2; ++f)
+        for (int maxt : {2, kClusterMaxTerms}) {
+            cudaError_t e = cudaFuncSetAttribute(cluster_kernel_for(f != 0, maxt),
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+    return cudaSuccess;
 }
 
 static cudaLaunchConfig_t cluster_config(const ClusterPlan& p, int64_t T, cudaStream_t s,
@@ -252,12 +267,10 @@ static cudaLaunchConfig_t cluster_config(const ClusterPlan& p, int64_t T, cudaSt
 int cluster_rows_max_cluster(int threads, int smem, bool res_f32) {
     for (int C = 16; C >= 1; C >>= 1) {
         cudaLaunchAttribute attr[1];
-        ClusterPlan p{C, 1, 1, threads, smem};
+        ClusterPlan p{C, 1, 1, threads, smem, kClusterMaxTerms};
         cudaLaunchConfig_t cfg = cluster_config(p, 1, nullptr, attr);
         int n = 0;
-        cudaError_t e = res_f32
-                            ? cudaOccupancyMaxActiveClusters(&n, cluster_rows_kernel<true>, &cfg)
-                            : cudaOccupancyMaxActiveClusters(&n, cluster_rows_kernel<false>, &cfg);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, cluster_kernel_for(res_f32, kClusterMaxTerms), &cfg);
         if (e == cudaSuccess && n > 0) return C;
         (void)cudaGetLastError();
     }
@@ -273,9 +286,11 @@ cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res
         attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
         ++cfg.numAttrs;
     }
-    if (res_f32)
-        return cudaLaunchKernelEx(&cfg, cluster_rows_kernel<true>, a, p.C, p.nch, p.G);
-    return cudaLaunchKernelEx(&cfg, cluster_rows_kernel<false>, a, p.C, p.nch, p.G);
+    const void* k = cluster_kernel_for(res_f32, p.maxt);
+    if (!k) return cudaErrorInvalidValue;
+    int C = p.C, nch = p.nch, G = p.G;
+    void* args[] = {const_cast<RowArgs*>(&a), &C, &nch, &G};
+    return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 }  // namespace arf
