@@ -8,7 +8,10 @@
 // column chunk are split over G thread groups, each thread issuing all of
 // its (<= 8) 16-byte loads at once.  Group partials meet in shared memory,
 // the row's sum of squares meets across the cluster in distributed shared
-// memory, and every CTA normalises and stores its own columns.
+// memory, and every CTA normalises and stores its own columns.  Rows of at
+// most two loads per thread (the all-reduce of two partials) run an
+// instantiation capped at 40 registers, twice the resident CTAs of the
+// generic one (80): at T = 128 a call takes 4.8 us instead of 7.1.
 //
 // Operation: sglang PR #37196 "[Comm] Share the CuTe DSL AR fusion core and
 // wire it for DeepSeek-V3 / GLM-5.x", Motivation and Modifications sections
