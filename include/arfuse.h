@@ -99,8 +99,9 @@ typedef enum ar_status {
 #define AR_REGIME_ONESHOT 3  /* one cluster per row, every load in flight at once from    */
                              /* registers, no pipeline (latency-optimal for tiny rows)    */
 #define AR_REGIME_SPLIT 4    /* small T: one cluster per row, the row's segments dealt    */
-                             /* to its C CTAs, partial rows reduce-scattered through      */
-                             /* distributed shared memory (fewest copies per CTA)         */
+                             /* to its C CTAs (in column groups), partial rows            */
+                             /* reduce-scattered through distributed shared memory        */
+                             /* (fewest copies per CTA)                                   */
 
 typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
 
