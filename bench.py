@@ -58,6 +58,7 @@ def parse_regime(tok: str):
         return REGIMES["split"], int(tok[1:])
     return REGIMES[tok], 0
 CPU_SAMPLE_T = 512
+WARM_CALLS = 64  # calls per graph in the L2-warm sweep (all on the one input set)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "stream_rows_prefill_traffic.json")
 
 
@@ -93,6 +94,9 @@ def parse():
                    help="headline and e2e workspaces launch with programmatic dependent launch")
     p.add_argument("--sweep-pdl", choices=["off", "on", "both"], default="both",
                    help="sweep points without / with programmatic dependent launch (AR_WS_PDL)")
+    p.add_argument("--sweep-perm", choices=["random", "expert_sorted"], default="random",
+                   help="routing permutation of the sweep's inputs: a random permutation of the "
+                        "expert rows, or the expert-sorted order a real MoE dispatch produces")
     p.add_argument("--sweep-mode", choices=["rotate", "scatter", "warm"], default="rotate",
                    help="rotate: L2-cold, each call gathers within its own expert block; "
                         "scatter: L2-cold, gathers spread over all sets' rows; "
@@ -400,7 +404,8 @@ def main_ours(args):
         sweep = run_sweep(arf, torch, dev, stream, peak, args.sweep_regimes.split(","),
                           [w for w in args.sweep_only.split(",") if w], args.sweep_mode,
                           gated=args.gated,
-                          pdls={"off": (False,), "on": (True,), "both": (False, True)}[args.sweep_pdl])
+                          pdls={"off": (False,), "on": (True,), "both": (False, True)}[args.sweep_pdl],
+                          perm_kind=args.sweep_perm)
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
@@ -498,7 +503,7 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
 
 
 def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate",
-              gated=False, pdls=(False,)):
+              gated=False, pdls=(False,), perm_kind="random"):
     """µs/call vs T for every workload: L2-cold by rotating through disjoint
     input sets (>= 3x L2 in total; each set gathers only within its own block
     of expert rows, like successive layers), timed by replaying a CUDA graph
@@ -517,7 +522,7 @@ def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="r
                 for pdl in pdls:
                     res.append(sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T,
                                            *parse_regime(regime_name), mode=mode,
-                                           gated=gated and cfg.K > 0, pdl=pdl))
+                                           gated=gated and cfg.K > 0, pdl=pdl, perm_kind=perm_kind))
     from gen import MHC_SHAPES
     for name, shp in MHC_SHAPES.items():
         if only and name not in only and "mhc" not in only:
@@ -547,14 +552,17 @@ def sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode="rotat
     for i in range(min(n_sets, 4)):
         call(i)
     torch.cuda.synchronize()
+    # warm: the one input set called WARM_CALLS times per graph (a graph of
+    # one call would time the graph launch, not the call)
+    calls = WARM_CALLS if mode == "warm" else n_sets
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for i in range(n_sets):
-            call(i)
+        for i in range(calls):
+            call(i % n_sets)
     g.replay()
     torch.cuda.synchronize()
     per = []
-    reps = 200 if mode == "warm" else 1
+    reps = 4 if mode == "warm" else 1
     for _ in range(3):
         a = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
@@ -563,7 +571,7 @@ def sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode="rotat
             g.replay()
         e.record(stream)
         torch.cuda.synchronize()
-        per.append(a.elapsed_time(e) * 1e3 / (n_sets * reps))
+        per.append(a.elapsed_time(e) * 1e3 / (calls * reps))
     us = statistics.median(per)
     gbs = b / (us * 1e-6) / 1e9
     err = arf.ar_workspace_device_error(ws)
@@ -572,19 +580,19 @@ def sweep_mhc_point(arf, torch, dev, stream, peak, l2, name, shp, T, mode="rotat
     torch.cuda.empty_cache()
     return {"workload": name, "R": R, "K": 0, "H": H, "hc": hc, "T": T, "us_per_call": round(us, 3),
             "GBps": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4), "regime": "mhc_post",
-            "ctas": None, "forced": False, "calls_per_graph": n_sets, "mode": mode, "gated": False,
+            "ctas": None, "forced": False, "calls_per_graph": calls, "mode": mode, "gated": False,
             "pdl": pdl, "device_error": err}
 
 
 def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0, mode="rotate",
-                gated=False, pdl=False):
+                gated=False, pdl=False, perm_kind="random"):
     """One (workload, T, regime) point of the sweep."""
     from gen import make_gate_logits, make_inputs, problem_bytes
     b = problem_bytes(cfg.R, cfg.K, cfg.H, T)
     n_sets = int(min(8192, max(2, math.ceil(3 * l2 / b))))
     if mode == "warm":
         n_sets = 1
-    big = make_inputs(cfg, T * n_sets, seed=11 + T, device=dev,
+    big = make_inputs(cfg, T * n_sets, seed=11 + T, device=dev, perm_kind=perm_kind,
                       perm_blocks=n_sets if mode == "rotate" else 1)
     ws = arf.ar_workspace_create(cfg.R, cfg.K, cfg.H, T, cfg.eps, device=dev.index,
                                  flags=arf.AR_WS_PDL if pdl else 0)
@@ -620,15 +628,16 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
     torch.cuda.current_stream(dev).wait_stream(side)
     torch.cuda.synchronize()
     regime, ctas = arf.ar_workspace_last_regime(ws)
+    calls = WARM_CALLS if mode == "warm" else n_sets
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         cs = torch.cuda.current_stream(dev)
-        for i in range(n_sets):
-            call(i, cs)
+        for i in range(calls):
+            call(i % n_sets, cs)
     g.replay()
     torch.cuda.synchronize()
     per = []
-    reps = 200 if mode == "warm" else 1
+    reps = 4 if mode == "warm" else 1
     for _ in range(3):
         a = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
@@ -637,7 +646,7 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
             g.replay()
         e.record(stream)
         torch.cuda.synchronize()
-        per.append(a.elapsed_time(e) * 1e3 / (n_sets * reps))
+        per.append(a.elapsed_time(e) * 1e3 / (calls * reps))
     us = statistics.median(per)
     gbs = b / (us * 1e-6) / 1e9
     err = arf.ar_workspace_device_error(ws)
@@ -648,7 +657,8 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
             "us_per_call": round(us, 3), "GBps": round(gbs, 1),
             "frac_of_hbm_peak": round(gbs / peak, 4),
             "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas,
-            "forced": force != 0, "calls_per_graph": n_sets, "mode": mode, "gated": gated,
+            "forced": force != 0, "calls_per_graph": calls, "mode": mode, "perm": perm_kind,
+            "gated": gated,
             "pdl": pdl, "device_error": err}
 
 

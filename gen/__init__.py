@@ -167,10 +167,15 @@ def make_inputs(cfg, T: int, seed: int | None = None, device="cpu",
         elif perm_kind == "random":
             perm = torch.randperm(rows_e, generator=g, device=device).to(torch.int32).view(T, K)
         elif perm_kind == "expert_sorted":
-            # position of slot (t, k) after a stable sort of all slots by expert id
-            order = torch.sort(ids.reshape(-1), stable=True).indices
+            # position of slot (t, k) after a stable sort of the slots by
+            # expert id, within each of perm_blocks blocks of tokens
+            if T % perm_blocks:
+                raise ValueError("T must be a multiple of perm_blocks")
+            blk = rows_e // perm_blocks
+            order = torch.sort(ids.reshape(perm_blocks, blk), dim=1, stable=True).indices
+            base = torch.arange(perm_blocks, device=device).view(-1, 1) * blk
             perm = torch.empty(rows_e, dtype=torch.int32, device=device)
-            perm[order] = torch.arange(rows_e, dtype=torch.int32, device=device)
+            perm[(order + base).reshape(-1)] = (torch.arange(blk, device=device).view(1, -1) + base).reshape(-1).to(torch.int32)
             perm = perm.view(T, K)
         else:
             raise ValueError(perm_kind)
