@@ -220,11 +220,12 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def cpu_oracle_run(min_seconds: float, seed: int, reps_max: int = 1000):
+def cpu_oracle_run(min_seconds: float, seed: int, reps_max: int = 1000, one_thread_passes: int = 0):
     """Time the CPU oracle on a bounded sample of the headline workload: T=512
     token rows drawn with the same recipe (R=8, K=10, H=8192), repeated until
     at least min_seconds have passed.  Returns (GB/s, threads, sample text,
-    per-pass seconds)."""
+    per-pass seconds, GB/s on one thread over one_thread_passes passes or
+    None)."""
     import oracle
     from gen import make_inputs, problem_bytes
     from tests._util import oracle_args
@@ -245,7 +246,18 @@ def cpu_oracle_run(min_seconds: float, seed: int, reps_max: int = 1000):
     gbs = b * len(times) / sum(times) / 1e9
     sample = (f"{CPU_SAMPLE_T} token rows of the prefill workload (R=8, K=10, H=8192) drawn with its "
               f"recipe, {b / 1e9:.3f} GB per pass, {len(times)} passes in {sum(times):.1f} s")
-    return gbs, oracle.num_threads(), sample, times
+    threads = oracle.num_threads()
+    gbs1 = None
+    if one_thread_passes > 0:
+        oracle.set_num_threads(1)
+        try:
+            t0 = time.perf_counter()
+            for _ in range(one_thread_passes):
+                call()
+            gbs1 = b * one_thread_passes / (time.perf_counter() - t0) / 1e9
+        finally:
+            oracle.set_num_threads(threads)
+    return gbs, threads, sample, times, gbs1
 
 
 def run_reference(args):
@@ -409,9 +421,9 @@ def main_ours(args):
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
-        gbs, cores, sample, _ = cpu_oracle_run(10.0, seed=7)
+        gbs, cores, sample, _, gbs1 = cpu_oracle_run(10.0, seed=7, one_thread_passes=2)
         cpu = {"value": round(gbs, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": sample}
+               "sample": sample, "value_1_thread": round(gbs1, 3)}
 
     ws.destroy()
     if rank == 0:
