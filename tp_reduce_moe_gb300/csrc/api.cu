@@ -174,15 +174,16 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
 
 // The built-in choice (measured on GB300 with bench.py's sweep):
 //  - light rows (at most 8 summands per 16-byte chunk, one load wave per
-//    thread) below one row per two SMs, and rows of at most 2 summands (the
-//    40-register variant) up to 1.5 rows per SM: the one-shot kernel;
+//    thread) up to three rows per four SMs (eight partials, K = 0, H = 7168:
+//    5.9 us at T = 96 against 7.4 streaming), and rows of at most 2 summands
+//    (the 40-register variant) up to 1.5 rows per SM: the one-shot kernel;
 //  - heavy rows at small T (one cluster per row in three quarters of the
 //    SMs): the split kernel, fewest bulk copies per CTA;
 //  - otherwise the streaming kernel (tiles over a cluster for small T, whole
 //    rows for large T).
 int plan_heuristic(const ar_workspace* ws, int R, int K, int H, bool shared, int64_t T, Plans* p) {
     const int summands = (shared ? R : 0) + R * K;
-    const bool light = (summands <= 8 && 2 * T < ws->num_sms) ||
+    const bool light = (summands <= 8 && 4 * T <= 3 * (int64_t)ws->num_sms) ||
                        (summands <= 2 && 2 * T <= 3 * (int64_t)ws->num_sms);
     if (light && arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c))
         return AR_REGIME_ONESHOT;
