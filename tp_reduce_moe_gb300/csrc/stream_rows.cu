@@ -155,11 +155,12 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    // Cluster barrier: arrived on now (this CTA's barriers exist), waited on
+    // by the consumers before their first push into a peer and by the
+    // producers before they exit -- the producers' first copies do not wait
+    // for the peers.
+    if (CLUSTERED) cluster_arrive_release();
     pdl_wait();  // no global memory access before this point
-    if (CLUSTERED) {  // every peer's barriers exist before anyone pushes
-        cluster_arrive_release();
-        cluster_wait_acquire();
-    }
 
     if (warp < W) {
         // ----------------------------------------------------------- producers
@@ -319,6 +320,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
                 }
             }
         }
+        if (CLUSTERED) {
+            __syncwarp();
+            cluster_wait_acquire();
+        }
         // After an abort, wait (briefly, bounded) for every copy still landing
         // in this warp's slots before the CTA may exit.
         if (lane == 0 && *abort_flag) {
@@ -331,6 +336,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     }
 
     // -------------------------------------------------------------- consumers
+    if (CLUSTERED) cluster_wait_acquire();  // every peer's barriers exist before any push
     const int ci = threadIdx.x - 32 * W;
     const int nct = ncw * 32;
     int lch[CPT];
