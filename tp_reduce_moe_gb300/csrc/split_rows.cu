@@ -161,10 +161,15 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         const int ci = threadIdx.x - 32;
         const int nct = ncw * 32;
         float acc[CPT][8];
+        bool valid[CPT];
+        const uint8_t* src[CPT];  // this thread's chunk in segment 0
 #pragma unroll
-        for (int m = 0; m < CPT; ++m)
+        for (int m = 0; m < CPT; ++m) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[m][j] = 0.0f;
+            valid[m] = ci + m * nct < chunks;
+            src[m] = segbuf + (size_t)(ci + m * nct) * 16;
+        }
         bool ok = true;
         for (int phase_set = 0; phase_set < 2; ++phase_set) {
             const int i_begin = phase_set == 0 ? 0 : nsr_c;
@@ -175,29 +180,34 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                 if (!*abort_flag) atomicOr(a.err, kErrTimeout);
                 *abort_flag = 1;
             }
+            // Full steps of SU segments without per-segment guards (the
+            // instruction count, not the load latency, bounds this loop),
+            // then the remaining segments one at a time; the same
+            // sequential order per column either way.
             constexpr int SU = CPT >= 4 ? 2 : 4;  // segments per step (loads in registers)
-            for (int i0 = i_begin; i0 < i_end; i0 += SU) {
+            const size_t stride = (size_t)geo.seg_stride;
+            int i0 = i_begin;
+            for (; i0 + SU <= i_end; i0 += SU) {
                 float cf[SU];
                 uint4 v[SU][CPT];
 #pragma unroll
-                for (int u = 0; u < SU; ++u) cf[u] = i0 + u < i_end ? coef[i0 + u] : 0.0f;
+                for (int u = 0; u < SU; ++u) cf[u] = coef[i0 + u];
 #pragma unroll
                 for (int u = 0; u < SU; ++u)
 #pragma unroll
-                    for (int m = 0; m < CPT; ++m) {
-                        const int ch = ci + m * nct;
-                        if (i0 + u < i_end && ch < chunks)
-                            v[u][m] = reinterpret_cast<const uint4*>(segbuf + (size_t)(i0 + u) * geo.seg_stride)[ch];
-                    }
+                    for (int m = 0; m < CPT; ++m)
+                        if (valid[m]) v[u][m] = *reinterpret_cast<const uint4*>(src[m] + (size_t)(i0 + u) * stride);
 #pragma unroll
                 for (int u = 0; u < SU; ++u)
 #pragma unroll
-                    for (int m = 0; m < CPT; ++m) {
-                        const int ch = ci + m * nct;
-                        if (i0 + u < i_end && ch < chunks) {
-                            fma_bf16x8(acc[m], cf[u], v[u][m]);
-                        }
-                    }
+                    for (int m = 0; m < CPT; ++m)
+                        if (valid[m]) fma_bf16x8(acc[m], cf[u], v[u][m]);
+            }
+            for (; i0 < i_end; ++i0) {
+                const float cf = coef[i0];
+#pragma unroll
+                for (int m = 0; m < CPT; ++m)
+                    if (valid[m]) fma_bf16x8(acc[m], cf, *reinterpret_cast<const uint4*>(src[m] + (size_t)i0 * stride));
             }
         }
         // The partial row, locally (over the spent segment buffers); made
