@@ -102,6 +102,42 @@ __device__ __forceinline__ void part_stage_range(int j, int P, int nsr, int a, i
     }
 }
 
+// acc[m] += sum over the slot's cnt segments of coef[i] * segment i's chunk
+// lch[m] (for valid[m]): full steps of U segments, loads first, with no
+// per-segment guards (the instruction count bounds this loop), then the
+// remaining segments one at a time; the same sequential order per column.
+template <int CPT, int U>
+__device__ __forceinline__ void fold_slot(float (&acc)[CPT][8], const float* coef, const uint8_t* seg,
+                                          size_t seg_stride, int cnt, const int (&lch)[CPT],
+                                          const bool (&valid)[CPT]) {
+    const uint8_t* src[CPT];
+#pragma unroll
+    for (int m = 0; m < CPT; ++m) src[m] = seg + (size_t)lch[m] * 16;
+    int i0 = 0;
+    for (; i0 + U <= cnt; i0 += U) {
+        float cf[U];
+        uint4 v[U][CPT];
+#pragma unroll
+        for (int u = 0; u < U; ++u) cf[u] = coef[i0 + u];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int m = 0; m < CPT; ++m)
+                if (valid[m]) v[u][m] = *reinterpret_cast<const uint4*>(src[m] + (size_t)(i0 + u) * seg_stride);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int m = 0; m < CPT; ++m)
+                if (valid[m]) fma_bf16x8(acc[m], cf[u], v[u][m]);
+    }
+    for (; i0 < cnt; ++i0) {
+        const float cf = coef[i0];
+#pragma unroll
+        for (int m = 0; m < CPT; ++m)
+            if (valid[m]) fma_bf16x8(acc[m], cf, *reinterpret_cast<const uint4*>(src[m] + (size_t)i0 * seg_stride));
+    }
+}
+
 template <int CPT, int U, bool RES_F32, bool CLUSTERED>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     stream_rows_kernel(const __grid_constant__ RowArgs a, const StreamGeom geo) {
@@ -377,25 +413,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
             const float* coef = reinterpret_cast<const float*>(base);
             const uint8_t* seg = base + kSlotHeader;
             // U segments at a time: loads first, then FMAs.
-            for (int i0 = 0; i0 < cnt; i0 += U) {
-                float cf[U];
-                uint4 v[U][CPT];
-#pragma unroll
-                for (int u = 0; u < U; ++u) cf[u] = i0 + u < cnt ? coef[i0 + u] : 0.0f;
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int m = 0; m < CPT; ++m)
-                        if (i0 + u < cnt && valid[m])
-                            v[u][m] = reinterpret_cast<const uint4*>(seg + (size_t)(i0 + u) * geo.seg_stride)[lch[m]];
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int m = 0; m < CPT; ++m)
-                        if (i0 + u < cnt && valid[m]) {
-                            fma_bf16x8(acc[m], cf[u], v[u][m]);
-                        }
-            }
+            fold_slot<CPT, U>(acc, coef, seg, (size_t)geo.seg_stride, cnt, lch, valid);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&empty[slot]));
             if (++slot == nst) {
@@ -486,25 +504,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
             const uint8_t* base = ring + (size_t)slot * geo.slot_bytes;
             const float* coef = reinterpret_cast<const float*>(base);
             const uint8_t* seg = base + kSlotHeader;
-            for (int i0 = 0; i0 < cnt; i0 += U) {
-                float cf[U];
-                uint4 v[U][CPT];
-#pragma unroll
-                for (int u = 0; u < U; ++u) cf[u] = i0 + u < cnt ? coef[i0 + u] : 0.0f;
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int m = 0; m < CPT; ++m)
-                        if (i0 + u < cnt && valid[m])
-                            v[u][m] = reinterpret_cast<const uint4*>(seg + (size_t)(i0 + u) * geo.seg_stride)[lch[m]];
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int m = 0; m < CPT; ++m)
-                        if (i0 + u < cnt && valid[m]) {
-                            fma_bf16x8(acc[m], cf[u], v[u][m]);
-                        }
-            }
+            fold_slot<CPT, U>(acc, coef, seg, (size_t)geo.seg_stride, cnt, lch, valid);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&empty[slot]));
             if (++slot == nst) {
