@@ -134,10 +134,11 @@ def make_inputs(cfg, T: int, seed: int | None = None, device="cpu",
     [T*K, H] or None), perm (int32 [T, K] or None), w (fp32 [T, K] or None),
     S (list of R bf16 [T, H] or None), residual (bf16 [T, H]), gamma (bf16 [H]).
 
-    perm_blocks = n > 1 (random perm only) draws the T rows as n equal blocks,
-    each gathering only from its own contiguous block of T*K/n expert rows --
-    n independent problems packed in one buffer, as n successive layers' expert
-    outputs would be.
+    perm_blocks = n > 1 draws the T rows as n equal blocks, each gathering only
+    from its own contiguous block of T*K/n expert rows -- n independent
+    problems packed in one buffer, as n successive layers' expert outputs would
+    be (perm_kind "random": a random permutation within each block;
+    "expert_sorted": the slots of each block stably sorted by expert id).
     """
     if isinstance(cfg, str):
         cfg = CONFIGS[cfg]
