@@ -148,10 +148,16 @@ def peaks():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the streaming kernel's code (comments and blank lines dropped,
+    so an edited comment does not void a traffic capture)."""
+    import re
     h = hashlib.sha256()
     for name in ("stream_rows.cu", "arf_common.cuh"):
-        with open(os.path.join(ROOT, "tp_reduce_moe_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "tp_reduce_moe_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
 
 

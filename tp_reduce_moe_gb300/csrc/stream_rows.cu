@@ -16,9 +16,9 @@
 //     fills one slot per latency; W producer warps take the slots
 //     round-robin and keep W slots in flight;
 //   * consumer warps fold each landed slot into fp32 accumulators held in
-//     registers (CPT 16-byte chunks per thread, U slots per step so several
-//     shared-memory loads are in flight), then release it on the slot's
-//     `empty` mbarrier;
+//     registers (CPT 16-byte chunks per thread, U segments per step with
+//     their shared-memory loads issued together and no per-segment guards),
+//     then release it on the slot's `empty` mbarrier;
 //   * after a row's last segment the consumers finish the row on chip: store
 //     residual_out, reduce the sum of squares (warp shuffle + one named
 //     barrier), and -- for tiles -- push the CTA's partial into every peer's
