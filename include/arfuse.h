@@ -83,8 +83,8 @@ typedef enum ar_status {
 /* ar_workspace_create() flags. */
 #define AR_WS_DRY_RUN 0x1u      /* no GPU state: calls validate, then return AR_VALIDATED   */
 #define AR_WS_NORM_BF16_H 0x2u  /* the norm reads h rounded to bf16, as a bf16 residual_out  */
-#define AR_WS_PDL 0x4u          /* launch with programmatic dependent launch (see below)      */
                                 /* stores it (default: the unrounded fp32 sum)              */
+#define AR_WS_PDL 0x4u          /* launch with programmatic dependent launch (see below)      */
 
 /* Bits of the device error word (ar_workspace_device_error). */
 #define AR_DEVERR_PERM_RANGE 0x1   /* some perm value was outside [0, rows_e); clamped */
@@ -223,7 +223,14 @@ ARFUSE_API ar_status ar_rmsnorm(ar_workspace* ws, const void* const* partials, i
  * Read and clear the workspace's device error word (AR_DEVERR_* bits) into
  * *code (host pointer).  Synchronises the workspace's device first.  Returns
  * AR_ERR_DEVICE_CHECK when a bit was set, AR_OK when none, AR_ERR_INVALID_ARG
- * for NULL arguments, AR_ERR_CUDA on a failed copy.
+ * for NULL arguments, AR_ERR_CUDA on a failed copy.  A set bit means the
+ * fused call declined part of its work on the device (rows left unfinished
+ * after a wait ran out, or clamped perm values): the caller still owes that
+ * reduction and can rerun the step on its own unfused path, as a runtime
+ * decline of the fused boundary must allow (sglang PR #37104 "perf(mtp): fuse
+ * trailing TP all-reduce with final RMSNorm", Changes).  When a bit was set
+ * the workspace's split-row counters are reset too, so the next call starts
+ * clean.
  */
 ARFUSE_API ar_status ar_workspace_device_error(ar_workspace* ws, int* code);
 
@@ -294,6 +301,23 @@ ARFUSE_API ar_status ar_workspace_set_split_column_groups(ar_workspace* ws, int 
 #define AR_MAX_SPLIT_PARTS 8
 ARFUSE_API ar_status ar_workspace_set_split_rows(ar_workspace* ws, int max_parts);
 
+/*
+ * Failure injection for tests of the device-side timeout path (the clean
+ * decline of sglang PR #37104 "perf(mtp): fuse trailing TP all-reduce with
+ * final RMSNorm", Changes: a fused call that gives up must leave the caller
+ * able to finish the reduction itself).  With limit_ns > 0, later calls on
+ * this workspace that run whole-row streaming (AR_REGIME_STREAM) make every
+ * consumer warp's first wait target a barrier that nothing arrives on, bounded
+ * by limit_ns nanoseconds: the wait runs out, the kernel records
+ * AR_DEVERR_TIMEOUT in the error word, skips its remaining waits (its rows are
+ * left unfinished: out and residual_out of that call are undefined), waits for
+ * its own bulk copies still in flight and returns.  Nothing faults or hangs.
+ * Calls in any other regime return AR_ERR_UNSUPPORTED while it is set (force
+ * AR_REGIME_STREAM with ar_workspace_set_regime).  limit_ns = 0 turns it off;
+ * values outside [0, 1e9] are AR_ERR_INVALID_ARG.
+ */
+ARFUSE_API ar_status ar_workspace_inject_wait_timeout(ar_workspace* ws, int64_t limit_ns);
+
 /* Regime (AR_REGIME_CLUSTER / _STREAM / _ONESHOT / _SPLIT) of the last
  * launched call (on a dry-run workspace: of the last validated call), 0
  * before the first one.  *ctas receives the CTAs per row
@@ -348,7 +372,9 @@ ARFUSE_API ar_status ar_workspace_get_regime_table(const ar_workspace* ws, ar_re
  * output back as the FFN's tensor-parallel all-reduce followed by hc_post,
  * which reads the reduced output back and mixes it into the hc_mult (four)
  * residual streams; the fused kernel does both in one pass.  The page gives
- * no formula for the mix; this entry point computes the per-token linear mix
+ * no formula for the mix, so parity of this entry point is unpinned: its
+ * oracle fixes only this library's reading of the page, the per-token linear
+ * mix
  *
  *   y[t,j]     = sum_{r<R} partials[r][t,j]                       (fp32)
  *   out[t,i,j] = post[t,i] * y[t,j] + sum_{k<hc} comb[t,i,k] * streams[t,k,j]
@@ -393,12 +419,20 @@ ARFUSE_API ar_status ar_mhc_post(ar_workspace* ws, const void* const* partials, 
  * bytes for any size, so the array's 256 bytes always suffice.
  *
  *   - The first call on a device (the current device) does a one-time set-up
- *     there: kernel attributes and the device address of the array.  Make that
- *     first call before any stream capture on that device.
- *   - Each call clears the status word on `stream` before its kernel runs.
- *     Device-side check results (a clamped perm value, a wait past its time
- *     limit) land in that word and are not reported by this entry point; check
- *     perm ranges on the host where they matter, or use a workspace.
+ *     there: kernel attributes and the device address of the array; the first
+ *     call with each new (R, K, H) also measures that shape's launch limits on
+ *     the host.  Make those first calls before any stream capture on that
+ *     device.
+ *   - The plans are those of ar_finalize_rmsnorm() on a workspace of the same
+ *     shape, with one difference: without a workspace's split-row scratch,
+ *     whole-row streaming never splits the rows of its last, partial wave
+ *     over idle CTAs (so at T mod SMs > 0 a call can be slower than the
+ *     workspace entry point's).  A plan the device cannot co-schedule is
+ *     declined as AR_ERR_UNSUPPORTED before anything is launched.
+ *   - Device-side check results (a clamped perm value, a wait past its time
+ *     limit) are OR-ed into the status word, which this entry point neither
+ *     clears nor reads: check perm ranges on the host where they matter, or
+ *     use a workspace.
  *   - Every call shares the array: calls that overlap on the GPU (on
  *     different streams, without ordering between them) race on the status
  *     word.  Their outputs are unaffected.
@@ -411,7 +445,10 @@ ARFUSE_API ar_status ar_finalize_rmsnorm_noalloc(const void* const* expert_out, 
                                                  int K, int H, void* out, void* residual_out,
                                                  int residual_out_is_fp32, void* stream);
 
-/* Static description of a status code; never NULL. */
+/* Static description of a status code; never NULL.  Every status other than
+ * AR_OK / AR_VALIDATED is a clean decline: nothing was launched and the
+ * caller runs its own split path (sglang PR #37104 "perf(mtp): fuse trailing
+ * TP all-reduce with final RMSNorm", Changes). */
 ARFUSE_API const char* ar_status_string(ar_status s);
 
 #ifdef __cplusplus

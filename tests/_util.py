@@ -65,3 +65,24 @@ def check_f32(got: torch.Tensor, ref64: np.ndarray, abs64: np.ndarray, what: str
             f"first {idx.tolist()}: got {g[bad][:5]} want {ref64[bad][:5]}")
     big = np.abs(ref64) >= 1e-2
     return float((err[big] / np.abs(ref64[big])).max()) if big.any() else 0.0
+
+
+def sample_rows(d, rows):
+    """Compact CPU problem holding only the given token rows of a device problem
+    (the gathered expert rows become a dense [len(rows)*K, H] block)."""
+    dev = d["residual"].device
+    idx = torch.as_tensor(rows, device=dev, dtype=torch.long)
+    K = d["K"]
+    comp = dict(R=d["R"], K=K, H=d["H"], T=len(rows), rows_e=len(rows) * K, eps=d["eps"],
+                weight_bias=d["weight_bias"])
+    if K > 0:
+        gathered = d["perm"][idx].reshape(-1).long()
+        comp["E"] = [e.index_select(0, gathered).cpu() for e in d["E"]]
+        comp["perm"] = torch.arange(len(rows) * K, dtype=torch.int32).view(len(rows), K)
+        comp["w"] = d["w"][idx].cpu()
+    else:
+        comp["E"], comp["perm"], comp["w"] = None, None, None
+    comp["S"] = [s[idx].cpu() for s in d["S"]] if d["S"] is not None else None
+    comp["residual"] = d["residual"][idx].cpu()
+    comp["gamma"] = d["gamma"].cpu()
+    return comp

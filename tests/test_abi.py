@@ -399,3 +399,24 @@ def test_pdl_flag_is_accepted(lib):
     h = ctypes.c_void_p()
     assert lib.ar_workspace_create(0, R, K, H, TMAX, EPS, arf.AR_WS_DRY_RUN | 0x8, ctypes.byref(h)) == \
         arf.AR_ERR_INVALID_ARG
+
+
+def test_wait_timeout_injection_setter(lib):
+    w = arf.ar_workspace_create(R, K, H, TMAX, EPS, flags=arf.AR_WS_DRY_RUN)
+    try:
+        arf.ar_workspace_inject_wait_timeout(w, 50_000)
+        # the injected wait exists only in whole-row streaming: any other regime declines
+        for regime in (arf.AR_REGIME_CLUSTER, arf.AR_REGIME_ONESHOT, arf.AR_REGIME_SPLIT):
+            arf.ar_workspace_set_regime(w, regime)
+            assert Fake().call(lib, w) == arf.AR_ERR_UNSUPPORTED
+        arf.ar_workspace_set_regime(w, arf.AR_REGIME_STREAM)
+        assert Fake().call(lib, w) == arf.AR_VALIDATED
+        arf.ar_workspace_inject_wait_timeout(w, 0)
+        arf.ar_workspace_set_regime(w, arf.AR_REGIME_SPLIT)
+        assert Fake().call(lib, w) == arf.AR_VALIDATED
+        for bad in (-1, 1_000_000_001):
+            with pytest.raises(arf.ArfuseError):
+                arf.ar_workspace_inject_wait_timeout(w, bad)
+    finally:
+        w.destroy()
+    assert lib.ar_workspace_inject_wait_timeout(None, 1) == arf.AR_ERR_INVALID_ARG

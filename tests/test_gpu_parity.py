@@ -14,7 +14,7 @@ import torch
 import oracle
 import tp_reduce_moe_gb300 as arf
 from gen import CONFIGS, Config, make_inputs, make_perm_decode_inputs
-from tests._util import check_bf16, check_f32, oracle_args, run_oracle
+from tests._util import check_bf16, check_f32, oracle_args, run_oracle, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -98,28 +98,12 @@ def test_config_full(cfg, T):
 
 
 # ----------------------------- full-size prefill: sampled rows against the oracle
-def _sample_rows(d, rows):
-    """Compact CPU problem holding only the given token rows of a device problem."""
-    idx = torch.as_tensor(rows, device=DEV, dtype=torch.long)
-    K = d["K"]
-    gathered = d["perm"][idx].reshape(-1).long()
-    comp = dict(R=d["R"], K=K, H=d["H"], T=len(rows), rows_e=len(rows) * K, eps=d["eps"],
-                weight_bias=d["weight_bias"])
-    comp["E"] = [e.index_select(0, gathered).cpu() for e in d["E"]]
-    comp["perm"] = torch.arange(len(rows) * K, dtype=torch.int32).view(len(rows), K)
-    comp["w"] = d["w"][idx].cpu()
-    comp["S"] = [s[idx].cpu() for s in d["S"]] if d["S"] is not None else None
-    comp["residual"] = d["residual"][idx].cpu()
-    comp["gamma"] = d["gamma"].cpu()
-    return comp
-
-
 @pytest.mark.parametrize("T", [2048, 8192])
 def test_prefill_full_size_sampled(T):
     d = make_inputs("prefill", T, device=DEV)
     rng = np.random.default_rng(T)
     rows = sorted(set([0, 1, T // 2, T - 2, T - 1] + rng.integers(0, T, 59).tolist()))
-    ref = run_oracle(_sample_rows(d, rows), want_abs=True)
+    ref = run_oracle(sample_rows(d, rows), want_abs=True)
     ws = make_ws(d)
     try:
         for regime in REGIMES:

@@ -17,4 +17,4 @@ from .binding import (  # noqa: F401
     ar_workspace_set_producer_warps, ar_workspace_set_stage_bytes, load_library,
     AR_MAX_REGIME_RULES, RegimeRule, ar_workspace_get_regime_table, ar_workspace_set_regime_table,
     AR_MAX_HC_STREAMS, ar_mhc_post, AR_MAX_SPLIT_PARTS, ar_workspace_set_split_rows,
-    ar_workspace_set_split_column_groups)
+    ar_workspace_set_split_column_groups, ar_workspace_inject_wait_timeout)

@@ -87,6 +87,8 @@ def load_library(path: str | None = None):
         lib.ar_workspace_set_stage_bytes.argtypes = [P, I]
         lib.ar_workspace_set_split_rows.restype = I
         lib.ar_workspace_set_split_rows.argtypes = [P, I]
+        lib.ar_workspace_inject_wait_timeout.restype = I
+        lib.ar_workspace_inject_wait_timeout.argtypes = [P, I64]
         lib.ar_workspace_set_producer_warps.restype = I
         lib.ar_workspace_set_producer_warps.argtypes = [P, I]
         lib.ar_workspace_set_split_column_groups.restype = I
@@ -226,6 +228,15 @@ def ar_workspace_set_producer_warps(ws: Workspace, warps: int) -> None:
     """Cap the streaming kernels' producer warps (1..4; tuning); 0 = automatic."""
     _check(load_library().ar_workspace_set_producer_warps(ctypes.c_void_p(ws.handle), int(warps)),
            "ar_workspace_set_producer_warps")
+
+
+def ar_workspace_inject_wait_timeout(ws: Workspace, limit_ns: int) -> None:
+    """Failure injection for tests (0 = off): whole-row streaming calls make
+    their consumers wait on a barrier nothing arrives on, for limit_ns, so the
+    call takes the device-side timeout path (AR_DEVERR_TIMEOUT, outputs of
+    that call undefined); other regimes decline while it is set."""
+    _check(load_library().ar_workspace_inject_wait_timeout(ctypes.c_void_p(ws.handle), int(limit_ns)),
+           "ar_workspace_inject_wait_timeout")
 
 
 def ar_workspace_last_regime(ws: Workspace):

@@ -39,6 +39,7 @@ struct ar_workspace {
     int split_groups;        // column groups per row of the split kernel; 0: automatic
     int last_regime;
     int last_ctas;
+    unsigned long long stall_wait_ns;  // failure injection (whole-row streaming), 0 = off
     int table_n;  // rules in `table` (0: heuristic only)
     ar_regime_rule table[AR_MAX_REGIME_RULES];
 };
@@ -200,11 +201,35 @@ int plan_heuristic(const ar_workspace* ws, int R, int K, int H, bool shared, int
     return p->s.geo.C > 1 ? AR_REGIME_CLUSTER : AR_REGIME_STREAM;
 }
 
+// Largest clusters the device co-schedules for the block shapes of one model
+// shape (R, K, H): the one-shot kernel, the clustered streaming kernel (16
+// tiles of one row) and the split kernel.
+void cluster_limits(int R, int K, int H, int num_sms, int smem_optin, int* max_cluster,
+                    int* max_cluster_stream, int* max_cluster_split) {
+    arf::ClusterPlan p{};
+    *max_cluster = 16;
+    if (arf::plan_cluster_rows(R, K, H, true, 16, 1, num_sms, &p))
+        *max_cluster = arf::cluster_rows_max_cluster(p.threads, p.smem, false);
+    if (*max_cluster < 1) *max_cluster = 1;
+    arf::StreamPlan sp{};
+    *max_cluster_stream = 1;
+    for (int c = 16; c >= 2 && *max_cluster_stream == 1; c >>= 1)
+        if (arf::plan_stream_rows(R, K, H, true, 1, num_sms, smem_optin, 16, c, 0, &sp))
+            *max_cluster_stream = arf::stream_rows_max_cluster(sp.threads, sp.smem, sp.cpt);
+    arf::SplitPlan xp{};
+    *max_cluster_split = 1;
+    for (int c = 16; c >= 2 && *max_cluster_split == 1; c >>= 1)
+        if (arf::plan_split_rows(R, K, H, true, 1, num_sms, smem_optin, 16, c, &xp))
+            *max_cluster_split = arf::split_rows_max_cluster(xp.threads, xp.smem, xp.cpt);
+}
+
 ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int32_t* perm,
               const float* w, const void* const* S, const void* residual, const void* gamma,
               float weight_bias, float eps, int64_t T, int R, int K, int H, void* out,
               void* residual_out, int res_f32, void* stream, bool routed_call,
-              const float* gate = nullptr) {
+              const float* gate = nullptr,
+              bool (*plan_fits)(void* ctx, int regime, const Plans& p, bool res_f32) = nullptr,
+              void* fits_ctx = nullptr) {
     if (!ws) return AR_ERR_INVALID_ARG;
     if (R != ws->R || H != ws->H) return AR_ERR_INVALID_ARG;
     if (routed_call && K != ws->K) return AR_ERR_INVALID_ARG;
@@ -282,6 +307,12 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
         if (!regime) regime = plan_heuristic(ws, R, K, H, shared, T, &pl);
         if (!regime) return AR_ERR_UNSUPPORTED;
     }
+    // The injected wait exists only in whole-row streaming.
+    if (ws->stall_wait_ns && regime != AR_REGIME_STREAM) return AR_ERR_UNSUPPORTED;
+    // A caller-supplied check of the exact launch (block, shared memory,
+    // cluster): a plan the device cannot co-schedule is declined here, before
+    // anything is launched.
+    if (plan_fits && !plan_fits(fits_ctx, regime, pl, res_f32 != 0)) return AR_ERR_UNSUPPORTED;
     const int ctas = regime == AR_REGIME_ONESHOT ? pl.c.C
                      : regime == AR_REGIME_SPLIT ? pl.x.geo.C
                      : regime == AR_REGIME_CLUSTER ? pl.s.geo.C
@@ -324,6 +355,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     a.norm_bf16_h = (ws->flags & AR_WS_NORM_BF16_H) ? 1 : 0;
     a.weight_bias = weight_bias;
     a.eps = eps;
+    a.stall_wait_ns = ws->stall_wait_ns;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -412,26 +444,8 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
         st = AR_ERR_CUDA;
         goto fail;
     }
-    {
-        // Largest cluster the device co-schedules for this model's block shape.
-        arf::ClusterPlan p{};
-        ws->max_cluster = 16;
-        if (arf::plan_cluster_rows(ranks, top_k, hidden, true, 16, 1, ws->num_sms, &p))
-            ws->max_cluster = arf::cluster_rows_max_cluster(p.threads, p.smem, false);
-        if (ws->max_cluster < 1) ws->max_cluster = 1;
-        // ... and for the clustered streaming kernel (16 tiles of one row).
-        arf::StreamPlan sp{};
-        ws->max_cluster_stream = 1;
-        for (int c = 16; c >= 2 && ws->max_cluster_stream == 1; c >>= 1)
-            if (arf::plan_stream_rows(ranks, top_k, hidden, true, 1, ws->num_sms, ws->smem_optin, 16, c, 0, &sp))
-                ws->max_cluster_stream = arf::stream_rows_max_cluster(sp.threads, sp.smem, sp.cpt);
-        // ... and for the split kernel.
-        arf::SplitPlan xp{};
-        ws->max_cluster_split = 1;
-        for (int c = 16; c >= 2 && ws->max_cluster_split == 1; c >>= 1)
-            if (arf::plan_split_rows(ranks, top_k, hidden, true, 1, ws->num_sms, ws->smem_optin, 16, c, &xp))
-                ws->max_cluster_split = arf::split_rows_max_cluster(xp.threads, xp.smem, xp.cpt);
-    }
+    cluster_limits(ranks, top_k, hidden, ws->num_sms, ws->smem_optin, &ws->max_cluster,
+                   &ws->max_cluster_stream, &ws->max_cluster_split);
     if (cudaMalloc(&ws->d_err, 256) != cudaSuccess || cudaMemset(ws->d_err, 0, 256) != cudaSuccess) {
         st = AR_ERR_CUDA;
         goto fail;
@@ -634,6 +648,13 @@ ar_status ar_workspace_set_split_column_groups(ar_workspace* ws, int groups) {
     return AR_OK;
 }
 
+ar_status ar_workspace_inject_wait_timeout(ar_workspace* ws, int64_t limit_ns) {
+    if (!ws) return AR_ERR_INVALID_ARG;
+    if (limit_ns < 0 || limit_ns > (int64_t)arf::kWaitLimitNs) return AR_ERR_INVALID_ARG;
+    ws->stall_wait_ns = (unsigned long long)limit_ns;
+    return AR_OK;
+}
+
 ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps) {
     if (!ws) return AR_ERR_INVALID_ARG;
     if (warps < 0 || warps > 4) return AR_ERR_INVALID_ARG;
@@ -671,31 +692,46 @@ const char* ar_status_string(ar_status s) {
 // plugins living under an engine whose memory pool owns all device memory and
 // rejects allocations it did not make, or deployments with a fixed device
 // memory budget checked at start-up.  ar_workspace_create() allocates a small
-// device block for the kernels' status word, so those callers cannot use it.
-// ar_finalize_rmsnorm_noalloc() needs no workspace: the only global memory the
-// kernels use beyond the caller's inputs and outputs -- the status word that
-// device-side checks write -- lives in the fixed array below, which every GPU
-// that loads this library holds until the process exits.
+// device block for the kernels' status word (and a split-row scratch), so
+// those callers cannot use it.  ar_finalize_rmsnorm_noalloc() needs no
+// workspace: the only global memory the kernels use beyond the caller's
+// inputs and outputs -- the status word that device-side checks write -- lives
+// in the fixed array below, which every GPU that loads this library holds
+// until the process exits.  Without a split-row scratch, its plans never split
+// the rows of whole-row streaming's last partial wave.
 namespace {
 
 constexpr int kNoAllocScratchBytes = 256;  // stated maximum; a call uses 4 bytes
 static __device__ __align__(256) unsigned int g_noalloc_scratch[kNoAllocScratchBytes / 4];
 
+// Host-side caches (fixed size, no allocation): cluster limits per model
+// shape, and whether an exact launch fits the device.
 constexpr int kNoAllocMaxDevices = 64;
+constexpr int kShapeCache = 32;
+constexpr int kFitCache = 64;
+struct ShapeLimits {
+    int R, K, H;  // R == 0: empty entry
+    int max_cluster, max_cluster_stream, max_cluster_split;
+};
+struct LaunchFit {
+    int key[6];  // regime, instantiation, res_f32, threads, smem, cluster size; key[0] == 0: empty
+    bool fits;
+};
 struct NoAllocDevice {
     bool ready;
     unsigned* scratch;  // device address of g_noalloc_scratch on this device
     int num_sms;
     int smem_optin;
-    int max_cluster;
-    int max_cluster_stream;
-    int max_cluster_split;
+    ShapeLimits shapes[kShapeCache];
+    int next_shape;
+    LaunchFit fit[kFitCache];
+    int next_fit;
 };
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 std::mutex g_noalloc_mu;
 
-// One-time set-up for the current device: kernel attributes, launch limits and
-// the device address of the scratch array.  Allocates nothing.
+// One-time set-up for the current device: kernel attributes and the device
+// address of the scratch array.  Allocates nothing.
 ar_status noalloc_setup(int device, NoAllocDevice** out) {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     NoAllocDevice& d = g_noalloc_dev[device];
@@ -720,16 +756,47 @@ ar_status noalloc_setup(int device, NoAllocDevice** out) {
     d.scratch = static_cast<unsigned*>(p);
     d.num_sms = prop.multiProcessorCount;
     d.smem_optin = (int)prop.sharedMemPerBlockOptin;
-    // Largest co-schedulable clusters for the biggest block shapes the plans
-    // can produce (one-shot: 768 threads, 24 KB; tiles: 544 threads, a third
-    // of shared memory).
-    d.max_cluster = arf::cluster_rows_max_cluster(768, 24576, false);
-    if (d.max_cluster < 1) d.max_cluster = 1;
-    d.max_cluster_stream = arf::stream_rows_max_cluster(544, d.smem_optin / 3, 1);
-    d.max_cluster_split = arf::split_rows_max_cluster(544, d.smem_optin, 2);
     d.ready = true;
     *out = &d;
     return AR_OK;
+}
+
+// Cluster limits of a model shape, computed as ar_workspace_create() does
+// (so the plans match the workspace entry point's) and cached.
+ShapeLimits noalloc_limits(NoAllocDevice* d, int R, int K, int H) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    for (const ShapeLimits& e : d->shapes)
+        if (e.R == R && e.K == K && e.H == H) return e;
+    ShapeLimits e{R, K, H, 1, 1, 1};
+    cluster_limits(R, K, H, d->num_sms, d->smem_optin, &e.max_cluster, &e.max_cluster_stream,
+                   &e.max_cluster_split);
+    d->shapes[d->next_shape] = e;
+    d->next_shape = (d->next_shape + 1) % kShapeCache;
+    return e;
+}
+
+// Whether the device can run the exact launch of a plan (cached).
+bool noalloc_plan_fits(void* ctx, int regime, const Plans& p, bool res_f32) {
+    NoAllocDevice* d = static_cast<NoAllocDevice*>(ctx);
+    int key[6] = {regime, 0, res_f32 ? 1 : 0, 0, 0, 0};
+    if (regime == AR_REGIME_ONESHOT) {
+        key[1] = p.c.maxt; key[3] = p.c.threads; key[4] = p.c.smem; key[5] = p.c.C;
+    } else if (regime == AR_REGIME_SPLIT) {
+        key[1] = p.x.cpt; key[3] = p.x.threads; key[4] = p.x.smem; key[5] = p.x.geo.C;
+    } else {
+        key[1] = p.s.cpt; key[3] = p.s.threads; key[4] = p.s.smem; key[5] = p.s.geo.C;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    for (const LaunchFit& f : d->fit)
+        if (f.key[0] != 0 && std::memcmp(f.key, key, sizeof key) == 0) return f.fits;
+    const bool fits = regime == AR_REGIME_ONESHOT ? arf::cluster_rows_plan_fits(p.c, res_f32)
+                      : regime == AR_REGIME_SPLIT ? arf::split_rows_plan_fits(p.x, res_f32)
+                                                  : arf::stream_rows_plan_fits(p.s, res_f32);
+    LaunchFit& f = d->fit[d->next_fit];
+    std::memcpy(f.key, key, sizeof key);
+    f.fits = fits;
+    d->next_fit = (d->next_fit + 1) % kFitCache;
+    return fits;
 }
 
 }  // namespace
@@ -753,9 +820,11 @@ ar_status ar_finalize_rmsnorm_noalloc(const void* const* expert_out, int64_t row
     NoAllocDevice* d = nullptr;
     const ar_status st = noalloc_setup(device, &d);
     if (st != AR_OK) return st;
+    const ShapeLimits lim = noalloc_limits(d, R, K, H);
 
     // A workspace on the stack: the same validation, plans and kernels as
-    // ar_finalize_rmsnorm(), with the scratch array as the status word.
+    // ar_finalize_rmsnorm(), with the scratch array as the status word and no
+    // split-row scratch.
     ar_workspace ws;
     std::memset(&ws, 0, sizeof ws);
     ws.device = device;
@@ -764,28 +833,20 @@ ar_status ar_finalize_rmsnorm_noalloc(const void* const* expert_out, int64_t row
     ws.H = H;
     ws.max_tokens = kMaxTokensLimit;
     ws.eps = eps;
-    ws.flags = AR_WS_DRY_RUN;  // first pass: validate only
+    ws.flags = 0;
     ws.d_err = d->scratch;
     ws.num_sms = d->num_sms;
     ws.smem_optin = d->smem_optin;
-    ws.max_cluster = d->max_cluster;
-    ws.max_cluster_stream = d->max_cluster_stream;
-    ws.max_cluster_split = d->max_cluster_split;
+    ws.max_cluster = lim.max_cluster;
+    ws.max_cluster_stream = lim.max_cluster_stream;
+    ws.max_cluster_split = lim.max_cluster_split;
     ws.regime_force = AR_REGIME_AUTO;
     install_builtin_table(&ws);
-    ar_status v = run(&ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma,
-                      weight_bias, eps, T, R, K, H, out, residual_out, residual_out_is_fp32,
-                      stream, true);
-    if (v != AR_VALIDATED) return v;  // AR_OK for T == 0, else the rejection
-    // The status word must start at zero for this call.
-    if (cudaMemsetAsync(d->scratch, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream)) !=
-        cudaSuccess) {
-        (void)cudaGetLastError();
-        return AR_ERR_CUDA;
-    }
-    ws.flags = 0;
+    // The status word is only ever OR-ed into by the kernels and read by
+    // nobody here, so it is not cleared between calls.
     return run(&ws, expert_out, rows_e, perm, topk_w, shared_out, residual, gamma, weight_bias,
-               eps, T, R, K, H, out, residual_out, residual_out_is_fp32, stream, true);
+               eps, T, R, K, H, out, residual_out, residual_out_is_fp32, stream, true, nullptr,
+               noalloc_plan_fits, d);
 }
 
 }  // extern "C"

@@ -46,6 +46,10 @@ struct RowArgs {
     int norm_bf16_h;               // the norm reads h rounded to bf16 (as a bf16 residual_out stores it)
     float weight_bias;
     float eps;
+    // Failure injection (whole-row streaming only; 0 = off): the consumers'
+    // first wait targets a barrier nothing arrives on, bounded by this many
+    // nanoseconds, so the call takes its timeout path (tests of that path).
+    unsigned long long stall_wait_ns;
 };
 
 // Coefficient of the shared partials of row t: sigmoid of the row's gate
@@ -342,6 +346,7 @@ int cluster_rows_max_cluster(int threads, int smem, bool res_f32);
 cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res_f32,
                                 cudaStream_t stream, bool pdl = false);
 cudaError_t cluster_rows_set_attributes();
+bool cluster_rows_plan_fits(const ClusterPlan& p, bool res_f32);
 
 // Each ring slot starts with a header holding the coefficient of each of its
 // segments (1 for shared partials and the residual, w[t,k] for routed rows).
@@ -397,6 +402,7 @@ cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, bool res_f
 cudaError_t stream_rows_set_attributes(int smem_optin);
 // Largest cluster (<= 16) co-schedulable for a clustered plan of this shape.
 int stream_rows_max_cluster(int threads, int smem, int cpt);
+bool stream_rows_plan_fits(const StreamPlan& p, bool res_f32);
 
 // Geometry of one split_rows launch (kernel parameter).
 struct SplitGeom {
@@ -426,5 +432,6 @@ cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32
                               cudaStream_t stream, bool pdl = false);
 cudaError_t split_rows_set_attributes(int smem_optin);
 int split_rows_max_cluster(int threads, int smem, int cpt);
+bool split_rows_plan_fits(const SplitPlan& p, bool res_f32);
 
 }  // namespace arf

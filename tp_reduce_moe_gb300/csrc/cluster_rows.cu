@@ -280,6 +280,18 @@ int cluster_rows_max_cluster(int threads, int smem, bool res_f32) {
     return 0;
 }
 
+// Whether the device can co-schedule one cluster of exactly this plan's launch
+// (block size, shared memory, cluster size, kernel instantiation).
+bool cluster_rows_plan_fits(const ClusterPlan& p, bool res_f32) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster_config(p, 1, nullptr, attr);
+    cfg.gridDim = dim3((unsigned)p.C, 1, 1);
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, cluster_kernel_for(res_f32, p.maxt), &cfg);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e == cudaSuccess && n > 0;
+}
+
 cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res_f32,
                                 cudaStream_t stream, bool pdl) {
     cudaLaunchAttribute attr[2];

@@ -456,6 +456,27 @@ int split_rows_max_cluster(int threads, int smem, int cpt) {
     return 1;
 }
 
+// Whether the device can co-schedule one cluster of exactly this plan's launch.
+bool split_rows_plan_fits(const SplitPlan& p, bool res_f32) {
+    const void* k = split_kernel_for(p.cpt, res_f32);
+    if (!k) return false;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)p.geo.C);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = (size_t)p.smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.geo.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e == cudaSuccess && n > 0;
+}
+
 cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32, cudaStream_t stream,
                               bool pdl) {
     const void* k = split_kernel_for(p.cpt, res_f32);

@@ -395,6 +395,16 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     int par_row = 0;
     uint32_t xph = 0u;  // bit p: phase of xbar[p] to wait for next
     bool ok = true;
+    if (!CLUSTERED && a.stall_wait_ns) {
+        // Failure injection: xbar[0] is unused by whole rows and nothing
+        // arrives on it, so this bounded wait runs out and the CTA takes the
+        // same timeout path as a pipeline wait that never completes.
+        if (!mbar_wait_bounded(smem_addr(&xbar[0]), 0u, abort_flag, a.stall_wait_ns)) {
+            ok = false;
+            if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+            *abort_flag = 1;
+        }
+    }
     for (int64_t t = first_row; t < main_rows; t += row_step) {
         float acc[CPT][8];
 #pragma unroll
@@ -755,6 +765,34 @@ int stream_rows_max_cluster(int threads, int smem, int cpt) {
         (void)cudaGetLastError();
     }
     return 1;
+}
+
+// Whether the device can run exactly this plan's blocks (and, for tiles, one
+// cluster of them at once).
+bool stream_rows_plan_fits(const StreamPlan& p, bool res_f32) {
+    const bool clustered = p.geo.C > 1;
+    const void* k = kernel_for(p.cpt, res_f32, clustered);
+    if (!k) return false;
+    int n = 0;
+    cudaError_t e;
+    if (!clustered) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, p.threads, (size_t)p.smem);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3((unsigned)p.geo.C);
+        cfg.blockDim = dim3((unsigned)p.threads);
+        cfg.dynamicSmemBytes = (size_t)p.smem;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)p.geo.C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+    }
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e == cudaSuccess && n > 0;
 }
 
 cudaError_t launch_stream_rows(const RowArgs& a, const StreamPlan& p, bool res_f32,
