@@ -12,7 +12,7 @@
 #include <cstdlib>
 using namespace arf;
 int main() {
-  long checks = 0, fails = 0;
+  long checks = 0, fails = 0, n64 = 0;
   int Hs[] = {8, 56, 256, 264, 2048, 6144, 7168, 8192, 12296, 16384};
   int Rs[] = {1, 2, 3, 8, 16};
   int Ks[] = {0, 1, 2, 5, 8, 10, 16};
@@ -128,6 +128,21 @@ int main() {
     if ((long)p.nch * p.C < chunks || p.nch > chunks) bad = true;                // every chunk has a CTA
     if ((long)p.G * p.maxt < NT || (p.maxt != 2 && p.maxt != 8)) bad = true;     // every term has a load slot
     if (p.smem != (p.G - 1) * 2 * p.nch * 16) bad = true;
+    // the 64-register form: chosen only for eight-load plans of at most 512
+    // threads that do not fit one wave of the 80-register form (register
+    // counts 80 and 64, 65536 registers and 2048 threads per SM)
+    {
+      auto blocks = [&](int regs) {
+        const int warps = (p.threads + 31) / 32;
+        const int by_regs = 65536 / (warps * ((regs * 32 + 255) / 256 * 256));
+        return std::min(by_regs, 2048 / p.threads);
+      };
+      const int b80 = blocks(80), b64 = blocks(64);
+      const bool use64 = oneshot_prefer_64(p, T, 152, b80, b64);
+      if (use64 && (p.maxt != 8 || p.threads > 512 || T * p.C <= (long)b80 * 152 || b64 <= b80)) bad = true;
+      if (!use64 && p.maxt == 8 && p.threads <= 512 && T * p.C > (long)b80 * 152 && b64 > b80) bad = true;
+      if (use64) ++n64;
+    }
     if (bad) { ++fails; if (fails < 20) printf("BAD oneshot H=%d R=%d K=%d sh=%d T=%ld mc=%d\n", H, R, K, sh, T, mc); }
   }
   // show the automatic plans for the workloads
@@ -138,6 +153,20 @@ int main() {
     {"prefill", 8, 10, 8192, true, {512, 2048, 8192, 0}}};
   for (auto& w : ws) for (long T : w.T) { if (!T) break; StreamPlan p; bool ok = plan_stream_rows(w.R, w.K, w.H, w.sh, T, 152, 232448, 16, 0, 0, &p);
       printf("%-8s T=%5ld ok=%d C=%2d tile=%4d cpt=%d thr=%3d nst=%3d P=%2d slot=%5d smem=%6d grid=%4d\n", w.n, T, ok, p.geo.C, p.geo.tile_chunks, p.cpt, p.threads, p.geo.nstages, p.geo.seg_per_stage, p.geo.slot_bytes, p.smem, p.grid); }
+  if (n64 == 0) { ++fails; printf("the 64-register one-shot form is never chosen\n"); }
+  {
+    // eight partials, K = 0, H = 7168: the 80-register form up to one wave,
+    // the 64-register form at T = 128 and 256
+    ClusterPlan p;
+    for (long T : {16L, 128L, 256L}) {
+      if (!plan_cluster_rows(8, 0, 7168, true, 16, T, 152, &p)) { ++fails; continue; }
+      const int warps = (p.threads + 31) / 32;
+      const int b80 = std::min(65536 / (warps * 2560), 2048 / p.threads), b64 = std::min(65536 / (warps * 2048), 2048 / p.threads);
+      const bool use64 = oneshot_prefer_64(p, T, 152, b80, b64);
+      printf("oneshot R=8 K=0 H=7168 T=%ld C=%d threads=%d -> %s\n", T, p.C, p.threads, use64 ? "64-register form" : "80-register form");
+      if (use64 != (T >= 128)) { ++fails; printf("unexpected form at T=%ld\n", T); }
+    }
+  }
   printf("checked %ld plans, %ld bad\n", checks, fails);
   return fails != 0;
 }

@@ -704,3 +704,53 @@ def test_pdl_chain_reads_the_previous_calls_output(cfg, T):
             check_bf16(res[n + 1], ref["h"], f"pdl chain {cfg} T={T} step {n} residual_out")
     finally:
         ws.destroy()
+
+
+# ------------------------------- split kernel with more rows than resident clusters
+@pytest.mark.parametrize("cfg,T,csize", [("dsv3_decode", 64, 16), ("dsv3_decode", 100, 8), ("glm_gemma", 40, 16),
+                                         ("prefill", 30, 16), ("tiny", 1000, 4)])
+def test_split_clusters_loop_over_rows(cfg, T, csize):
+    """When T exceeds the clusters the device runs at once, each cluster of the
+    split kernel loops over rows k, k + n, ... (every barrier one phase per row,
+    the producer reusing the buffers once the row's exchange is done)."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        arf.ar_workspace_set_cluster_size(ws, csize)
+        d = to_dev(inp)
+        for fp32 in (False, True):
+            out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_SPLIT)
+            torch.cuda.synchronize()
+            assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_SPLIT, csize)
+            tag = f"{cfg} T={T} split C={csize} fp32={fp32}"
+            check_bf16(out, ref["out"], tag + " out")
+            if fp32:
+                check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+            else:
+                check_bf16(r_out, ref["h"], tag + " residual_out")
+        # the same call twice gives the same bits (fixed order whatever the grid)
+        a1 = run_gpu(ws, d, fp32=True, regime=arf.AR_REGIME_SPLIT)
+        a2 = run_gpu(ws, d, fp32=True, regime=arf.AR_REGIME_SPLIT)
+        torch.cuda.synchronize()
+        assert torch.equal(a1[0], a2[0]) and torch.equal(a1[1], a2[1])
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
+
+
+# ------------------------ trailing all-reduce of eight partials (K = 0, TP8)
+@pytest.mark.parametrize("T", [16, 128, 256])
+def test_eight_partial_allreduce_both_oneshot_forms(T):
+    """The one-shot kernel's eight-load forms: 80 registers within one wave
+    (T = 16), 64 registers once the launch no longer fits one wave of the
+    80-register form (T = 128, 256; the switch itself is checked on the host)."""
+    from gen import Config
+    cfg = Config("ar8", 77, R=8, K=0, H=7168, Ts=(T,), eps=1e-6, weights="none", has_shared=True)
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        check_all(ws, to_dev(inp), ref, f"R=8 K=0 T={T}", regimes=(arf.AR_REGIME_ONESHOT, arf.AR_REGIME_AUTO))
+    finally:
+        ws.destroy()

@@ -98,6 +98,11 @@ const BuiltinTable kBuiltinTables[] = {
       {64, AR_REGIME_CLUSTER, 8}, {256, AR_REGIME_STREAM, 0}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0)
     {2, 0, 7168, 2, {{192, AR_REGIME_ONESHOT, 0}, {256, AR_REGIME_STREAM, 0}}},
+    // trailing all-reduce + RMSNorm, eight partials (K = 0, TP8): the one-shot
+    // kernel throughout, its 64-register form once a launch no longer fits one
+    // wave of the 80-register form (T = 128 6.5 us, T = 256 11.9 us against
+    // 8.2 and 12.7 us whole-row streaming)
+    {8, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0}}},
 };
 
 bool valid_regime(int r) {
@@ -134,6 +139,45 @@ struct Plans {
     arf::StreamPlan s{};
     arf::SplitPlan x{};
 };
+
+// Resident blocks per SM of a one-shot plan's kernel instantiation, per
+// (device, instantiation, block, shared memory): a host-side occupancy query,
+// cached (fixed size, no allocation).
+struct OccEntry {
+    int key[5];  // device + 1, maxt, res_f32, threads, smem; key[0] == 0: empty
+    int n;
+};
+OccEntry g_occ[64];
+int g_occ_next = 0;
+std::mutex g_occ_mu;
+
+int oneshot_blocks_per_sm(int device, const arf::ClusterPlan& p, bool res_f32) {
+    const int key[5] = {device + 1, p.maxt, res_f32 ? 1 : 0, p.threads, p.smem};
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    for (const OccEntry& e : g_occ)
+        if (std::memcmp(e.key, key, sizeof key) == 0) return e.n;
+    const int n = arf::cluster_rows_blocks_per_sm(p, res_f32);
+    OccEntry& e = g_occ[g_occ_next];
+    std::memcpy(e.key, key, sizeof key);
+    e.n = n;
+    g_occ_next = (g_occ_next + 1) % 64;
+    return n;
+}
+
+// A one-shot launch of eight loads per thread that does not fit one wave of
+// the 80-register form runs the 64-register form when that holds more CTAs
+// (measured for eight partials, K = 0, H = 7168: T = 128 9.1 -> 7.0 us,
+// T = 256 17.2 -> 12.9 us; within one wave the 80-register form is 0.2-0.4 us
+// faster).
+void oneshot_wave_fit(const ar_workspace* ws, arf::ClusterPlan* p, int64_t T, bool res_f32) {
+    if ((ws->flags & AR_WS_DRY_RUN) || p->maxt != 8 || p->threads > 512) return;
+    const int b80 = oneshot_blocks_per_sm(ws->device, *p, res_f32);
+    if (T * p->C <= (int64_t)b80 * ws->num_sms) return;
+    arf::ClusterPlan q = *p;
+    q.maxt = arf::kClusterMaxTerms64;
+    if (arf::oneshot_prefer_64(*p, T, ws->num_sms, b80, oneshot_blocks_per_sm(ws->device, q, res_f32))) *p = q;
+}
+
 
 // Column groups of a split plan (0: the planner's choice).
 int split_groups(const ar_workspace* ws) { return ws->split_groups; }
@@ -313,6 +357,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     // cluster): a plan the device cannot co-schedule is declined here, before
     // anything is launched.
     if (plan_fits && !plan_fits(fits_ctx, regime, pl, res_f32 != 0)) return AR_ERR_UNSUPPORTED;
+    if (regime == AR_REGIME_ONESHOT) oneshot_wave_fit(ws, &pl.c, T, res_f32 != 0);
     const int ctas = regime == AR_REGIME_ONESHOT ? pl.c.C
                      : regime == AR_REGIME_SPLIT ? pl.x.geo.C
                      : regime == AR_REGIME_CLUSTER ? pl.s.geo.C

@@ -115,6 +115,24 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     return v;
 }
 
+// 8- and 16-byte read-only loads issued where they stand: volatile, so the
+// compiler keeps them ahead of the barrier waits that follow instead of
+// sinking them to their first use (a load of data needed only at the end of
+// a row -- gamma -- is requested at kernel start and has long arrived by
+// then).
+__device__ __forceinline__ uint2 ld_early8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_early16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void st_global16(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
@@ -283,8 +301,29 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// Arrive on the cluster barrier without release semantics.  Used right after
+// mbarrier initialisation: fence.mbarrier_init.release.cluster (fence_mbar_init)
+// already makes the initialised barriers visible at cluster scope, and the
+// peers' barrier.cluster.wait acquires; a release arrive here would also wait
+// for every earlier memory operation of the thread (measured on GB300: about
+// 0.5 us at kernel start, on the critical path of every decode call).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// Sum of the C per-CTA partials pushed into `slots`, in rank order (every CTA
+// of a cluster sums the same values in the same order, so all derive the same
+// scale).  Plain loads, issued together: the caller has already waited
+// (acquire) on the barrier that counted the pushes.
+__device__ __forceinline__ float sum_slots(const float* slots, int C) {
+    float v[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) v[r] = r < C ? slots[r] : 0.0f;
+    float total = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+        if (r < C) total += v[r];
+    return total;
 }
 
 __device__ __forceinline__ void cluster_wait_acquire() {
@@ -334,8 +373,10 @@ struct ClusterPlan {
     int G;    // thread groups splitting the term list
     int threads;
     int smem;  // dynamic shared memory bytes
-    int maxt;  // loads per thread the kernel instantiation holds (2, 4 or 8)
+    int maxt;  // loads per thread the kernel instantiation holds: 2, 8, or
+               // kClusterMaxTerms64 (eight in a 64-register form)
 };
+constexpr int kClusterMaxTerms64 = 9;
 
 // Kernel plan for the small-T regime; returns false if (R, K, H, shared) has
 // no launchable plan with a cluster of at most max_c CTAs.  T and the SM count
@@ -347,6 +388,8 @@ cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res
                                 cudaStream_t stream, bool pdl = false);
 cudaError_t cluster_rows_set_attributes();
 bool cluster_rows_plan_fits(const ClusterPlan& p, bool res_f32);
+int cluster_rows_blocks_per_sm(const ClusterPlan& p, bool res_f32);
+bool oneshot_prefer_64(const ClusterPlan& p, int64_t T, int num_sms, int blocks80, int blocks64);
 
 // Each ring slot starts with a header holding the coefficient of each of its
 // segments (1 for shared partials and the residual, w[t,k] for routed rows).

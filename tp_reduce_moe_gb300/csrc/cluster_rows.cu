@@ -30,8 +30,8 @@ constexpr int kClusterMaxThreads = 768;
 // row may be ragged).  blockDim.x = nch * G.  Term q of a thread group:
 // q < nS is shared partial S_q; otherwise e = q - nS selects slot k = e / R
 // of rank r = e % R.
-template <bool RES_F32, int MAXT>
-__global__ void __launch_bounds__(kClusterMaxThreads, MAXT <= 2 ? 2 : 1)
+template <bool RES_F32, int MAXT, int MAX_THREADS, int MIN_BLOCKS>
+__global__ void __launch_bounds__(MAX_THREADS, MIN_BLOCKS)
     cluster_rows_kernel(const __grid_constant__ RowArgs a, int C, int nch, int G) {
     extern __shared__ __align__(16) uint8_t dyn_smem[];
     pdl_trigger();
@@ -66,12 +66,12 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MAXT <= 2 ? 2 : 1)
     }
     if (C > 1) {
         __syncthreads();
-        cluster_arrive_release();
+        cluster_arrive_relaxed();
     }
     pdl_wait();  // no global memory access before this point
     // gamma, requested now (it is needed only at the end)
     uint4 gv = make_uint4(0, 0, 0, 0);
-    if (g == 0 && active) gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + col));
+    if (g == 0 && active) gv = ld_early16(a.gamma + col);
 
     for (int k = tid; k < a.K; k += blockDim.x) {
         s_row[k] = checked_row(a.perm[t * a.K + k], a.rows_e, a.err);
@@ -175,8 +175,7 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MAXT <= 2 ? 2 : 1)
             if (!s_abort) atomicOr(a.err, kErrTimeout);
             s_abort = 1;
         }
-        total = 0.0f;
-        for (int rk = 0; rk < C; ++rk) total += reinterpret_cast<volatile float*>(s_parts)[rk];
+        total = sum_slots(s_parts, C);
     } else {
         total = 0.0f;
         const int nw = (blockDim.x + 31) >> 5;
@@ -229,19 +228,47 @@ bool plan_cluster_rows(int R, int K, int H, bool shared, int max_c, int64_t T, i
     return true;
 }
 
-// The kernel instantiation for (residual_out type, loads per thread).
+// The kernel instantiation for (residual_out type, loads per thread):
+// maxt 2 -- two loads, 40 registers (two blocks of 768 threads per SM);
+// maxt 8 -- eight loads, 80 registers (one block of 768 threads);
+// kClusterMaxTerms64 -- eight loads in 64 registers, blocks of at most 512
+// threads, two per SM (more resident CTAs once a launch no longer fits one
+// wave of the 80-register form; 4 bytes of spills).
 static const void* cluster_kernel_for(bool res_f32, int maxt) {
-    if (maxt == 2) return res_f32 ? reinterpret_cast<const void*>(cluster_rows_kernel<true, 2>)
-                                  : reinterpret_cast<const void*>(cluster_rows_kernel<false, 2>);
+    if (maxt == 2) return res_f32 ? reinterpret_cast<const void*>(cluster_rows_kernel<true, 2, 768, 2>)
+                                  : reinterpret_cast<const void*>(cluster_rows_kernel<false, 2, 768, 2>);
     if (maxt == kClusterMaxTerms)
-        return res_f32 ? reinterpret_cast<const void*>(cluster_rows_kernel<true, kClusterMaxTerms>)
-                       : reinterpret_cast<const void*>(cluster_rows_kernel<false, kClusterMaxTerms>);
+        return res_f32 ? reinterpret_cast<const void*>(cluster_rows_kernel<true, kClusterMaxTerms, 768, 1>)
+                       : reinterpret_cast<const void*>(cluster_rows_kernel<false, kClusterMaxTerms, 768, 1>);
+    if (maxt == kClusterMaxTerms64)
+        return res_f32 ? reinterpret_cast<const void*>(cluster_rows_kernel<true, kClusterMaxTerms, 512, 2>)
+                       : reinterpret_cast<const void*>(cluster_rows_kernel<false, kClusterMaxTerms, 512, 2>);
     return nullptr;
+}
+
+// Whether an eight-load plan for T rows should run the 64-register form,
+// given the resident blocks per SM of each form: only when the launch does
+// not fit one wave of the 80-register form and the 64-register form holds
+// more blocks.
+bool oneshot_prefer_64(const ClusterPlan& p, int64_t T, int num_sms, int blocks80, int blocks64) {
+    if (p.maxt != kClusterMaxTerms || p.threads > 512) return false;
+    return T * p.C > (int64_t)blocks80 * num_sms && blocks64 > blocks80;
+}
+
+// Resident blocks per SM of a plan's kernel instantiation (0 on error).
+int cluster_rows_blocks_per_sm(const ClusterPlan& p, bool res_f32) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cluster_kernel_for(res_f32, p.maxt), p.threads,
+                                                      (size_t)p.smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 cudaError_t cluster_rows_set_attributes() {
     for (int f = 0; f < 2; ++f)
-        for (int maxt : {2, kClusterMaxTerms}) {
+        for (int maxt : {2, kClusterMaxTerms, kClusterMaxTerms64}) {
             cudaError_t e = cudaFuncSetAttribute(cluster_kernel_for(f != 0, maxt),
                                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;

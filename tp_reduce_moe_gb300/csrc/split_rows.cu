@@ -54,11 +54,12 @@ constexpr int kSplitMaxThreads = 32 + kSplitMaxConsumers;
 constexpr int kSplitHeader = 1024;      // barriers, coefficient table, partial sums, flags
 constexpr int kSplitMinGroupChunks = 128;  // automatic column groups: at least 2 KB per copy
 
-// Header layout (bytes): 0 bar[2] (segment loads), 16 rbar (slices received),
-// 24 ssbar (sums of squares received); 32 coef[32] f32; 160 red[32] f32;
-// 288 ss slots [16] f32 (one per source CTA); 352 abort flag; 1024 receive
-// buffer [Cs][tile_chunks*8] f32 (slice of every source CTA's partial row);
-// then the segment buffers at seg_stride, which the partial row
+// Header layout (bytes): 0 bar[3] (segment loads: shared partials and
+// residual, first and second half of the routed rows), 24 rbar (slices
+// received), 32 ssbar (sums of squares received); 64 coef[32] f32; 192
+// red[32] f32; 320 ss slots [16] f32 (one per source CTA); 384 abort flag;
+// 1024 receive buffer [Cs][tile_chunks*8] f32 (slice of every source CTA's
+// partial row); then the segment buffers at seg_stride, which the partial row
 // [group_chunks*8] f32 reuses once the segments are folded in.
 template <int CPT, bool RES_F32>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
@@ -66,12 +67,12 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_trigger();
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* rbar = bar + 2;
-    uint64_t* ssbar = bar + 3;
-    float* coef = reinterpret_cast<float*>(smem + 32);
-    float* red = reinterpret_cast<float*>(smem + 160);
-    float* ss_slots = reinterpret_cast<float*>(smem + 288);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 352);
+    uint64_t* rbar = bar + 3;
+    uint64_t* ssbar = bar + 4;
+    float* coef = reinterpret_cast<float*>(smem + 64);
+    float* red = reinterpret_cast<float*>(smem + 192);
+    float* ss_slots = reinterpret_cast<float*>(smem + 320);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 384);
     float* recv = reinterpret_cast<float*>(smem + kSplitHeader);
     uint8_t* segbuf = smem + kSplitHeader + geo.part_bytes;
     // the CTA's fp32 partial row reuses the segment buffers once every
@@ -96,15 +97,19 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     const int nS = a.has_shared ? a.R : 0;
     const int nsr = nS + 1;                          // shared partials + residual
     const int nseg = nsr + a.R * a.K;
-    // Segments of this CTA: s = cs + i*Cs, i < ns; the first nsr_c need no perm.
+    // Segments of this CTA: s = cs + i*Cs, i < ns; the first nsr_c need no
+    // perm; the routed ones i in [nsr_c, nmid) complete on bar[1], the rest on
+    // bar[2], so the consumers fold the first half while the second lands.
     const int ns = (nseg - cs + Cs - 1) / Cs;
     const int nsr_c = (nsr > cs) ? (nsr - 1 - cs) / Cs + 1 : 0;
+    const int nmid = nsr_c + (ns - nsr_c + 1) / 2;
 
     const int tile = geo.tile_chunks;
     const int ntile_c = min(tile, chunks - cs * tile);  // chunks of this CTA's tile
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&bar[0]), 1);
         mbar_init(smem_addr(&bar[1]), 1);
+        mbar_init(smem_addr(&bar[2]), 1);
         mbar_init(smem_addr(rbar), 1);
         mbar_init(smem_addr(ssbar), 1);
         *abort_flag = 0;
@@ -116,8 +121,24 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     }
     __syncthreads();
     // barrier A, arrive: this CTA's mbarriers exist
-    cluster_arrive_release();
+    cluster_arrive_relaxed();
     pdl_wait();  // no global memory access before this point
+
+    // This CTA's column tile: work item q = one float4 (half a 16-byte bf16
+    // chunk); a consumer thread owns items ci + m*nct (m < CPT, enough since
+    // a tile is at most half the row).  Its gamma is requested now, so that
+    // the load is long done when the row is normalised.
+    const int tile0 = g0 + cs * tile;  // first chunk of this CTA's tile in the row
+    const int ci = threadIdx.x - 32;
+    const int nct = ncw * 32;
+    uint2 gpre[CPT];
+    bool hv[CPT];
+#pragma unroll
+    for (int m = 0; m < CPT; ++m) {
+        const int q = ci + m * nct;
+        hv[m] = warp > 0 && q < 2 * ntile_c;
+        gpre[m] = hv[m] ? ld_early8(a.gamma + (int64_t)tile0 * 8 + (int64_t)q * 4) : make_uint2(0, 0);
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -147,19 +168,18 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         const int64_t row_k = __shfl_sync(0xffffffffu, rowv, k);
         const float w_k = __shfl_sync(0xffffffffu, wv, k);
         if (mine && !is_sr)
-            bulk_g2s(dst, a.E[e % a.R] + row_k * H + col0, row_bytes, smem_addr(&bar[1]), pol);
+            bulk_g2s(dst, a.E[e % a.R] + row_k * H + col0, row_bytes, smem_addr(&bar[i < nmid ? 1 : 2]), pol);
         // 3. coefficients, then arm both barriers (a phase needs lane 0's
         //    arrival as well as the bytes, so it cannot complete early)
         if (mine) coef[i] = is_sr ? (s < nS ? shared_coef(a, t) : 1.0f) : w_k;
         __syncwarp();
         if (lane == 0) {
             if (nsr_c > 0) mbar_arrive_expect_tx(smem_addr(&bar[0]), (uint32_t)nsr_c * row_bytes);
-            if (ns > nsr_c) mbar_arrive_expect_tx(smem_addr(&bar[1]), (uint32_t)(ns - nsr_c) * row_bytes);
+            if (nmid > nsr_c) mbar_arrive_expect_tx(smem_addr(&bar[1]), (uint32_t)(nmid - nsr_c) * row_bytes);
+            if (ns > nmid) mbar_arrive_expect_tx(smem_addr(&bar[2]), (uint32_t)(ns - nmid) * row_bytes);
         }
     } else {
         // ------------------------------------------------------------ consumers
-        const int ci = threadIdx.x - 32;
-        const int nct = ncw * 32;
         float acc[CPT][8];
         bool valid[CPT];
         const uint8_t* src[CPT];  // this thread's chunk in segment 0
@@ -171,9 +191,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             src[m] = segbuf + (size_t)(ci + m * nct) * 16;
         }
         bool ok = true;
-        for (int phase_set = 0; phase_set < 2; ++phase_set) {
-            const int i_begin = phase_set == 0 ? 0 : nsr_c;
-            const int i_end = phase_set == 0 ? nsr_c : ns;
+        for (int phase_set = 0; phase_set < 3; ++phase_set) {
+            const int i_begin = phase_set == 0 ? 0 : phase_set == 1 ? nsr_c : nmid;
+            const int i_end = phase_set == 0 ? nsr_c : phase_set == 1 ? nmid : ns;
             if (i_begin >= i_end) continue;
             if (ok && !mbar_wait_bounded(smem_addr(&bar[phase_set]), 0u, abort_flag)) {
                 ok = false;
@@ -241,17 +261,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     }
 
     // ---- this CTA's column tile: the C received slices summed locally, in
-    // rank order.  Work item q = one float4 (half a 16-byte bf16 chunk); a
-    // consumer thread owns items ci + m*nct (m < CPT, enough since a tile is
-    // at most half the row).
-    const int tile0 = g0 + cs * tile;  // first chunk of this CTA's tile in the row
-    const int ntile = ntile_c;
-    const int ci = threadIdx.x - 32;
-    const int nct = ncw * 32;
+    // rank order.
     const size_t slice = (size_t)tile * 8;  // floats per source slice
     float4 hq[CPT];
-    bool hv[CPT];
-    uint2 gpre[CPT];  // gamma of this thread's items, requested before the exchanges
     float ss = 0.0f;
     bool ok2 = true;
     if (warp > 0 && !mbar_wait_bounded(smem_addr(rbar), 0u, abort_flag)) {
@@ -262,11 +274,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 #pragma unroll
     for (int m = 0; m < CPT; ++m) {
         const int q = ci + m * nct;
-        hv[m] = warp > 0 && q < 2 * ntile;
         hq[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        gpre[m] = make_uint2(0, 0);
         if (!hv[m]) continue;
-        gpre[m] = __ldg(reinterpret_cast<const uint2*>(a.gamma + (int64_t)tile0 * 8 + (int64_t)q * 4));
         const float* src = recv + (size_t)q * 4;
         for (int r = 0; r < Cs; ++r) {
             const float4 x = *reinterpret_cast<const float4*>(src + r * slice);
@@ -309,8 +318,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         }
     }
 
-    float total = 0.0f;
-    for (int r = 0; r < C; ++r) total += reinterpret_cast<volatile float*>(ss_slots)[r];
+    const float total = sum_slots(ss_slots, C);
 
     const float inv = rsqrtf(total / (float)H + a.eps);
     const float wb = a.weight_bias;
@@ -331,7 +339,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     // period, before the CTA may exit.
     if (threadIdx.x == 0 && *abort_flag) {
         if (nsr_c > 0) (void)mbar_wait_bounded(smem_addr(&bar[0]), 0u, nullptr, 10000000ull);
-        if (ns > nsr_c) (void)mbar_wait_bounded(smem_addr(&bar[1]), 0u, nullptr, 10000000ull);
+        if (nmid > nsr_c) (void)mbar_wait_bounded(smem_addr(&bar[1]), 0u, nullptr, 10000000ull);
+        if (ns > nmid) (void)mbar_wait_bounded(smem_addr(&bar[2]), 0u, nullptr, 10000000ull);
         (void)mbar_wait_bounded(smem_addr(rbar), 0u, nullptr, 10000000ull);
         (void)mbar_wait_bounded<true>(smem_addr(ssbar), 0u, nullptr, 10000000ull);
         grace_period(1000000ull);

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     // by the consumers before their first push into a peer and by the
     // producers before they exit -- the producers' first copies do not wait
     // for the peers.
-    if (CLUSTERED) cluster_arrive_release();
+    if (CLUSTERED) cluster_arrive_relaxed();
     pdl_wait();  // no global memory access before this point
 
     if (warp < W) {
@@ -466,9 +466,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
                 *abort_flag = 1;
             }
             xph ^= 1u << par_row;
-            const volatile float* xs = xslot + par_row * kMaxCluster;
-            tot = 0.0f;
-            for (int rk = 0; rk < C; ++rk) tot += xs[rk];
+            tot = sum_slots(xslot + par_row * kMaxCluster, C);
         }
         const float inv = rsqrtf(tot / (float)H + a.eps);
 #pragma unroll
