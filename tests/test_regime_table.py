@@ -142,13 +142,13 @@ def test_get_with_small_capacity(lib_handle=None):
 
 def test_k0_table_selects_oneshot_then_stream():
     """Two partials, K = 0: the one-shot kernel's 40-register variant up to
-    T = 192, whole-row streaming beyond (the built-in table, then the
-    heuristic past 1.5 rows per SM)."""
+    T = 256 (the built-in table), whole-row streaming beyond (the heuristic
+    past 1.5 rows per SM)."""
     s = Shape(2, 0, 7168)
     try:
         assert s.plan(8)[0] == arf.AR_REGIME_ONESHOT
-        assert s.plan(192)[0] == arf.AR_REGIME_ONESHOT
-        assert s.plan(200)[0] == arf.AR_REGIME_STREAM
+        assert s.plan(200)[0] == arf.AR_REGIME_ONESHOT
+        assert s.plan(256)[0] == arf.AR_REGIME_ONESHOT
         assert s.plan(300)[0] == arf.AR_REGIME_STREAM
     finally:
         s.ws.destroy()

@@ -80,28 +80,26 @@ struct BuiltinTable {
 };
 const BuiltinTable kBuiltinTables[] = {
     // DeepSeek-V3 decode, TP8 (H = 7168, top-8)
-    {8, 8, 7168, 5,
-     {{12, AR_REGIME_SPLIT, 16}, {16, AR_REGIME_CLUSTER, 16}, {32, AR_REGIME_CLUSTER, 8},
-      {64, AR_REGIME_CLUSTER, 4}, {256, AR_REGIME_STREAM, 0}}},
+    {8, 8, 7168, 4,
+     {{16, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 4},
+      {256, AR_REGIME_STREAM, 0}}},
     // DeepSeek-V3 decode, TP4
     {4, 8, 7168, 4,
-     {{8, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_SPLIT, 8}, {64, AR_REGIME_CLUSTER, 4},
+     {{4, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_SPLIT, 8}, {64, AR_REGIME_CLUSTER, 4},
       {256, AR_REGIME_STREAM, 0}}},
     // GLM-style decode, TP8 (H = 6144, top-8)
     {8, 8, 6144, 4,
      {{16, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 4},
       {256, AR_REGIME_STREAM, 0}}},
-    // H = 8192, top-10, TP8 (whole rows from T = 48, the last wave's rows split; eight-CTA
-    // tiles measured 5 % faster again at T = 64)
-    {8, 10, 8192, 5,
-     {{12, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {48, AR_REGIME_STREAM, 0},
-      {64, AR_REGIME_CLUSTER, 8}, {256, AR_REGIME_STREAM, 0}}},
+    // H = 8192, top-10, TP8 (eight- and sixteen-CTA tiles within noise at T = 24 and 48)
+    {8, 10, 8192, 3,
+     {{12, AR_REGIME_SPLIT, 16}, {64, AR_REGIME_CLUSTER, 8}, {256, AR_REGIME_STREAM, 0}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0)
-    {2, 0, 7168, 2, {{192, AR_REGIME_ONESHOT, 0}, {256, AR_REGIME_STREAM, 0}}},
+    {2, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0}}},
     // trailing all-reduce + RMSNorm, eight partials (K = 0, TP8): the one-shot
     // kernel throughout, its 64-register form once a launch no longer fits one
-    // wave of the 80-register form (T = 128 6.5 us, T = 256 11.9 us against
-    // 8.2 and 12.7 us whole-row streaming)
+    // wave of the 80-register form (T = 128 6.6 us, T = 256 11.8 us against
+    // 8.2 and 12.4 us whole-row streaming)
     {8, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0}}},
 };
 
@@ -220,19 +218,18 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
     return 0;
 }
 
-// The built-in choice (measured on GB300 with bench.py's sweep):
+// The built-in choice (measured on GB300 with the tuner):
 //  - light rows (at most 8 summands per 16-byte chunk, one load wave per
-//    thread) up to three rows per four SMs (eight partials, K = 0, H = 7168:
-//    5.9 us at T = 96 against 7.4 streaming), and rows of at most 2 summands
-//    (the 40-register variant) up to 1.5 rows per SM: the one-shot kernel;
+//    thread) up to 5/3 rows per SM: the one-shot kernel (two and eight
+//    partials, K = 0, H = 7168: ahead of whole-row streaming to T = 256 with
+//    the 40-register and the 64-register forms);
 //  - heavy rows at small T (one cluster per row in three quarters of the
 //    SMs): the split kernel, fewest bulk copies per CTA;
 //  - otherwise the streaming kernel (tiles over a cluster for small T, whole
 //    rows for large T).
 int plan_heuristic(const ar_workspace* ws, int R, int K, int H, bool shared, int64_t T, Plans* p) {
     const int summands = (shared ? R : 0) + R * K;
-    const bool light = (summands <= 8 && 4 * T <= 3 * (int64_t)ws->num_sms) ||
-                       (summands <= 2 && 2 * T <= 3 * (int64_t)ws->num_sms);
+    const bool light = summands <= 8 && 3 * T <= 5 * (int64_t)ws->num_sms;
     if (light && arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c))
         return AR_REGIME_ONESHOT;
     if (summands > 8 && arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
