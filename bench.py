@@ -75,7 +75,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=8)
+    p.add_argument("--e2e-steps", type=int, default=16)
     p.add_argument("--e2e-streams", type=int, default=1,
                    help="streams the per-step host->device input copies are spread over")
     p.add_argument("--regime", default="auto",

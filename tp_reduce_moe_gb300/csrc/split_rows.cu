@@ -243,15 +243,19 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        named_barrier_sync(1, nct);
     }
+    // The partial row is complete (consumers) and the producer warp, idle
+    // since its copies went out, takes over the cluster traffic: the remote
+    // sends go out from a warp that reads no shared memory afterwards, so the
+    // consumers' next shared-memory reads are not queued behind them.
+    named_barrier_sync(2, blockDim.x);
 
     // ---- barrier A, wait: every peer's receive barrier exists
     __syncwarp();
     cluster_wait_acquire();
     // send slice j of the group's partial row to CTA j of the group (one
     // bulk copy each)
-    if (warp == 1 && lane < Cs) {
+    if (warp == 0 && lane < Cs) {
         const int j = lane;
         const int nj = min(tile, chunks - j * tile);
         const uint32_t peer = (uint32_t)(grp * Cs + j);
@@ -302,20 +306,24 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     if (warp > 0) {
         ss = warp_sum(ss);
         if (lane == 0) red[warp - 1] = ss;
-        named_barrier_sync(1, nct);
-        float tot = 0.0f;
-        for (int w = 0; w < ncw; ++w) tot += red[w];
-        // push this tile's sum of squares into every peer's slot c
-        // (asynchronous remote stores counted on the peer's barrier) -- only
-        // once every slice has arrived, which is what lets the receivers
-        // exit without a cluster barrier
-        if (ci < C && ok2)
-            st_async_remote_f32(map_shared_rank(smem_addr(ss_slots + c), (uint32_t)ci), tot,
-                                map_shared_rank(smem_addr(ssbar), (uint32_t)ci));
-        if (ok2 && !mbar_wait_bounded<true>(smem_addr(ssbar), 0u, abort_flag)) {
-            if (!*abort_flag) atomicOr(a.err, kErrTimeout);
-            *abort_flag = 1;
+    }
+    named_barrier_sync(2, blockDim.x);
+    if (warp == 0) {
+        // the producer warp pushes this tile's sum of squares into every
+        // peer's slot c (asynchronous remote stores counted on the peer's
+        // barrier) -- only once every slice has arrived (the consumers waited
+        // for them before the barrier; a wait that ran out raised the abort
+        // flag), which is what lets the receivers exit without a cluster
+        // barrier
+        if (lane < C && !*abort_flag) {
+            float tot = 0.0f;
+            for (int w = 0; w < ncw; ++w) tot += red[w];
+            st_async_remote_f32(map_shared_rank(smem_addr(ss_slots + c), (uint32_t)lane), tot,
+                                map_shared_rank(smem_addr(ssbar), (uint32_t)lane));
         }
+    } else if (ok2 && !mbar_wait_bounded<true>(smem_addr(ssbar), 0u, abort_flag)) {
+        if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+        *abort_flag = 1;
     }
 
     const float total = sum_slots(ss_slots, C);
