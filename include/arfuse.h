@@ -338,7 +338,12 @@ ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
  * T <= max_tokens.  regime is AR_REGIME_CLUSTER, _STREAM, _ONESHOT or _SPLIT,
  * or AR_REGIME_AUTO for the built-in heuristic over that range; ctas_per_row
  * is 0 (the regime's own choice) or, for the cluster and split regimes,
- * 2..16.  A call past the last rule, or one whose rule has no launch plan for
+ * 2..16; stage_bytes and producer_warps are 0 (the workspace's setting, see
+ * ar_workspace_set_stage_bytes / _set_producer_warps) or, for the cluster and
+ * stream regimes, the ring-slot size (1024..131072) and the producer-warp cap
+ * (1..4) of that rule -- smaller slots and fewer producer warps let more
+ * CTAs of a clustered plan reside per SM, which wins at some T and loses at
+ * others, so the tuner measures them per shape.  A call past the last rule, or one whose rule has no launch plan for
  * it (a cluster size the device cannot co-schedule, a row too long for the
  * split kernel), runs the heuristic.  A regime forced with
  * ar_workspace_set_regime takes precedence over the table.  Every regime
@@ -357,8 +362,10 @@ ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
  */
 typedef struct ar_regime_rule {
     int64_t max_tokens;
-    int32_t regime;        /* AR_REGIME_* */
-    int32_t ctas_per_row;  /* 0, or 2..16 for AR_REGIME_CLUSTER / AR_REGIME_SPLIT */
+    int32_t regime;          /* AR_REGIME_* */
+    int32_t ctas_per_row;    /* 0, or 2..16 for AR_REGIME_CLUSTER / AR_REGIME_SPLIT */
+    int32_t stage_bytes;     /* 0, or 1024..131072 for AR_REGIME_CLUSTER / AR_REGIME_STREAM */
+    int32_t producer_warps;  /* 0, or 1..4 for AR_REGIME_CLUSTER / AR_REGIME_STREAM */
 } ar_regime_rule;
 #define AR_MAX_REGIME_RULES 32
 ARFUSE_API ar_status ar_workspace_set_regime_table(ar_workspace* ws, const ar_regime_rule* rules,

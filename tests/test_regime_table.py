@@ -46,7 +46,7 @@ def dsv3():
 def test_builtin_table_is_installed_for_measured_shapes(dsv3):
     rules = arf.ar_workspace_get_regime_table(dsv3.ws)
     assert len(rules) >= 2
-    assert [t for t, _, _ in rules] == sorted({t for t, _, _ in rules})
+    assert [r[0] for r in rules] == sorted({r[0] for r in rules})
     other = Shape(3, 5, 1024)
     try:
         assert arf.ar_workspace_get_regime_table(other.ws) == []
@@ -107,6 +107,11 @@ def test_forced_regime_takes_precedence(dsv3):
     [(8, arf.AR_REGIME_CLUSTER, 1)],                                 # ctas out of range
     [(8, arf.AR_REGIME_SPLIT, 17)],
     [(t + 1, arf.AR_REGIME_STREAM, 0) for t in range(arf.AR_MAX_REGIME_RULES + 1)],  # too long
+    [(8, arf.AR_REGIME_SPLIT, 16, 32768, 0)],                        # slot size for a regime without a ring
+    [(8, arf.AR_REGIME_ONESHOT, 0, 0, 2)],                           # producer warps likewise
+    [(8, arf.AR_REGIME_CLUSTER, 8, 512, 0)],                         # slot size out of range
+    [(8, arf.AR_REGIME_STREAM, 0, 262144, 0)],
+    [(8, arf.AR_REGIME_CLUSTER, 8, 0, 5)],                           # producer warps out of range
 ])
 def test_invalid_tables_are_rejected_and_keep_the_old_one(dsv3, rules):
     before = arf.ar_workspace_get_regime_table(dsv3.ws)
@@ -117,9 +122,13 @@ def test_invalid_tables_are_rejected_and_keep_the_old_one(dsv3, rules):
 
 
 def test_table_round_trip(dsv3):
-    rules = [(t, arf.AR_REGIME_CLUSTER, 2 << (t % 4)) for t in range(1, arf.AR_MAX_REGIME_RULES + 1)]
+    rules = [(t, arf.AR_REGIME_CLUSTER, 2 << (t % 4), 8192 * (t % 3), t % 5)
+             for t in range(1, arf.AR_MAX_REGIME_RULES + 1)]
     arf.ar_workspace_set_regime_table(dsv3.ws, rules)
     assert arf.ar_workspace_get_regime_table(dsv3.ws) == rules
+    # three-field rules: slot size and producer warps automatic
+    arf.ar_workspace_set_regime_table(dsv3.ws, [(4, arf.AR_REGIME_SPLIT, 8)])
+    assert arf.ar_workspace_get_regime_table(dsv3.ws) == [(4, arf.AR_REGIME_SPLIT, 8, 0, 0)]
 
 
 def test_get_with_small_capacity(lib_handle=None):
@@ -201,9 +210,22 @@ def test_split_column_groups_need_two_ctas_per_group(dsv3):
 def test_eight_partial_allreduce_table_runs_the_one_shot_kernel():
     s = Shape(8, 0, 7168)
     try:
-        assert arf.ar_workspace_get_regime_table(s.ws) == [(256, arf.AR_REGIME_ONESHOT, 0)]
+        assert arf.ar_workspace_get_regime_table(s.ws) == [(256, arf.AR_REGIME_ONESHOT, 0, 0, 0)]
         for T in (1, 64, 128, 256):
             assert s.plan(T)[0] == arf.AR_REGIME_ONESHOT
         assert s.plan(300)[0] == arf.AR_REGIME_STREAM   # past the table: the heuristic
     finally:
         s.ws.destroy()
+
+
+def test_rule_slot_size_and_producers_reach_the_plan(dsv3):
+    """A rule's slot size and producer-warp cap give the same plan as the
+    workspace-wide tuning controls with those values."""
+    arf.ar_workspace_set_regime_table(dsv3.ws, [(64, arf.AR_REGIME_CLUSTER, 4, 24576, 2)])
+    with_rule = dsv3.plan(48)
+    arf.ar_workspace_set_regime_table(dsv3.ws, [])
+    arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_CLUSTER)
+    arf.ar_workspace_set_cluster_size(dsv3.ws, 4)
+    arf.ar_workspace_set_stage_bytes(dsv3.ws, 24576)
+    arf.ar_workspace_set_producer_warps(dsv3.ws, 2)
+    assert dsv3.plan(48) == with_rule == (arf.AR_REGIME_CLUSTER, 4)

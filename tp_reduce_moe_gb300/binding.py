@@ -180,31 +180,35 @@ def ar_workspace_set_stage_bytes(ws: Workspace, nbytes: int) -> None:
 class RegimeRule(ctypes.Structure):
     """One rule of a regime table (``ar_regime_rule``)."""
     _fields_ = [("max_tokens", ctypes.c_int64), ("regime", ctypes.c_int32),
-                ("ctas_per_row", ctypes.c_int32)]
+                ("ctas_per_row", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("producer_warps", ctypes.c_int32)]
 
 
 AR_MAX_REGIME_RULES = 32
 
 
 def ar_workspace_set_regime_table(ws: Workspace, rules) -> None:
-    """Replace the workspace's regime table: ``[(max_tokens, regime, ctas_per_row), ...]``
-    with strictly ascending max_tokens (empty: heuristic only)."""
-    rules = list(rules)
-    arr = (RegimeRule * max(1, len(rules)))(*[RegimeRule(int(t), int(r), int(c)) for t, r, c in rules])
+    """Replace the workspace's regime table: ``[(max_tokens, regime, ctas_per_row
+    [, stage_bytes, producer_warps]), ...]`` with strictly ascending max_tokens
+    (empty: heuristic only); omitted fields are 0 (automatic)."""
+    rules = [tuple(r) + (0,) * (5 - len(r)) for r in rules]
+    arr = (RegimeRule * max(1, len(rules)))(*[RegimeRule(*[int(x) for x in r]) for r in rules])
     _check(load_library().ar_workspace_set_regime_table(ctypes.c_void_p(ws.handle),
                                                         ctypes.cast(arr, ctypes.c_void_p), len(rules)),
            "ar_workspace_set_regime_table")
 
 
 def ar_workspace_get_regime_table(ws: Workspace):
-    """The workspace's regime table as ``[(max_tokens, regime, ctas_per_row), ...]``."""
+    """The workspace's regime table as ``[(max_tokens, regime, ctas_per_row,
+    stage_bytes, producer_warps), ...]``."""
     arr = (RegimeRule * AR_MAX_REGIME_RULES)()
     n = ctypes.c_int(0)
     _check(load_library().ar_workspace_get_regime_table(ctypes.c_void_p(ws.handle),
                                                         ctypes.cast(arr, ctypes.c_void_p),
                                                         AR_MAX_REGIME_RULES, ctypes.byref(n)),
            "ar_workspace_get_regime_table")
-    return [(int(arr[i].max_tokens), int(arr[i].regime), int(arr[i].ctas_per_row))
+    return [(int(arr[i].max_tokens), int(arr[i].regime), int(arr[i].ctas_per_row),
+             int(arr[i].stage_bytes), int(arr[i].producer_warps))
             for i in range(min(n.value, AR_MAX_REGIME_RULES))]
 
 

@@ -70,37 +70,46 @@ Range range_of(const void* p, int64_t bytes) {
 
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
-// Regime tables measured on GB300 (tp_reduce_moe_gb300.tune: every regime and
-// cluster size, L2-cold, T = 1..128, whole-row streaming beyond; ties within
-// noise merged into the neighbouring rule), installed for these shapes at
-// create.
+// Regime tables measured on GB300 (tp_reduce_moe_gb300.tune: every regime,
+// cluster size and ring variant, L2-cold, T = 1..256; ties within noise merged
+// into the neighbouring rule), installed for these shapes at create.
 struct BuiltinTable {
     int R, K, H, n;
-    ar_regime_rule rules[6];
+    ar_regime_rule rules[10];
 };
+// Rules: {max_tokens, regime, ctas_per_row, stage_bytes, producer_warps}.  A
+// clustered rule with 24 KB slots and two producer warps holds more CTAs per
+// SM than the default plan (64 KB slots), which the tuner found faster at
+// T = 48 and 96-192 for these shapes (dsv3 T = 96 24.97 -> 21.17 us, GLM T = 96
+// 23.01 -> 18.39 us, H = 8192 K = 10 T = 48 20.42 -> 14.98 us).
 const BuiltinTable kBuiltinTables[] = {
     // DeepSeek-V3 decode, TP8 (H = 7168, top-8)
-    {8, 8, 7168, 4,
-     {{16, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 4},
-      {256, AR_REGIME_STREAM, 0}}},
+    {8, 8, 7168, 8,
+     {{16, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {192, AR_REGIME_CLUSTER, 4, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // DeepSeek-V3 decode, TP4
-    {4, 8, 7168, 4,
-     {{4, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_SPLIT, 8}, {64, AR_REGIME_CLUSTER, 4},
-      {256, AR_REGIME_STREAM, 0}}},
+    {4, 8, 7168, 8,
+     {{4, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_SPLIT, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 0},
+      {192, AR_REGIME_CLUSTER, 4, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 0}}},
     // GLM-style decode, TP8 (H = 6144, top-8)
-    {8, 8, 6144, 4,
-     {{16, AR_REGIME_SPLIT, 16}, {32, AR_REGIME_CLUSTER, 8}, {64, AR_REGIME_CLUSTER, 4},
-      {256, AR_REGIME_STREAM, 0}}},
-    // H = 8192, top-10, TP8 (eight- and sixteen-CTA tiles within noise at T = 24 and 48)
-    {8, 10, 8192, 3,
-     {{12, AR_REGIME_SPLIT, 16}, {64, AR_REGIME_CLUSTER, 8}, {256, AR_REGIME_STREAM, 0}}},
+    {8, 8, 6144, 8,
+     {{16, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {192, AR_REGIME_CLUSTER, 4, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
+    // H = 8192, top-10, TP8 (eight- and sixteen-CTA tiles within noise at T = 16-32)
+    {8, 10, 8192, 6,
+     {{12, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {64, AR_REGIME_CLUSTER, 4, 24576, 2}, {96, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0)
-    {2, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0}}},
+    {2, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0, 0, 0}}},
     // trailing all-reduce + RMSNorm, eight partials (K = 0, TP8): the one-shot
     // kernel throughout, its 64-register form once a launch no longer fits one
     // wave of the 80-register form (T = 128 6.6 us, T = 256 11.8 us against
     // 8.2 and 12.4 us whole-row streaming)
-    {8, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0}}},
+    {8, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0, 0, 0}}},
 };
 
 bool valid_regime(int r) {
@@ -117,6 +126,11 @@ bool valid_table(const ar_regime_rule* rules, int n) {
         if (r.ctas_per_row != 0) {
             if (r.regime != AR_REGIME_CLUSTER && r.regime != AR_REGIME_SPLIT) return false;
             if (r.ctas_per_row < 2 || r.ctas_per_row > 16) return false;
+        }
+        if (r.stage_bytes != 0 || r.producer_warps != 0) {
+            if (r.regime != AR_REGIME_CLUSTER && r.regime != AR_REGIME_STREAM) return false;
+            if (r.stage_bytes != 0 && (r.stage_bytes < 1024 || r.stage_bytes > 131072)) return false;
+            if (r.producer_warps < 0 || r.producer_warps > 4) return false;
         }
     }
     return true;
@@ -184,7 +198,9 @@ int split_groups(const ar_workspace* ws) { return ws->split_groups; }
 // Returns the regime that will run (a streaming plan reports CLUSTER when its
 // rows are split over a cluster, STREAM otherwise), 0 when there is no plan.
 int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int H, bool shared,
-                int64_t T, Plans* p) {
+                int64_t T, Plans* p, int stage_bytes = 0, int producer_warps = 0) {
+    const int sb = stage_bytes ? stage_bytes : ws->stage_bytes;
+    const int pw = producer_warps ? producer_warps : ws->producer_warps;
     switch (regime) {
         case AR_REGIME_ONESHOT:
             return arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c)
@@ -203,14 +219,13 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
             if (C == 0) {
                 arf::StreamPlan probe{};
                 if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                           ws->max_cluster_stream, 0, ws->stage_bytes, &probe,
-                                           ws->producer_warps))
+                                           ws->max_cluster_stream, 0, sb, &probe, pw))
                     return 0;
                 C = probe.geo.C > 1 ? probe.geo.C : 2;
             }
             if (!arf::plan_stream_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                       ws->max_cluster_stream, C, ws->stage_bytes, &p->s,
-                                       ws->producer_warps, ws->split_ok ? ws->max_tail_parts : 0))
+                                       ws->max_cluster_stream, C, sb, &p->s, pw,
+                                       ws->split_ok ? ws->max_tail_parts : 0))
                 return 0;
             return p->s.geo.C > 1 ? AR_REGIME_CLUSTER : AR_REGIME_STREAM;
         }
@@ -342,7 +357,8 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
             if (T <= ws->table[i].max_tokens) {
                 if (ws->table[i].regime != AR_REGIME_AUTO)
                     regime = plan_regime(ws, ws->table[i].regime, ws->table[i].ctas_per_row, R, K, H,
-                                         shared, T, &pl);
+                                         shared, T, &pl, ws->table[i].stage_bytes,
+                                         ws->table[i].producer_warps);
                 break;
             }
         if (!regime) regime = plan_heuristic(ws, R, K, H, shared, T, &pl);

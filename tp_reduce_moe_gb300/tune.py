@@ -35,10 +35,14 @@ REGIME_NAME = {arf.AR_REGIME_AUTO: "auto", arf.AR_REGIME_CLUSTER: "cluster",
 
 
 def candidates():
-    """Every (regime, ctas_per_row) the library accepts; 0 = its own choice."""
-    out = [(arf.AR_REGIME_STREAM, 0), (arf.AR_REGIME_ONESHOT, 0)]
-    out += [(arf.AR_REGIME_CLUSTER, c) for c in (2, 4, 8, 16)]
-    out += [(arf.AR_REGIME_SPLIT, c) for c in (2, 4, 8, 16)]
+    """Every (regime, ctas_per_row, stage_bytes, producer_warps) timed; 0 = the
+    library's own choice.  The streaming kernels also run with 24 KB ring
+    slots and two producer warps: fewer, smaller slots and fewer threads let
+    more CTAs of a clustered plan reside per SM, which wins at some T."""
+    out = [(arf.AR_REGIME_STREAM, 0, 0, 0), (arf.AR_REGIME_STREAM, 0, 0, 2), (arf.AR_REGIME_ONESHOT, 0, 0, 0)]
+    for c in (2, 4, 8, 16):
+        out += [(arf.AR_REGIME_CLUSTER, c, 0, 0), (arf.AR_REGIME_CLUSTER, c, 24576, 2)]
+    out += [(arf.AR_REGIME_SPLIT, c, 0, 0) for c in (2, 4, 8, 16)]
     return out
 
 
@@ -83,11 +87,15 @@ class _Inputs:
                                     stream=stream, rows_e=self.rows_e)
 
 
-def time_regime(ws, inp: _Inputs, eps: float, regime: int, ctas: int, dev, reps: int = 3):
-    """Median µs per call of one forced (regime, ctas_per_row), or None when the
-    library has no plan for it.  Returns (us, regime_run, ctas_run)."""
+def time_regime(ws, inp: _Inputs, eps: float, regime: int, ctas: int, dev, reps: int = 3,
+                stage_bytes: int = 0, producer_warps: int = 0):
+    """Median µs per call of one forced (regime, ctas_per_row, stage_bytes,
+    producer_warps), or None when the library has no plan for it.  Returns
+    (us, regime_run, ctas_run)."""
     arf.ar_workspace_set_regime(ws, regime)
     arf.ar_workspace_set_cluster_size(ws, ctas)
+    arf.ar_workspace_set_stage_bytes(ws, stage_bytes)
+    arf.ar_workspace_set_producer_warps(ws, producer_warps)
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     try:
@@ -126,8 +134,9 @@ def tune(R: int, K: int, H: int, tokens=DEFAULT_TOKENS, shared: bool = True, eps
          device: int = 0, cands=None, log=None):
     """Time every candidate at every T; returns (rules, points).
 
-    rules: [(max_tokens, regime, ctas_per_row)], consecutive equal winners
-    merged; points: one dict per (T, candidate) with the measured µs.
+    rules: [(max_tokens, regime, ctas_per_row, stage_bytes, producer_warps)],
+    consecutive equal winners merged; points: one dict per (T, candidate) with
+    the measured µs.
     """
     dev = torch.device("cuda", device)
     torch.cuda.set_device(dev)
@@ -139,26 +148,27 @@ def tune(R: int, K: int, H: int, tokens=DEFAULT_TOKENS, shared: bool = True, eps
         inp = _Inputs(R, K, H, T, shared, n_sets, dev)
         ws = arf.ar_workspace_create(R, K, H, T, eps, device=device)
         best = None
-        for regime, ctas in cands:
-            us, ran_regime, ran_ctas = time_regime(ws, inp, eps, regime, ctas, dev)
-            pt = {"T": T, "regime": REGIME_NAME[regime], "ctas_per_row": ctas, "us": us,
-                  "ran": [REGIME_NAME.get(ran_regime, "?"), ran_ctas]}
+        for regime, ctas, sb, pw in cands:
+            us, ran_regime, ran_ctas = time_regime(ws, inp, eps, regime, ctas, dev, stage_bytes=sb,
+                                                   producer_warps=pw)
+            pt = {"T": T, "regime": REGIME_NAME[regime], "ctas_per_row": ctas, "stage_bytes": sb,
+                  "producer_warps": pw, "us": us, "ran": [REGIME_NAME.get(ran_regime, "?"), ran_ctas]}
             points.append(pt)
             if log:
                 log(pt)
             if us is not None and (best is None or us < best[0]):
-                best = (us, regime, ctas)
+                best = (us, regime, ctas, sb, pw)
         ws.destroy()
         del inp
         torch.cuda.empty_cache()
         if best is not None:
-            winners.append((T, best[1], best[2]))
+            winners.append((T,) + best[1:])
     rules = []
-    for T, regime, ctas in winners:
-        if rules and rules[-1][1] == regime and rules[-1][2] == ctas:
-            rules[-1] = (T, regime, ctas)
+    for w in winners:
+        if rules and rules[-1][1:] == w[1:]:
+            rules[-1] = w
         else:
-            rules.append((T, regime, ctas))
+            rules.append(w)
     return rules, points
 
 
@@ -177,7 +187,7 @@ def main(argv=None):
                          shared=shared, eps=args.eps, device=args.device)
     print(json.dumps({"R": args.R, "K": args.K, "H": args.H, "shared": shared,
                       "device": torch.cuda.get_device_name(args.device),
-                      "rules": [[t, REGIME_NAME[r], c] for t, r, c in rules],
+                      "rules": [[t, REGIME_NAME[r], c, sb, pw] for t, r, c, sb, pw in rules],
                       "points": points}))
     return 0
 
