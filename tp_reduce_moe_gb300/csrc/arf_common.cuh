@@ -120,9 +120,21 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // sinking them to their first use (a load of data needed only at the end of
 // a row -- gamma -- is requested at kernel start and has long arrived by
 // then).
+__device__ __forceinline__ uint32_t ld_early4(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ uint2 ld_early8(const void* p) {
     uint2 v;
     asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_early16_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
     return v;
 }
 __device__ __forceinline__ uint4 ld_early16(const void* p) {

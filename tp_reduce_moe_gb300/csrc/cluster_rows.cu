@@ -56,28 +56,13 @@ __global__ void __launch_bounds__(MAX_THREADS, MIN_BLOCKS)
     const int NT = active ? nS + a.R * a.K : 0;
     const int64_t rowoff = t * H + col;
 
-    // The exchange barrier exists (and expects its C pushed sums) before any
-    // peer may push: cluster barrier arrived on here, waited on before the push.
-    if (tid == 0) {
-        mbar_init(smem_addr(&s_bar), 1);
-        s_abort = 0;
-        fence_mbar_init();
-        mbar_arrive_expect_tx(smem_addr(&s_bar), (uint32_t)C * 4u);
-    }
-    if (C > 1) {
-        __syncthreads();
-        cluster_arrive_relaxed();
-    }
+    // Every load that needs no routing metadata -- gamma (needed only at the
+    // end), the routing metadata itself, the shared partials, the residual --
+    // is requested first, with loads the compiler keeps in place, so their
+    // memory round trips overlap the barrier set-up below.
     pdl_wait();  // no global memory access before this point
-    // gamma, requested now (it is needed only at the end)
     uint4 gv = make_uint4(0, 0, 0, 0);
     if (g == 0 && active) gv = ld_early16(a.gamma + col);
-
-    for (int k = tid; k < a.K; k += blockDim.x) {
-        s_row[k] = checked_row(a.perm[t * a.K + k], a.rows_e, a.err);
-        s_w[k] = a.w[t * a.K + k];
-    }
-
     // Pass 1: loads that do not depend on the routing metadata.
     uint4 v[MAXT];
     float coef[MAXT];
@@ -92,7 +77,23 @@ __global__ void __launch_bounds__(MAX_THREADS, MIN_BLOCKS)
     }
     uint4 res = make_uint4(0, 0, 0, 0);
     if (g == 0 && active) res = ld_stream16(a.residual + rowoff);
+
+    // The exchange barrier exists (and expects its C pushed sums) before any
+    // peer may push: cluster barrier arrived on after the block barrier below,
+    // waited on before the push.  The last thread sets it up while threads
+    // k < K wait for the routing metadata.
+    if (tid == (int)blockDim.x - 1) {
+        mbar_init(smem_addr(&s_bar), 1);
+        s_abort = 0;
+        fence_mbar_init();
+        mbar_arrive_expect_tx(smem_addr(&s_bar), (uint32_t)C * 4u);
+    }
+    for (int k = tid; k < a.K; k += blockDim.x) {
+        s_row[k] = checked_row(a.perm[t * a.K + k], a.rows_e, a.err);
+        s_w[k] = a.w[t * a.K + k];
+    }
     __syncthreads();
+    if (C > 1) cluster_arrive_relaxed();
 
     // Pass 2: the routed (gathered) expert rows.
 #pragma unroll

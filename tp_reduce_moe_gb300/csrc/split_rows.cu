@@ -106,6 +106,32 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 
     const int tile = geo.tile_chunks;
     const int ntile_c = min(tile, chunks - cs * tile);  // chunks of this CTA's tile
+    const int tile0 = g0 + cs * tile;  // first chunk of this CTA's tile in the row
+    const int ci = threadIdx.x - 32;
+    const int nct = ncw * 32;
+
+    // The routing metadata (producer lanes k < K) and gamma (consumers, for
+    // this CTA's column tile: work item q = one float4, half a 16-byte bf16
+    // chunk; a consumer thread owns items ci + m*nct, m < CPT, enough since a
+    // tile is at most half the row) are requested first, with loads the
+    // compiler keeps in place: their memory round trips overlap the barrier
+    // set-up below instead of following it.
+    pdl_wait();  // no global memory access before this point
+    int32_t raw = 0;
+    float wv = 0.0f;
+    if (warp == 0 && lane < a.K) {
+        raw = (int32_t)ld_early4(a.perm + t * a.K + lane);
+        wv = __uint_as_float(ld_early4(a.w + t * a.K + lane));
+    }
+    uint2 gpre[CPT];
+    bool hv[CPT];
+#pragma unroll
+    for (int m = 0; m < CPT; ++m) {
+        const int q = ci + m * nct;
+        hv[m] = warp > 0 && q < 2 * ntile_c;
+        gpre[m] = hv[m] ? ld_early8(a.gamma + (int64_t)tile0 * 8 + (int64_t)q * 4) : make_uint2(0, 0);
+    }
+
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&bar[0]), 1);
         mbar_init(smem_addr(&bar[1]), 1);
@@ -122,63 +148,48 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     __syncthreads();
     // barrier A, arrive: this CTA's mbarriers exist
     cluster_arrive_relaxed();
-    pdl_wait();  // no global memory access before this point
 
-    // This CTA's column tile: work item q = one float4 (half a 16-byte bf16
-    // chunk); a consumer thread owns items ci + m*nct (m < CPT, enough since
-    // a tile is at most half the row).  Its gamma is requested now, so that
-    // the load is long done when the row is normalised.
-    const int tile0 = g0 + cs * tile;  // first chunk of this CTA's tile in the row
-    const int ci = threadIdx.x - 32;
-    const int nct = ncw * 32;
-    uint2 gpre[CPT];
-    bool hv[CPT];
-#pragma unroll
-    for (int m = 0; m < CPT; ++m) {
-        const int q = ci + m * nct;
-        hv[m] = warp > 0 && q < 2 * ntile_c;
-        gpre[m] = hv[m] ? ld_early8(a.gamma + (int64_t)tile0 * 8 + (int64_t)q * 4) : make_uint2(0, 0);
-    }
-
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    // A bulk-copy instruction holds the warp that issues it for about a memory
+    // latency, so the two kinds of copies go out from two warps at once: the
+    // first consumer warp issues the perm-independent copies (shared partials
+    // and residual, on bar[0]) before it starts consuming, and the producer
+    // warp the routed rows (on bar[1] and bar[2]) -- the routing metadata has
+    // been in flight since before the barrier set-up.  Each warp writes its
+    // segments' coefficients, then arms its barriers (a phase needs the
+    // arming lane's arrival as well as the bytes, so it cannot complete
+    // early; the arrival publishes the coefficients).
+    if (warp <= 1) {
         const uint64_t pol = l2_evict_first_policy();
         const int i = lane;
         const int s = cs + i * Cs;
-        const bool mine = i < ns;
-        const bool is_sr = mine && i < nsr_c;
         const uint32_t dst = smem_addr(segbuf + (size_t)i * geo.seg_stride);
-        // 1. routing metadata requested first (a bulk-copy instruction
-        //    holds the warp for about a memory latency), then the
-        //    perm-independent copies, at once
-        int32_t raw = 0;
-        float wv = 0.0f;
-        if (lane < a.K) {
-            raw = __ldg(a.perm + t * a.K + lane);
-            wv = __ldg(a.w + t * a.K + lane);
+        if (warp == 1) {
+            if (i < nsr_c) {
+                const uint16_t* src = (s < nS ? a.S[s] + t * H : a.residual + t * H) + col0;
+                bulk_g2s(dst, src, row_bytes, smem_addr(&bar[0]), pol);
+                coef[i] = s < nS ? shared_coef(a, t) : 1.0f;
+            }
+            __syncwarp();
+            if (lane == 0 && nsr_c > 0) mbar_arrive_expect_tx(smem_addr(&bar[0]), (uint32_t)nsr_c * row_bytes);
+        } else {
+            const bool routed = i >= nsr_c && i < ns;
+            const int64_t rowv = lane < a.K ? checked_row(raw, a.rows_e, a.err) : 0;
+            const int e = s - nsr;
+            const int k = routed ? e / a.R : 0;
+            const int64_t row_k = __shfl_sync(0xffffffffu, rowv, k);
+            const float w_k = __shfl_sync(0xffffffffu, wv, k);
+            if (routed) {
+                bulk_g2s(dst, a.E[e % a.R] + row_k * H + col0, row_bytes, smem_addr(&bar[i < nmid ? 1 : 2]), pol);
+                coef[i] = w_k;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (nmid > nsr_c) mbar_arrive_expect_tx(smem_addr(&bar[1]), (uint32_t)(nmid - nsr_c) * row_bytes);
+                if (ns > nmid) mbar_arrive_expect_tx(smem_addr(&bar[2]), (uint32_t)(ns - nmid) * row_bytes);
+            }
         }
-        if (is_sr) {
-            const uint16_t* src = (s < nS ? a.S[s] + t * H : a.residual + t * H) + col0;
-            bulk_g2s(dst, src, row_bytes, smem_addr(&bar[0]), pol);
-        }
-        // 2. routed copies
-        const int64_t rowv = lane < a.K ? checked_row(raw, a.rows_e, a.err) : 0;
-        const int e = s - nsr;
-        const int k = (mine && !is_sr) ? e / a.R : 0;
-        const int64_t row_k = __shfl_sync(0xffffffffu, rowv, k);
-        const float w_k = __shfl_sync(0xffffffffu, wv, k);
-        if (mine && !is_sr)
-            bulk_g2s(dst, a.E[e % a.R] + row_k * H + col0, row_bytes, smem_addr(&bar[i < nmid ? 1 : 2]), pol);
-        // 3. coefficients, then arm both barriers (a phase needs lane 0's
-        //    arrival as well as the bytes, so it cannot complete early)
-        if (mine) coef[i] = is_sr ? (s < nS ? shared_coef(a, t) : 1.0f) : w_k;
-        __syncwarp();
-        if (lane == 0) {
-            if (nsr_c > 0) mbar_arrive_expect_tx(smem_addr(&bar[0]), (uint32_t)nsr_c * row_bytes);
-            if (nmid > nsr_c) mbar_arrive_expect_tx(smem_addr(&bar[1]), (uint32_t)(nmid - nsr_c) * row_bytes);
-            if (ns > nmid) mbar_arrive_expect_tx(smem_addr(&bar[2]), (uint32_t)(ns - nmid) * row_bytes);
-        }
-    } else {
+    }
+    if (warp > 0) {
         // ------------------------------------------------------------ consumers
         float acc[CPT][8];
         bool valid[CPT];
