@@ -20,14 +20,20 @@
 // for G-fold more, smaller copies: measured at DeepSeek-V3 sizes (C = 16,
 // T = 1) 6.3 us with one group, 5.1 us with four.
 //
-//   producer warp: shared partials + residual copies go out at once (they
-//     need no routing metadata) on mbarrier 0; the routed copies follow as
-//     soon as perm arrives, on mbarrier 1; per-segment coefficients go into
-//     a shared-memory table published by the same barrier phases.
-//   consumers: fold the CTA's segments into registers, write the partial row
-//     over the spent segment buffers, send its slices; wait for the Cs slices
-//     of this tile; local sums; push the tile's sum of squares; wait for the
+//   start: the routing metadata and gamma are requested before the barrier
+//     set-up, so their round trips overlap it.
+//   copies: the first consumer warp issues the shared partials + residual
+//     (they need no routing metadata) on mbarrier 0 while the producer warp
+//     issues the routed rows in two halves on mbarriers 1 and 2 (a bulk-copy
+//     instruction holds its warp for about a memory latency, so one warp
+//     issuing both would delay the routed ones); per-segment coefficients go
+//     into a shared-memory table published by the same barrier phases.
+//   consumers: fold the CTA's segments into registers (the first routed half
+//     while the second lands), write the partial row over the spent segment
+//     buffers; wait for the Cs slices of this tile; local sums; wait for the
 //     C sums; normalise; store.
+//   producer warp, afterwards: sends the partial row's slices to the group
+//     peers and the tile's sum of squares to every CTA of the cluster.
 //
 // One cluster barrier (arrived on right after the mbarriers are initialised,
 // waited on just before the first send) keeps peers from signalling a

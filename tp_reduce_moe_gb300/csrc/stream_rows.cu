@@ -178,6 +178,17 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     const int parts = CLUSTERED ? 1 : geo.tail_parts;
     const bool has_part = !CLUSTERED && parts > 1 && (int64_t)blockIdx.x < (a.T - main_rows) * parts;
 
+    // The first row's routing metadata is requested before the barrier
+    // set-up (producer lanes k < K, a load the compiler keeps in place), so
+    // its memory round trip overlaps the set-up.
+    pdl_wait();  // no global memory access before this point
+    int32_t raw_first = 0;
+    float w_first = 0.0f;
+    if (warp < W && lane < a.K && first_row < main_rows) {
+        raw_first = (int32_t)ld_early4(a.perm + first_row * a.K + lane);
+        w_first = __uint_as_float(ld_early4(a.w + first_row * a.K + lane));
+    }
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
@@ -196,7 +207,6 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
     // producers before they exit -- the producers' first copies do not wait
     // for the peers.
     if (CLUSTERED) cluster_arrive_relaxed();
-    pdl_wait();  // no global memory access before this point
 
     if (warp < W) {
         // ----------------------------------------------------------- producers
@@ -213,13 +223,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
         // Routing metadata one row ahead: lane k holds perm[t, k] of the row
         // being issued and has the next row's value in flight (every
         // producer warp keeps its own copy).
-        int32_t raw_next = 0;
-        float w_next = 0.0f;
+        int32_t raw_next = raw_first;
+        float w_next = w_first;
         float gate_next = 0.0f;
-        if (lane < a.K && first_row < main_rows) {
-            raw_next = __ldg(a.perm + first_row * a.K + lane);
-            w_next = __ldg(a.w + first_row * a.K + lane);
-        }
         if (a.shared_gate && first_row < main_rows) gate_next = __ldg(a.shared_gate + first_row);
         int64_t g0 = 0;  // stage number of the row's first stage
         for (int64_t t = first_row; t < main_rows && ok; t += row_step, g0 += nstage_row) {
