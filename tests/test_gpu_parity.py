@@ -754,3 +754,33 @@ def test_eight_partial_allreduce_both_oneshot_forms(T):
         check_all(ws, to_dev(inp), ref, f"R=8 K=0 T={T}", regimes=(arf.AR_REGIME_ONESHOT, arf.AR_REGIME_AUTO))
     finally:
         ws.destroy()
+
+
+# --------------------- regime-table rules with their own ring slots / producer warps
+@pytest.mark.parametrize("cfg,T,ctas", [("dsv3_decode", 48, 8), ("dsv3_decode", 96, 4), ("glm_gemma", 96, 4),
+                                        ("dsv3_decode", 128, 128)])
+def test_builtin_rules_with_ring_variants(cfg, T, ctas):
+    """The built-in tables run 24 KB slots and two producer warps for some
+    clustered rules, and two producer warps for some whole-row rules; those
+    plans meet the oracle like the default ones."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        rules = arf.ar_workspace_get_regime_table(ws)
+        rule = next(r for r in rules if T <= r[0])
+        assert rule[3:] != (0, 0)   # the rule sets its own slot size and/or producer warps
+        for fp32 in (False, True):
+            out, r_out = run_gpu(ws, d, fp32=fp32)
+            torch.cuda.synchronize()
+            assert arf.ar_workspace_last_regime(ws) == (rule[1], ctas)
+            tag = f"{cfg} T={T} rule {rule} fp32={fp32}"
+            check_bf16(out, ref["out"], tag + " out")
+            if fp32:
+                check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+            else:
+                check_bf16(r_out, ref["h"], tag + " residual_out")
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
