@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     cluster_wait_acquire();
     // send slice j of the group's partial row to CTA j of the group (one
     // bulk copy each)
-    if (warp == 0 && lane < Cs) {
+    if (warp == 0 && lane < Cs && !*abort_flag) {  // nothing remote once this CTA has given up
         const int j = lane;
         const int nj = min(tile, chunks - j * tile);
         const uint32_t peer = (uint32_t)(grp * Cs + j);

@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1)
             // the peer's barrier), then wait for all C partials of the row.
             const uint32_t xb = smem_addr(&xbar[par_row]);
             if (ci == 0) mbar_arrive_expect_tx(xb, (uint32_t)C * 4u);
-            if (ci < C) {
+            if (ci < C && !*abort_flag) {  // nothing remote once this CTA has given up
                 const uint32_t mine = smem_addr(&xslot[par_row * kMaxCluster + crank]);
                 st_async_remote_f32(map_shared_rank(mine, (uint32_t)ci), tot, map_shared_rank(xb, (uint32_t)ci));
             }
