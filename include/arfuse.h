@@ -262,8 +262,8 @@ ARFUSE_API ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes);
 /*
  * Cap the producer warps of the streaming kernels (1..4; 0 restores the
  * automatic count, up to four and at most one per ring slot).  Each producer
- * warp fills its own ring slots; a bulk copy holds the warp that issues it
- * for about one memory latency, so more warps keep more slots in flight.
+ * warp fills its own ring slots; the lanes of a bulk-copy instruction are
+ * issued one after another, so more warps keep more slots in flight.
  * Other values are AR_ERR_INVALID_ARG.  A tuning control: results are
  * identical for every value.
  */

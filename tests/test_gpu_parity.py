@@ -757,8 +757,8 @@ def test_eight_partial_allreduce_both_oneshot_forms(T):
 
 
 # --------------------- regime-table rules with their own ring slots / producer warps
-@pytest.mark.parametrize("cfg,T,ctas", [("dsv3_decode", 48, 8), ("dsv3_decode", 96, 4), ("glm_gemma", 96, 4),
-                                        ("dsv3_decode", 128, 128)])
+@pytest.mark.parametrize("cfg,T,ctas", [("dsv3_decode", 48, 8), ("dsv3_decode", 96, 8), ("glm_gemma", 96, 8),
+                                        ("dsv3_decode", 128, 128), ("dsv3_decode", 192, 8)])
 def test_builtin_rules_with_ring_variants(cfg, T, ctas):
     """The built-in tables run 24 KB slots and two producer warps for some
     clustered rules, and two producer warps for some whole-row rules; those
@@ -776,6 +776,34 @@ def test_builtin_rules_with_ring_variants(cfg, T, ctas):
             torch.cuda.synchronize()
             assert arf.ar_workspace_last_regime(ws) == (rule[1], ctas)
             tag = f"{cfg} T={T} rule {rule} fp32={fp32}"
+            check_bf16(out, ref["out"], tag + " out")
+            if fp32:
+                check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+            else:
+                check_bf16(r_out, ref["h"], tag + " residual_out")
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
+
+
+# --------------------- clustered grids capped at the clusters the device co-schedules
+@pytest.mark.parametrize("T,ctas,stage,producers", [(96, 4, 0, 0), (192, 4, 24576, 2), (256, 8, 24576, 2)])
+def test_clustered_grid_capped_at_coresident_clusters(T, ctas, stage, producers):
+    """Clustered streaming plans whose shared-memory estimate asks for more
+    clusters than a GB300 co-schedules (a cluster lives in one GPC) run on a
+    grid capped at the co-resident count, each cluster taking more rows
+    round-robin; the results meet the oracle like any other plan."""
+    inp = make_inputs("dsv3_decode", T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        arf.ar_workspace_set_regime_table(ws, [(T, arf.AR_REGIME_CLUSTER, ctas, stage, producers)])
+        d = to_dev(inp)
+        for fp32 in (False, True):
+            out, r_out = run_gpu(ws, d, fp32=fp32)
+            torch.cuda.synchronize()
+            assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_CLUSTER, ctas)
+            tag = f"dsv3 T={T} tiles C={ctas} slots {stage} producers {producers} fp32={fp32}"
             check_bf16(out, ref["out"], tag + " out")
             if fp32:
                 check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")

@@ -210,9 +210,11 @@ def test_split_column_groups_need_two_ctas_per_group(dsv3):
 def test_eight_partial_allreduce_table_runs_the_one_shot_kernel():
     s = Shape(8, 0, 7168)
     try:
-        assert arf.ar_workspace_get_regime_table(s.ws) == [(256, arf.AR_REGIME_ONESHOT, 0, 0, 0)]
-        for T in (1, 64, 128, 256):
+        assert arf.ar_workspace_get_regime_table(s.ws) == [(192, arf.AR_REGIME_ONESHOT, 0, 0, 0),
+                                                          (256, arf.AR_REGIME_CLUSTER, 8, 24576, 2)]
+        for T in (1, 64, 128, 192):
             assert s.plan(T)[0] == arf.AR_REGIME_ONESHOT
+        assert s.plan(256) == (arf.AR_REGIME_CLUSTER, 8)
         assert s.plan(300)[0] == arf.AR_REGIME_STREAM   # past the table: the heuristic
     finally:
         s.ws.destroy()

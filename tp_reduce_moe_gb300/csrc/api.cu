@@ -80,36 +80,37 @@ struct BuiltinTable {
 // Rules: {max_tokens, regime, ctas_per_row, stage_bytes, producer_warps}.  A
 // clustered rule with 24 KB slots and two producer warps holds more CTAs per
 // SM than the default plan (64 KB slots), which the tuner found faster at
-// T = 48 and 96-192 for these shapes (dsv3 T = 96 24.97 -> 21.17 us, GLM T = 96
-// 23.01 -> 18.39 us, H = 8192 K = 10 T = 48 20.42 -> 14.98 us).
+// T = 48 and 96-192 for these shapes (dsv3 T = 96 22.9 -> 20.5 us with eight-CTA
+// tiles, H = 8192 K = 10 T = 192 54.2 us whole rows -> 48.0 us).
 const BuiltinTable kBuiltinTables[] = {
     // DeepSeek-V3 decode, TP8 (H = 7168, top-8)
     {8, 8, 7168, 8,
      {{16, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
-      {192, AR_REGIME_CLUSTER, 4, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
+      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_CLUSTER, 4, 0, 0}}},
     // DeepSeek-V3 decode, TP4
     {4, 8, 7168, 8,
      {{4, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_SPLIT, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 0},
-      {192, AR_REGIME_CLUSTER, 4, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 0}}},
+      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {192, AR_REGIME_CLUSTER, 4, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // GLM-style decode, TP8 (H = 6144, top-8)
     {8, 8, 6144, 8,
      {{16, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
-      {192, AR_REGIME_CLUSTER, 4, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
-    // H = 8192, top-10, TP8 (eight- and sixteen-CTA tiles within noise at T = 16-32)
-    {8, 10, 8192, 6,
+      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
+    // H = 8192, top-10, TP8 (eight- and sixteen-CTA tiles within noise at T = 13-16)
+    {8, 10, 8192, 8,
      {{12, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 4, 24576, 2}, {96, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {256, AR_REGIME_STREAM, 0, 0, 2}}},
+      {64, AR_REGIME_CLUSTER, 8, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0)
     {2, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0, 0, 0}}},
     // trailing all-reduce + RMSNorm, eight partials (K = 0, TP8): the one-shot
-    // kernel throughout, its 64-register form once a launch no longer fits one
-    // wave of the 80-register form (T = 128 6.6 us, T = 256 11.8 us against
-    // 8.2 and 12.4 us whole-row streaming)
-    {8, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0, 0, 0}}},
+    // kernel to T = 192, its 64-register form once a launch no longer fits one
+    // wave of the 80-register form (T = 128 6.7 us, T = 192 9.8 us against 8.2
+    // and 11.4 us whole-row streaming); eight-CTA tiles at T = 256 (11.0 us
+    // against 11.5 us one-shot)
+    {8, 0, 7168, 2, {{192, AR_REGIME_ONESHOT, 0, 0, 0}, {256, AR_REGIME_CLUSTER, 8, 24576, 2}}},
 };
 
 bool valid_regime(int r) {
@@ -152,28 +153,52 @@ struct Plans {
     arf::SplitPlan x{};
 };
 
-// Resident blocks per SM of a one-shot plan's kernel instantiation, per
-// (device, instantiation, block, shared memory): a host-side occupancy query,
-// cached (fixed size, no allocation).
+// Host-side occupancy queries, cached per (device, query kind, kernel
+// instantiation, block, shared memory, cluster) in a fixed-size table (no
+// allocation): resident blocks per SM of a one-shot plan (kind 0) and
+// co-resident clusters of a clustered streaming plan (kind 1).
 struct OccEntry {
-    int key[5];  // device + 1, maxt, res_f32, threads, smem; key[0] == 0: empty
+    int key[7];  // device + 1, kind, then the kind's fields; key[0] == 0: empty
     int n;
 };
 OccEntry g_occ[64];
 int g_occ_next = 0;
 std::mutex g_occ_mu;
 
-int oneshot_blocks_per_sm(int device, const arf::ClusterPlan& p, bool res_f32) {
-    const int key[5] = {device + 1, p.maxt, res_f32 ? 1 : 0, p.threads, p.smem};
+template <class Query>
+int occ_cached(const int (&key)[7], Query query) {
     std::lock_guard<std::mutex> lock(g_occ_mu);
     for (const OccEntry& e : g_occ)
         if (std::memcmp(e.key, key, sizeof key) == 0) return e.n;
-    const int n = arf::cluster_rows_blocks_per_sm(p, res_f32);
+    const int n = query();
     OccEntry& e = g_occ[g_occ_next];
     std::memcpy(e.key, key, sizeof key);
     e.n = n;
     g_occ_next = (g_occ_next + 1) % 64;
     return n;
+}
+
+int oneshot_blocks_per_sm(int device, const arf::ClusterPlan& p, bool res_f32) {
+    const int key[7] = {device + 1, 0, p.maxt, res_f32 ? 1 : 0, p.threads, p.smem, 0};
+    return occ_cached(key, [&] { return arf::cluster_rows_blocks_per_sm(p, res_f32); });
+}
+
+int stream_active_clusters(int device, const arf::StreamPlan& p, bool res_f32) {
+    const int key[7] = {device + 1, 1, p.cpt, res_f32 ? 1 : 0, p.threads, p.smem, p.geo.C};
+    return occ_cached(key, [&] { return arf::stream_rows_active_clusters(p, res_f32); });
+}
+
+// A clustered streaming plan sizes its grid from shared memory per SM; the
+// device may co-schedule fewer clusters (a cluster lives in one GPC, and the
+// GPCs' SM counts need not be multiples of the cluster size).  The rows go
+// round-robin over the clusters, so clusters beyond the co-resident ones
+// would only start once others finish (measured: dsv3 T = 192, four-CTA
+// tiles with 24 KB slots, 114 planned clusters, the last ones starting
+// 19 us into the launch); the grid is capped at the co-resident count.
+void stream_wave_fit(const ar_workspace* ws, arf::StreamPlan* p, bool res_f32) {
+    if ((ws->flags & AR_WS_DRY_RUN) || p->geo.C < 2) return;
+    const int n = stream_active_clusters(ws->device, *p, res_f32);
+    if (n >= 1 && (int64_t)n * p->geo.C < p->grid) p->grid = n * p->geo.C;
 }
 
 // A one-shot launch of eight loads per thread that does not fit one wave of
@@ -371,6 +396,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     // anything is launched.
     if (plan_fits && !plan_fits(fits_ctx, regime, pl, res_f32 != 0)) return AR_ERR_UNSUPPORTED;
     if (regime == AR_REGIME_ONESHOT) oneshot_wave_fit(ws, &pl.c, T, res_f32 != 0);
+    if (regime == AR_REGIME_CLUSTER) stream_wave_fit(ws, &pl.s, res_f32 != 0);
     const int ctas = regime == AR_REGIME_ONESHOT ? pl.c.C
                      : regime == AR_REGIME_SPLIT ? pl.x.geo.C
                      : regime == AR_REGIME_CLUSTER ? pl.s.geo.C

@@ -458,6 +458,8 @@ cudaError_t stream_rows_set_attributes(int smem_optin);
 // Largest cluster (<= 16) co-schedulable for a clustered plan of this shape.
 int stream_rows_max_cluster(int threads, int smem, int cpt);
 bool stream_rows_plan_fits(const StreamPlan& p, bool res_f32);
+// Clusters of a clustered plan the device co-schedules (0: query failed).
+int stream_rows_active_clusters(const StreamPlan& p, bool res_f32);
 
 // Geometry of one split_rows launch (kernel parameter).
 struct SplitGeom {

@@ -24,10 +24,11 @@
 //     set-up, so their round trips overlap it.
 //   copies: the first consumer warp issues the shared partials + residual
 //     (they need no routing metadata) on mbarrier 0 while the producer warp
-//     issues the routed rows in two halves on mbarriers 1 and 2 (a bulk-copy
-//     instruction holds its warp for about a memory latency, so one warp
-//     issuing both would delay the routed ones); per-segment coefficients go
-//     into a shared-memory table published by the same barrier phases.
+//     issues the routed rows in two halves on mbarriers 1 and 2 (the lanes
+//     of a bulk-copy instruction are issued one after another, 60-160 cycles
+//     each, so one warp issuing both would delay the routed ones);
+//     per-segment coefficients go into a shared-memory table published by
+//     the same barrier phases.
 //   consumers: fold the CTA's segments into registers (the first routed half
 //     while the second lands), write the partial row over the spent segment
 //     buffers; wait for the Cs slices of this tile; local sums; wait for the
@@ -155,8 +156,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     // barrier A, arrive: this CTA's mbarriers exist
     cluster_arrive_relaxed();
 
-    // A bulk-copy instruction holds the warp that issues it for about a memory
-    // latency, so the two kinds of copies go out from two warps at once: the
+    // A bulk-copy instruction holds its warp while its lanes' copies are
+    // issued one after another (60-160 cycles each: ~0.6 us for 16 lanes),
+    // so the two kinds of copies go out from two warps at once: the
     // first consumer warp issues the perm-independent copies (shared partials
     // and residual, on bar[0]) before it starts consuming, and the producer
     // warp the routed rows (on bar[1] and bar[2]) -- the routing metadata has

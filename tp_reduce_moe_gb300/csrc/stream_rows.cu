@@ -10,11 +10,12 @@
 //   * producer warps issue one 1-D bulk async copy per segment
 //     (cp.async.bulk, the TMA engine's untiled form, L2 evict-first), the
 //     copies of one slot from the lanes of one instruction, completion
-//     counted as transaction bytes on the slot's `full` mbarrier.  A bulk
-//     copy holds its issuing warp for about one memory latency (measured on
-//     GB300: ~0.6 us per instruction, whatever its size), so one warp alone
-//     fills one slot per latency; W producer warps take the slots
-//     round-robin and keep W slots in flight;
+//     counted as transaction bytes on the slot's `full` mbarrier.  Issue is
+//     costed per copy, not per byte (measured on GB300: 60-160 cycles a copy
+//     whatever its size from 0.9 to 14 KB, the lanes of one instruction
+//     issued one after another, about one copy per 70 cycles per SM), and
+//     one producer warp alone kept too few slots in flight; W producer warps
+//     take the slots round-robin;
 //   * consumer warps fold each landed slot into fp32 accumulators held in
 //     registers (CPT 16-byte chunks per thread, U segments per step with
 //     their shared-memory loads issued together and no per-segment guards),
@@ -678,9 +679,9 @@ bool plan_stream_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, 
     const int seg_stride = ceil_div(tile * 16, 128) * 128;
     // Segments per slot: enough for a ~64 KB slot, at most one per producer
     // lane, spread evenly over the row.  Bulk copies are issued one slot per
-    // instruction and an instruction costs its warp about a memory latency
-    // whatever its size, so slots are made large (measured on GB300: 64 KB
-    // slots beat 16 KB ones for column tiles as well as whole rows).
+    // instruction and issue costs per copy, not per byte, so slots are made
+    // large (measured on GB300: 64 KB slots beat 16 KB ones for column tiles
+    // as well as whole rows).
     const int target = stage_bytes > 0 ? stage_bytes : 65536;
     int P = target / seg_stride;
     if (P < 1) P = 1;
@@ -769,6 +770,30 @@ int stream_rows_max_cluster(int threads, int smem, int cpt) {
         (void)cudaGetLastError();
     }
     return 1;
+}
+
+// Clusters of a clustered plan the device holds at once (0 if the query
+// fails).
+int stream_rows_active_clusters(const StreamPlan& p, bool res_f32) {
+    const void* k = kernel_for(p.cpt, res_f32, true);
+    if (!k || p.geo.C < 2) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)p.geo.C);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = (size_t)p.smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.geo.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 // Whether the device can run exactly this plan's blocks (and, for tiles, one
