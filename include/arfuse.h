@@ -244,8 +244,9 @@ ARFUSE_API ar_status ar_workspace_set_regime(ar_workspace* ws, int regime);
 
 /*
  * Force the number of CTAs per token row (the cluster size C, 2..16) that
- * AR_REGIME_CLUSTER and AR_REGIME_SPLIT use; 0 restores the automatic choice.  A size that
- * cannot be launched for a call makes that call return AR_ERR_UNSUPPORTED.
+ * AR_REGIME_CLUSTER, AR_REGIME_SPLIT and AR_REGIME_ONESHOT use (one-shot:
+ * a power of two); 0 restores the automatic choice.  A size that cannot be
+ * launched for a call makes that call return AR_ERR_UNSUPPORTED.
  */
 ARFUSE_API ar_status ar_workspace_set_cluster_size(ar_workspace* ws, int ctas_per_row);
 
@@ -337,8 +338,9 @@ ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
  * max_tokens >= 1; a call with T tokens takes the first rule with
  * T <= max_tokens.  regime is AR_REGIME_CLUSTER, _STREAM, _ONESHOT or _SPLIT,
  * or AR_REGIME_AUTO for the built-in heuristic over that range; ctas_per_row
- * is 0 (the regime's own choice) or, for the cluster and split regimes,
- * 2..16; stage_bytes and producer_warps are 0 (the workspace's setting, see
+ * is 0 (the regime's own choice) or, for the cluster, split and one-shot
+ * regimes, 2..16 (one-shot: a power of two, else the rule has no plan);
+ * stage_bytes and producer_warps are 0 (the workspace's setting, see
  * ar_workspace_set_stage_bytes / _set_producer_warps) or, for the cluster and
  * stream regimes, the ring-slot size (1024..131072) and the producer-warp cap
  * (1..4) of that rule -- smaller slots and fewer producer warps let more
@@ -363,7 +365,7 @@ ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
 typedef struct ar_regime_rule {
     int64_t max_tokens;
     int32_t regime;          /* AR_REGIME_* */
-    int32_t ctas_per_row;    /* 0, or 2..16 for AR_REGIME_CLUSTER / AR_REGIME_SPLIT */
+    int32_t ctas_per_row;    /* 0, or 2..16 for AR_REGIME_CLUSTER / _SPLIT / _ONESHOT */
     int32_t stage_bytes;     /* 0, or 1024..131072 for AR_REGIME_CLUSTER / AR_REGIME_STREAM */
     int32_t producer_warps;  /* 0, or 1..4 for AR_REGIME_CLUSTER / AR_REGIME_STREAM */
 } ar_regime_rule;

@@ -812,3 +812,34 @@ def test_clustered_grid_capped_at_coresident_clusters(T, ctas, stage, producers)
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+# --------------------- the one-shot kernel at every cluster size
+@pytest.mark.parametrize("cfg,T", [("ar_only", 1), ("ar_only", 37), ("tiny", 5), ("dsv3_decode", 2)])
+def test_one_shot_every_cluster_size(cfg, T):
+    """A rule or the workspace may fix the one-shot kernel's cluster size
+    (fewer, larger CTAs per row); every power of two meets the oracle."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        d = to_dev(inp)
+        for c in (2, 4, 8, 16):
+            arf.ar_workspace_set_cluster_size(ws, c)
+            for fp32 in (False, True):
+                try:
+                    out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_ONESHOT)
+                except arf.ArfuseError as e:   # more CTAs than 16-byte chunks, or blocks too large
+                    assert e.status == arf.AR_ERR_UNSUPPORTED
+                    continue
+                torch.cuda.synchronize()
+                assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_ONESHOT, c)
+                tag = f"one-shot {cfg} T={T} C={c} fp32={fp32}"
+                check_bf16(out, ref["out"], tag + " out")
+                if fp32:
+                    check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+                else:
+                    check_bf16(r_out, ref["h"], tag + " residual_out")
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()

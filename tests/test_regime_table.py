@@ -103,7 +103,7 @@ def test_forced_regime_takes_precedence(dsv3):
     [(8, arf.AR_REGIME_STREAM, 0), (4, arf.AR_REGIME_SPLIT, 0)],
     [(8, 9, 0)],                                                     # unknown regime
     [(8, arf.AR_REGIME_STREAM, 4)],                                  # ctas for a regime without
-    [(8, arf.AR_REGIME_ONESHOT, 2)],
+    [(8, arf.AR_REGIME_ONESHOT, 17)],
     [(8, arf.AR_REGIME_CLUSTER, 1)],                                 # ctas out of range
     [(8, arf.AR_REGIME_SPLIT, 17)],
     [(t + 1, arf.AR_REGIME_STREAM, 0) for t in range(arf.AR_MAX_REGIME_RULES + 1)],  # too long
@@ -155,9 +155,10 @@ def test_k0_table_selects_oneshot_then_stream():
     past 1.5 rows per SM)."""
     s = Shape(2, 0, 7168)
     try:
-        assert s.plan(8)[0] == arf.AR_REGIME_ONESHOT
-        assert s.plan(200)[0] == arf.AR_REGIME_ONESHOT
-        assert s.plan(256)[0] == arf.AR_REGIME_ONESHOT
+        assert s.plan(8) == (arf.AR_REGIME_ONESHOT, 8)
+        assert s.plan(128) == (arf.AR_REGIME_ONESHOT, 8)
+        assert s.plan(200) == (arf.AR_REGIME_ONESHOT, 4)
+        assert s.plan(256) == (arf.AR_REGIME_ONESHOT, 4)
         assert s.plan(300)[0] == arf.AR_REGIME_STREAM
     finally:
         s.ws.destroy()
@@ -207,14 +208,35 @@ def test_split_column_groups_need_two_ctas_per_group(dsv3):
         dsv3.plan(1)
 
 
+def test_one_shot_cluster_size_from_a_rule_or_the_workspace():
+    """The one-shot kernel takes a rule's (or the workspace's) cluster size
+    when it is a power of two; another size has no one-shot plan: a forced
+    regime declines the call, a table rule falls back to the heuristic."""
+    s = Shape(2, 0, 7168)
+    try:
+        assert s.plan(8) == (arf.AR_REGIME_ONESHOT, 8)               # built-in table
+        arf.ar_workspace_set_regime_table(s.ws, [(16, arf.AR_REGIME_ONESHOT, 4)])
+        assert s.plan(8) == (arf.AR_REGIME_ONESHOT, 4)
+        arf.ar_workspace_set_regime_table(s.ws, [(16, arf.AR_REGIME_ONESHOT, 6)])
+        assert s.plan(8) == (arf.AR_REGIME_ONESHOT, 16)              # no plan for 6: the heuristic
+        arf.ar_workspace_set_regime(s.ws, arf.AR_REGIME_ONESHOT)
+        for c in (2, 4, 8, 16):
+            arf.ar_workspace_set_cluster_size(s.ws, c)
+            assert s.plan(8) == (arf.AR_REGIME_ONESHOT, c)
+        arf.ar_workspace_set_cluster_size(s.ws, 6)
+        with pytest.raises(arf.ArfuseError) as e:
+            s.plan(8)
+        assert e.value.status == arf.AR_ERR_UNSUPPORTED
+    finally:
+        s.ws.destroy()
+
+
 def test_eight_partial_allreduce_table_runs_the_one_shot_kernel():
     s = Shape(8, 0, 7168)
     try:
-        assert arf.ar_workspace_get_regime_table(s.ws) == [(192, arf.AR_REGIME_ONESHOT, 0, 0, 0),
-                                                          (256, arf.AR_REGIME_CLUSTER, 8, 24576, 2)]
-        for T in (1, 64, 128, 192):
-            assert s.plan(T)[0] == arf.AR_REGIME_ONESHOT
-        assert s.plan(256) == (arf.AR_REGIME_CLUSTER, 8)
+        assert arf.ar_workspace_get_regime_table(s.ws) == [(256, arf.AR_REGIME_ONESHOT, 8, 0, 0)]
+        for T in (1, 64, 128, 256):
+            assert s.plan(T) == (arf.AR_REGIME_ONESHOT, 8)
         assert s.plan(300)[0] == arf.AR_REGIME_STREAM   # past the table: the heuristic
     finally:
         s.ws.destroy()

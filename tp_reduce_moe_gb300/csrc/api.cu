@@ -103,14 +103,16 @@ const BuiltinTable kBuiltinTables[] = {
      {{12, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
       {64, AR_REGIME_CLUSTER, 8, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
       {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
-    // trailing all-reduce + RMSNorm, two partials (K = 0)
-    {2, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 0, 0, 0}}},
+    // trailing all-reduce + RMSNorm, two partials (K = 0): the one-shot kernel
+    // in eight-CTA clusters to T = 128, four-CTA ones beyond (smaller clusters
+    // than its plan's coverage rule picks: T = 1 2.77 -> 2.70 us, T = 256
+    // 7.43 -> 7.14 us)
+    {2, 0, 7168, 2, {{128, AR_REGIME_ONESHOT, 8, 0, 0}, {256, AR_REGIME_ONESHOT, 4, 0, 0}}},
     // trailing all-reduce + RMSNorm, eight partials (K = 0, TP8): the one-shot
-    // kernel to T = 192, its 64-register form once a launch no longer fits one
-    // wave of the 80-register form (T = 128 6.7 us, T = 192 9.8 us against 8.2
-    // and 11.4 us whole-row streaming); eight-CTA tiles at T = 256 (11.0 us
-    // against 11.5 us one-shot)
-    {8, 0, 7168, 2, {{192, AR_REGIME_ONESHOT, 0, 0, 0}, {256, AR_REGIME_CLUSTER, 8, 24576, 2}}},
+    // kernel in eight-CTA clusters, its 64-register form once a launch no
+    // longer fits one wave of the 80-register form (T = 128 6.7 us, T = 256
+    // 10.7 us against 8.2 and 12.2 us whole-row streaming)
+    {8, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 8, 0, 0}}},
 };
 
 bool valid_regime(int r) {
@@ -125,7 +127,8 @@ bool valid_table(const ar_regime_rule* rules, int n) {
         if (r.max_tokens < 1 || (i > 0 && r.max_tokens <= rules[i - 1].max_tokens)) return false;
         if (!valid_regime(r.regime)) return false;
         if (r.ctas_per_row != 0) {
-            if (r.regime != AR_REGIME_CLUSTER && r.regime != AR_REGIME_SPLIT) return false;
+            if (r.regime != AR_REGIME_CLUSTER && r.regime != AR_REGIME_SPLIT && r.regime != AR_REGIME_ONESHOT)
+                return false;
             if (r.ctas_per_row < 2 || r.ctas_per_row > 16) return false;
         }
         if (r.stage_bytes != 0 || r.producer_warps != 0) {
@@ -228,7 +231,7 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
     const int pw = producer_warps ? producer_warps : ws->producer_warps;
     switch (regime) {
         case AR_REGIME_ONESHOT:
-            return arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c)
+            return arf::plan_cluster_rows(R, K, H, shared, ws->max_cluster, T, ws->num_sms, &p->c, ctas)
                        ? AR_REGIME_ONESHOT
                        : 0;
         case AR_REGIME_SPLIT:

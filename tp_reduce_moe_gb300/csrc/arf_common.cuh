@@ -393,8 +393,9 @@ constexpr int kClusterMaxTerms64 = 9;
 // Kernel plan for the small-T regime; returns false if (R, K, H, shared) has
 // no launchable plan with a cluster of at most max_c CTAs.  T and the SM count
 // set how many CTAs per row are worth using.
+// force_c > 0: exactly that cluster size (a power of two up to 16), else no plan.
 bool plan_cluster_rows(int R, int K, int H, bool shared, int max_c, int64_t T, int num_sms,
-                       ClusterPlan* p);
+                       ClusterPlan* p, int force_c = 0);
 int cluster_rows_max_cluster(int threads, int smem, bool res_f32);
 cudaError_t launch_cluster_rows(const RowArgs& a, const ClusterPlan& p, bool res_f32,
                                 cudaStream_t stream, bool pdl = false);

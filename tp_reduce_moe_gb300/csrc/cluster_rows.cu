@@ -198,22 +198,30 @@ __global__ void __launch_bounds__(MAX_THREADS, MIN_BLOCKS)
 static int ceil_div_c(int a, int b) { return (a + b - 1) / b; }
 
 bool plan_cluster_rows(int R, int K, int H, bool shared, int max_c, int64_t T, int num_sms,
-                       ClusterPlan* p) {
+                       ClusterPlan* p, int force_c) {
     const int chunks = H / 8;
     const int NT = (shared ? R : 0) + R * K;
     if (NT < 1 || chunks < 1) return false;
     const int G = ceil_div_c(NT, kClusterMaxTerms);
     if (G > kClusterMaxThreads) return false;
-    // Enough CTAs to cover the GPU about twice over.
+    // Enough CTAs to cover the GPU about twice over, unless the caller fixes
+    // the cluster size (a power of two up to 16: fewer, larger CTAs launch
+    // and exchange sooner, which can beat the coverage rule at small T).
     int want = 1;
     while (want < 16 && (int64_t)want * T < 2LL * num_sms) want <<= 1;
+    if (force_c > 0 && (force_c > 16 || (force_c & (force_c - 1)))) return false;
     int best = 0, largest = 0;
     for (int C = 1; C <= 16 && C <= max_c && C <= chunks; C <<= 1) {
         const int nch = ceil_div_c(chunks, C);
         if (nch * G > kClusterMaxThreads) continue;
+        if (force_c > 0) {
+            if (C == force_c) best = C;
+            continue;
+        }
         largest = C;
         if (!best && C >= want) best = C;
     }
+    if (!best && force_c > 0) return false;
     if (!best) best = largest;
     if (!best) return false;
     p->C = best;

@@ -38,8 +38,11 @@ def candidates():
     """Every (regime, ctas_per_row, stage_bytes, producer_warps) timed; 0 = the
     library's own choice.  The streaming kernels also run with 24 KB ring
     slots and two producer warps: fewer, smaller slots and fewer threads let
-    more CTAs of a clustered plan reside per SM, which wins at some T."""
+    more CTAs of a clustered plan reside per SM, which wins at some T.  The
+    one-shot kernel also runs with every cluster size: smaller clusters
+    launch and exchange sooner than the CTA count its plan aims for."""
     out = [(arf.AR_REGIME_STREAM, 0, 0, 0), (arf.AR_REGIME_STREAM, 0, 0, 2), (arf.AR_REGIME_ONESHOT, 0, 0, 0)]
+    out += [(arf.AR_REGIME_ONESHOT, c, 0, 0) for c in (2, 4, 8, 16)]
     for c in (2, 4, 8, 16):
         out += [(arf.AR_REGIME_CLUSTER, c, 0, 0), (arf.AR_REGIME_CLUSTER, c, 24576, 2)]
     out += [(arf.AR_REGIME_SPLIT, c, 0, 0) for c in (2, 4, 8, 16)]
