@@ -271,9 +271,11 @@ ARFUSE_API ar_status ar_workspace_set_stage_bytes(ar_workspace* ws, int bytes);
 ARFUSE_API ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps);
 
 /*
- * Column groups per row of the split kernel (AR_REGIME_SPLIT): 1, 2, 4 or 8;
- * 0 (the default) picks the most groups that leave a plan, each group at least
- * 128 16-byte chunks wide.  With G groups the C CTAs of a row form G groups
+ * Column groups per row of the split kernel (AR_REGIME_SPLIT): 1..8 (a
+ * divisor of the cluster size; the last group may be narrower when G does not
+ * divide the row's 16-byte chunks); 0 (the default) picks the most groups (a
+ * power of two) that leave a plan, each group at least 128 16-byte chunks
+ * wide.  With G groups the C CTAs of a row form G groups
  * of C/G; each group covers 1/G of the row's columns, its CTAs deal the row's
  * segments among themselves (bulk copies of 1/G of a row each) and
  * reduce-scatter only their group's columns, which cuts the distributed-

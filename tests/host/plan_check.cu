@@ -82,9 +82,9 @@ int main() {
   // split plans (one row per cluster, segments dealt round-robin within a
   // column group)
   for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts)
-  for (int G = 1; G <= 8; G *= 2) {
+  for (int G = 1; G <= 8; ++G) {
     if (K == 0 && !sh) continue;
-    for (int Cf = 0; Cf <= 16; Cf = Cf ? Cf * 2 : 2) {
+    for (int Cf = 0; Cf <= 16; Cf = Cf ? Cf + 1 : 2) {
       SplitPlan p;
       if (!plan_split_rows(R, K, H, sh, T, 152, 232448, 16, Cf, &p, G)) continue;
       ++checks;
@@ -117,11 +117,12 @@ int main() {
   }
   // one-shot plans (one cluster per row, every load of a thread in flight)
   for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts)
-  for (int mc = 1; mc <= 16; mc *= 2) {
+  for (int mc = 1; mc <= 16; mc *= 2) for (int fc = 0; fc <= 16; fc = fc ? fc * 2 : 1) {
     if (K == 0 && !sh) continue;
     ClusterPlan p;
-    if (!plan_cluster_rows(R, K, H, sh, mc, T, 152, &p)) continue;
+    if (!plan_cluster_rows(R, K, H, sh, mc, T, 152, &p, fc)) continue;
     ++checks;
+    if (fc && p.C != fc) { ++fails; if (fails < 20) printf("BAD one-shot forced C=%d got %d\n", fc, p.C); }
     const int chunks = H / 8, NT = (sh ? R : 0) + R * K;
     bool bad = false;
     if (p.C < 1 || p.C > mc || p.threads != p.nch * p.G || p.threads > 768) bad = true;

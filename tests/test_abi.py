@@ -381,10 +381,10 @@ def test_split_rows_setter(lib, ws):
 
 
 def test_split_column_groups_setter(lib, ws):
-    for n in (0, 1, 2, 4, 8):
+    for n in range(9):
         arf.ar_workspace_set_split_column_groups(ws, n)
         assert Fake().call(lib, ws) == arf.AR_VALIDATED
-    for n in (-1, 3, 6, 16):
+    for n in (-1, 9, 16):
         with pytest.raises(arf.ArfuseError):
             arf.ar_workspace_set_split_column_groups(ws, n)
     arf.ar_workspace_set_split_column_groups(ws, 0)

@@ -843,3 +843,44 @@ def test_one_shot_every_cluster_size(cfg, T):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+# --------------------- split kernel: cluster sizes and column groups beyond powers of two
+@pytest.mark.parametrize("cfg,T,combos", [
+    ("dsv3_decode", 3, [(9, 3), (12, 3), (10, 2), (15, 5), (15, 3), (6, 2), (14, 2)]),
+    ("glm_gemma", 5, [(9, 3), (12, 4), (12, 6), (10, 2)]),
+    ("prefill", 2, [(9, 3), (12, 3), (10, 5)]),
+    ("tiny", 7, [(6, 3), (9, 3), (12, 6), (10, 5)]),
+])
+def test_split_any_cluster_size_and_groups(cfg, T, combos):
+    """Any cluster size 2..16 with column groups that divide it (ragged group
+    widths included) meets the oracle; a combination whose CTAs would hold
+    more than 32 segments is declined as AR_ERR_UNSUPPORTED."""
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    ran = 0
+    try:
+        d = to_dev(inp)
+        for c, g in combos:
+            arf.ar_workspace_set_cluster_size(ws, c)
+            arf.ar_workspace_set_split_column_groups(ws, g)
+            for fp32 in (False, True):
+                try:
+                    out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_SPLIT)
+                except arf.ArfuseError as e:
+                    assert e.status == arf.AR_ERR_UNSUPPORTED
+                    continue
+                torch.cuda.synchronize()
+                assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_SPLIT, c)
+                ran += 1
+                tag = f"split {cfg} T={T} C={c} G={g} fp32={fp32}"
+                check_bf16(out, ref["out"], tag + " out")
+                if fp32:
+                    check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+                else:
+                    check_bf16(r_out, ref["h"], tag + " residual_out")
+        assert ran > 0
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()

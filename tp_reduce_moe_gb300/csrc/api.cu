@@ -730,7 +730,7 @@ ar_status ar_workspace_set_split_rows(ar_workspace* ws, int max_parts) {
 
 ar_status ar_workspace_set_split_column_groups(ar_workspace* ws, int groups) {
     if (!ws) return AR_ERR_INVALID_ARG;
-    if (groups < 0 || groups > 8 || (groups & (groups - 1))) return AR_ERR_INVALID_ARG;
+    if (groups < 0 || groups > 8) return AR_ERR_INVALID_ARG;
     ws->split_groups = groups;
     return AR_OK;
 }
