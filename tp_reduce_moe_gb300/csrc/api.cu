@@ -81,11 +81,15 @@ struct BuiltinTable {
 // clustered rule with 24 KB slots and two producer warps holds more CTAs per
 // SM than the default plan (64 KB slots), which the tuner found faster at
 // T = 48 and 96-192 for these shapes (dsv3 T = 96 22.9 -> 20.5 us with eight-CTA
-// tiles, H = 8192 K = 10 T = 192 54.2 us whole rows -> 48.0 us).
+// tiles, H = 8192 K = 10 T = 192 54.2 us whole rows -> 48.0 us).  Twelve-CTA
+// split clusters (four groups of three CTAs, 1/4-row copies) win where
+// sixteen-CTA ones would leave most SMs with two CTAs: dsv3 T = 16 7.96 ->
+// 7.54 us, H = 8192 K = 10 T = 8 7.14 -> 6.70 us.
 const BuiltinTable kBuiltinTables[] = {
     // DeepSeek-V3 decode, TP8 (H = 7168, top-8)
-    {8, 8, 7168, 8,
-     {{16, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
+    {8, 8, 7168, 9,
+     {{12, AR_REGIME_SPLIT, 16, 0, 0}, {16, AR_REGIME_SPLIT, 12, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0},
+      {48, AR_REGIME_CLUSTER, 8, 24576, 2},
       {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
       {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_CLUSTER, 4, 0, 0}}},
     // DeepSeek-V3 decode, TP4
@@ -99,8 +103,9 @@ const BuiltinTable kBuiltinTables[] = {
       {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
       {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // H = 8192, top-10, TP8 (eight- and sixteen-CTA tiles within noise at T = 13-16)
-    {8, 10, 8192, 8,
-     {{12, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
+    {8, 10, 8192, 10,
+     {{4, AR_REGIME_SPLIT, 16, 0, 0}, {8, AR_REGIME_SPLIT, 12, 0, 0}, {12, AR_REGIME_SPLIT, 16, 0, 0},
+      {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
       {64, AR_REGIME_CLUSTER, 8, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
       {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0): the one-shot kernel
