@@ -147,14 +147,21 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+HOST_SIDE_MARK = "// ------------------------------------------------------------------ host side"
+
+
 def kernel_source_sha() -> str:
-    """Hash of the streaming kernel's code (comments and blank lines dropped,
-    so an edited comment does not void a traffic capture)."""
+    """Hash of the streaming kernel's device code: stream_rows.cu up to its
+    host-side section, and the device header arf_common.cuh, with comments
+    and blank lines dropped -- so an edited comment or a host-side change
+    (planning, launch, declarations) does not void a traffic capture."""
     import re
     h = hashlib.sha256()
     for name in ("stream_rows.cu", "arf_common.cuh"):
         with open(os.path.join(ROOT, "tp_reduce_moe_gb300", "csrc", name)) as f:
             text = f.read()
+        if name == "stream_rows.cu":
+            text = text[:text.index(HOST_SIDE_MARK)]
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())

@@ -14,7 +14,7 @@
 #include <mutex>
 #include <new>
 
-#include "arf_common.cuh"
+#include "arf_host.h"
 #include "arfuse.h"
 
 struct ar_workspace {

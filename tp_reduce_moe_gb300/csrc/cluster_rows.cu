@@ -18,7 +18,7 @@
 // 1-2 (finalize + shared add + all-reduce folded into the next input RMSNorm,
 // scale gamma + weight_bias); sglang PR #37104 "perf(mtp): fuse trailing TP
 // all-reduce with final RMSNorm", Changes (K = 0 form, residual required).
-#include "arf_common.cuh"
+#include "arf_host.h"
 
 namespace arf {
 

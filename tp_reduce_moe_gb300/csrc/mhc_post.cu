@@ -22,7 +22,7 @@
 // reads all of its chunk's streams before it writes any of them, and no
 // other thread touches that chunk), so the stream loads use the coherent
 // path.
-#include "arf_common.cuh"
+#include "arf_host.h"
 
 namespace arf {
 

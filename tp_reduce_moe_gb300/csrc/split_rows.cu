@@ -51,7 +51,7 @@
 // RMSNorm", Changes.
 #include <algorithm>
 
-#include "arf_common.cuh"
+#include "arf_host.h"
 
 namespace arf {
 

@@ -45,7 +45,7 @@
 // RMSNorm", Changes.
 #include <type_traits>
 
-#include "arf_common.cuh"
+#include "arf_host.h"
 
 namespace arf {
 
