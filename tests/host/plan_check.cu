@@ -20,7 +20,7 @@ int main() {
   for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts) {
     if (K == 0 && !sh) continue;
     for (int sb : {0, 1024, 4096, 16384, 65536, 131072})
-    for (int Cf = 0; Cf <= 16; Cf = Cf ? Cf * 2 : 1) {
+    for (int Cf = 0; Cf <= 16; ++Cf) {
       StreamPlan p;
       const int split = (sb == 0 || sb == 65536) ? 8 : 0;  // split rows of the last wave
       if (!plan_stream_rows(R, K, H, sh, T, 152, 232448, 16, Cf, sb, &p, 0, split)) {

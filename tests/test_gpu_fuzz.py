@@ -3,8 +3,9 @@
 Each case draws (R, K, H, T, shared partials, weight_bias, eps) at random --
 hidden sizes anywhere from one 16-byte chunk to the maximum, ragged against
 every tile and group width -- and runs every kernel regime (forced, and the
-automatic choice), both residual_out types, and the split kernel under
-random column-group counts.  A forced regime with no launch plan for the
+automatic choice), both residual_out types, the split kernel under random
+column-group counts (powers of two or not), and the forced regimes at a
+random cluster size (odd sizes included).  A forced regime with no launch plan for the
 shape must decline cleanly (AR_ERR_UNSUPPORTED, nothing launched).
 Tolerances as in test_gpu_parity.
 """
@@ -37,10 +38,11 @@ def _draw(i):
             break
     wb = rng.choice([0.0, 0.0, 1.0])
     eps = rng.choice([1e-6, 1e-5])
-    groups = rng.choice([0, 1, 2, 4])
+    groups = rng.choice([0, 1, 2, 3, 4, 5, 6])
+    csize = rng.choice([0, 0, 3, 5, 6, 9, 12])
     cfg = Config(f"fuzz{i}", 200 + i, R=R, K=K, H=H, Ts=(T,), eps=eps,
                  weights="softmax" if K > 0 else "none", s_sigma=1.0, has_shared=shared, weight_bias=wb)
-    return cfg, T, groups
+    return cfg, T, groups, csize
 
 
 CASES = [_draw(i) for i in range(N_CASES)]
@@ -66,9 +68,9 @@ def _to_dev(inp):
 
 
 @pytest.mark.parametrize("case", range(N_CASES),
-                         ids=[f"R{c.R}K{c.K}H{c.H}T{t}S{int(c.has_shared)}G{g}" for c, t, g in CASES])
+                         ids=[f"R{c.R}K{c.K}H{c.H}T{t}S{int(c.has_shared)}G{g}C{cs}" for c, t, g, cs in CASES])
 def test_random_shape(case):
-    cfg, T, groups = CASES[case]
+    cfg, T, groups, csize = CASES[case]
     inp = make_inputs(cfg, T, seed=7 + case)
     ref = run_oracle(inp, want_abs=True)
     d = _to_dev(inp)
@@ -76,6 +78,7 @@ def test_random_shape(case):
     ran = 0
     try:
         arf.ar_workspace_set_split_column_groups(ws, groups)
+        arf.ar_workspace_set_cluster_size(ws, csize)
         for regime in REGIMES:
             arf.ar_workspace_set_regime(ws, regime)
             for fp32 in (False, True):

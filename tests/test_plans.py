@@ -1,7 +1,7 @@
 """Host-side check of the streaming kernel's launch plans (no GPU needed).
 
 Compiles tests/host/plan_check.cu -- which includes the kernel source and calls
-its planner -- with nvcc for the host, then runs it over ~640k plans (hidden
+its planner -- with nvcc for the host, then runs it over ~1.1M plans (hidden
 8..16384 including ragged sizes, R 1..16, K 0..16, T 1..8192, every forced
 cluster size, column-group count and slot size).  Any plan whose shared-memory layout, tile split,
 thread coverage or transaction count is out of range fails the test."""
