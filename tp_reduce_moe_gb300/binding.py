@@ -165,7 +165,8 @@ def ar_workspace_set_regime(ws: Workspace, regime: int) -> None:
 
 
 def ar_workspace_set_cluster_size(ws: Workspace, ctas_per_row: int) -> None:
-    """Force the CTAs per row of the cluster regime (2..16); 0 = automatic."""
+    """Force the CTAs per row (2..16) of the cluster, split and one-shot
+    regimes (one-shot: a power of two); 0 = automatic."""
     _check(load_library().ar_workspace_set_cluster_size(ctypes.c_void_p(ws.handle),
                                                         int(ctas_per_row)),
            "ar_workspace_set_cluster_size")
@@ -223,7 +224,8 @@ def ar_workspace_set_split_rows(ws: Workspace, max_parts: int) -> None:
 
 
 def ar_workspace_set_split_column_groups(ws: Workspace, groups: int) -> None:
-    """Column groups per row of the split kernel (1, 2, 4, 8; tuning); 0 = automatic."""
+    """Column groups per row of the split kernel (1..8, a divisor of the
+    cluster size; tuning); 0 = automatic."""
     _check(load_library().ar_workspace_set_split_column_groups(ctypes.c_void_p(ws.handle), int(groups)),
            "ar_workspace_set_split_column_groups")
 
