@@ -6,7 +6,6 @@ rounded to bf16 (the bf16 bar of the main op).  The oracle itself is pinned
 only to this library's reading of hc_post (the pages give no formula), so
 this parity is parity with that reading.
 """
-import numpy as np
 import pytest
 import torch
 

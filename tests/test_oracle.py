@@ -17,7 +17,7 @@ import pytest
 import torch
 
 import oracle
-from gen import CONFIGS, bf16_bits, make_inputs, make_perm_decode_inputs
+from gen import bf16_bits, make_inputs, make_perm_decode_inputs
 from oracle.brute import bf16_bits_to_float, brute_ar_finalize_rmsnorm
 from tests._util import BF16_ATOL, BF16_RTOL, oracle_args, run_oracle
 
