@@ -527,6 +527,11 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
             "api": "tp_reduce_moe_gb300.ar_finalize_rmsnorm"}
 
 
+# Token counts swept beyond each workload's configured ones: the mid-range decode
+# T where the regime tables switch kernels and ring variants.
+SWEEP_EXTRA_T = {"dsv3_decode": (24, 32, 48, 96, 192, 256)}
+
+
 def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate",
               gated=False, pdls=(False,), perm_kind="random"):
     """µs/call vs T for every workload: L2-cold by rotating through disjoint
@@ -540,7 +545,7 @@ def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="r
         if only and name not in only:
             continue
         cfg = CONFIGS[name]
-        for T in cfg.Ts:
+        for T in sorted(set(cfg.Ts) | set(SWEEP_EXTRA_T.get(name, ()))):
             if name == "prefill" and T == HEADLINE[1]:
                 continue
             for regime_name in regimes:
