@@ -758,7 +758,7 @@ def test_eight_partial_allreduce_both_oneshot_forms(T):
 
 # --------------------- regime-table rules with their own ring slots / producer warps
 @pytest.mark.parametrize("cfg,T,ctas", [("dsv3_decode", 48, 8), ("dsv3_decode", 96, 8), ("glm_gemma", 96, 8),
-                                        ("dsv3_decode", 128, 128), ("dsv3_decode", 192, 8)])
+                                        ("dsv3_decode", 128, 128), ("dsv3_decode", 192, 8), ("prefill", 64, 4)])
 def test_builtin_rules_with_ring_variants(cfg, T, ctas):
     """The built-in tables run 24 KB slots and two producer warps for some
     clustered rules, and two producer warps for some whole-row rules; those
@@ -787,7 +787,8 @@ def test_builtin_rules_with_ring_variants(cfg, T, ctas):
 
 
 # --------------------- clustered grids capped at the clusters the device co-schedules
-@pytest.mark.parametrize("T,ctas,stage,producers", [(96, 4, 0, 0), (192, 4, 24576, 2), (256, 8, 24576, 2)])
+@pytest.mark.parametrize("T,ctas,stage,producers", [(96, 4, 0, 0), (192, 4, 24576, 2), (256, 8, 24576, 2),
+                                                     (48, 8, 32768, 2), (64, 4, 49152, 3)])
 def test_clustered_grid_capped_at_coresident_clusters(T, ctas, stage, producers):
     """Clustered streaming plans whose shared-memory estimate asks for more
     clusters than a GB300 co-schedules (a cluster lives in one GPC) run on a

@@ -81,7 +81,9 @@ struct BuiltinTable {
 // clustered rule with 24 KB slots and two producer warps holds more CTAs per
 // SM than the default plan (64 KB slots), which the tuner found faster at
 // T = 48 and 96-192 for these shapes (dsv3 T = 96 22.9 -> 20.5 us with eight-CTA
-// tiles, H = 8192 K = 10 T = 192 54.2 us whole rows -> 48.0 us).  Twelve-CTA
+// tiles, H = 8192 K = 10 T = 192 54.2 us whole rows -> 48.0 us); 32 KB slots
+// with two warps and 48 KB slots with three sit between the two (TP4 T = 96
+// 12.99 -> 12.39 us, H = 8192 K = 10 T = 64 20.4 -> 18.8 us).  Twelve-CTA
 // split clusters (four groups of three CTAs, 1/4-row copies) win where
 // sixteen-CTA ones would leave most SMs with two CTAs: dsv3 T = 16 7.96 ->
 // 7.54 us, H = 8192 K = 10 T = 8 7.14 -> 6.70 us.
@@ -94,9 +96,9 @@ const BuiltinTable kBuiltinTables[] = {
       {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_CLUSTER, 4, 0, 0}}},
     // DeepSeek-V3 decode, TP4
     {4, 8, 7168, 8,
-     {{4, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_SPLIT, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
-      {192, AR_REGIME_CLUSTER, 4, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
+     {{4, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_SPLIT, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 32768, 2},
+      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 32768, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {192, AR_REGIME_CLUSTER, 4, 32768, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // GLM-style decode, TP8 (H = 6144, top-8)
     {8, 8, 6144, 8,
      {{16, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
@@ -106,7 +108,7 @@ const BuiltinTable kBuiltinTables[] = {
     {8, 10, 8192, 10,
      {{4, AR_REGIME_SPLIT, 16, 0, 0}, {8, AR_REGIME_SPLIT, 12, 0, 0}, {12, AR_REGIME_SPLIT, 16, 0, 0},
       {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 8, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {64, AR_REGIME_CLUSTER, 4, 49152, 3}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
       {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0): the one-shot kernel
     // in eight-CTA clusters to T = 128, four-CTA ones beyond (smaller clusters

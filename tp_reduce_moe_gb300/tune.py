@@ -45,6 +45,8 @@ def candidates():
     out += [(arf.AR_REGIME_ONESHOT, c, 0, 0) for c in (2, 4, 8, 16)]
     for c in (2, 4, 8, 16):
         out += [(arf.AR_REGIME_CLUSTER, c, 0, 0), (arf.AR_REGIME_CLUSTER, c, 24576, 2)]
+        if c in (4, 8):  # mid-size slots: two CTAs per SM with deeper rings than 24 KB slots
+            out += [(arf.AR_REGIME_CLUSTER, c, 32768, 2), (arf.AR_REGIME_CLUSTER, c, 49152, 3)]
     # the split kernel also in twelve-CTA clusters (four groups of three): one
     # CTA per SM for more rows than sixteen-CTA clusters allow at T = 8-16
     out += [(arf.AR_REGIME_SPLIT, c, 0, 0) for c in (2, 4, 8, 12, 16)]
