@@ -64,7 +64,7 @@ extern "C" {
 #define ARFUSE_API
 #endif
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define AR_MAX_RANKS 16      /* R: rank partials per call            */
 #define AR_MAX_TOP_K 16      /* K: routed experts per token          */
 #define AR_MAX_HIDDEN 16384  /* H: columns per row (multiple of 8)   */
@@ -73,7 +73,7 @@ typedef enum ar_status {
     AR_OK = 0,
     AR_ERR_INVALID_ARG = 1,  /* NULL / inconsistent / overlapping arguments   */
     AR_ERR_ALIGNMENT = 2,    /* a pointer not 16-byte aligned, or H % 8 != 0   */
-    AR_ERR_UNSUPPORTED = 3,  /* outside this build's limits                   */
+    AR_ERR_UNSUPPORTED = 3,  /* outside the library's limits or launch plans  */
     AR_ERR_CAPACITY = 4,     /* T larger than the workspace's max_tokens       */
     AR_ERR_CUDA = 5,         /* a CUDA runtime call or the launch failed      */
     AR_ERR_DEVICE_CHECK = 6, /* a device-side check fired (see device_error)  */

@@ -767,7 +767,7 @@ const char* ar_status_string(ar_status s) {
         case AR_OK: return "ok";
         case AR_ERR_INVALID_ARG: return "invalid argument";
         case AR_ERR_ALIGNMENT: return "misaligned pointer or hidden size not a multiple of 8";
-        case AR_ERR_UNSUPPORTED: return "outside the limits of this build";
+        case AR_ERR_UNSUPPORTED: return "outside the library's limits";
         case AR_ERR_CAPACITY: return "more tokens than the workspace's max_tokens";
         case AR_ERR_CUDA: return "CUDA runtime error";
         case AR_ERR_DEVICE_CHECK: return "a device-side check fired";
