@@ -253,3 +253,25 @@ def test_rule_slot_size_and_producers_reach_the_plan(dsv3):
     arf.ar_workspace_set_stage_bytes(dsv3.ws, 24576)
     arf.ar_workspace_set_producer_warps(dsv3.ws, 2)
     assert dsv3.plan(48) == with_rule == (arf.AR_REGIME_CLUSTER, 4)
+
+
+@pytest.mark.parametrize("shape", [(8, 8, 7168), (4, 8, 7168), (8, 8, 6144), (8, 10, 8192), (2, 0, 7168),
+                                   (8, 0, 7168)])
+def test_every_builtin_rule_has_its_own_plan(shape):
+    """Every rule of every built-in table plans its own regime (and cluster
+    size, where it names one) at both ends of its token range on a GB300-sized
+    dry-run workspace -- no rule silently falls back to the heuristic."""
+    s = Shape(*shape, max_tokens=256)
+    try:
+        rules = arf.ar_workspace_get_regime_table(s.ws)
+        assert rules, "a built-in table is expected for this shape"
+        lo = 1
+        for max_tokens, regime, ctas, _stage, _producers in rules:
+            for T in (lo, max_tokens):
+                got_regime, got_ctas = s.plan(T)
+                assert got_regime == regime, (shape, T, rules)
+                if ctas and regime != arf.AR_REGIME_STREAM:
+                    assert got_ctas == ctas, (shape, T, rules)
+            lo = max_tokens + 1
+    finally:
+        s.ws.destroy()
