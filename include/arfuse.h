@@ -328,6 +328,12 @@ ARFUSE_API ar_status ar_workspace_inject_wait_timeout(ar_workspace* ws, int64_t 
  * regime); may be NULL. */
 ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
 
+/* CTAs launched by the last launched call (on a dry-run workspace: planned
+ * for the last validated call), 0 before the first one or for NULL.  For a
+ * clustered streaming plan this is the grid after it was capped at the
+ * clusters the device co-schedules (a multiple of the CTAs per row). */
+ARFUSE_API int ar_workspace_last_grid(const ar_workspace* ws);
+
 /*
  * Regime table: the kernel regime (and CTAs per row) that AR_REGIME_AUTO runs
  * at each token count.  The fastest regime depends on T and on the shape, and

@@ -275,3 +275,21 @@ def test_every_builtin_rule_has_its_own_plan(shape):
             lo = max_tokens + 1
     finally:
         s.ws.destroy()
+
+
+def test_last_grid_reports_the_planned_ctas(dsv3):
+    """ar_workspace_last_grid: the CTAs of the last planned call -- T x C for
+    the split and one-shot kernels, the persistent grid for streaming."""
+    assert arf.ar_workspace_last_grid(dsv3.ws) == 0
+    arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_SPLIT)
+    arf.ar_workspace_set_cluster_size(dsv3.ws, 16)
+    assert dsv3.plan(4) == (arf.AR_REGIME_SPLIT, 16)
+    assert arf.ar_workspace_last_grid(dsv3.ws) == 64
+    arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_STREAM)
+    assert dsv3.plan(300) == (arf.AR_REGIME_STREAM, 152)
+    assert arf.ar_workspace_last_grid(dsv3.ws) == 152
+    arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_CLUSTER)
+    arf.ar_workspace_set_cluster_size(dsv3.ws, 4)
+    regime, ctas = dsv3.plan(24)
+    assert (regime, ctas) == (arf.AR_REGIME_CLUSTER, 4)
+    assert arf.ar_workspace_last_grid(dsv3.ws) == 24 * 4      # one cluster per row when that fits

@@ -103,6 +103,8 @@ def load_library(path: str | None = None):
         lib.ar_workspace_set_cluster_size.argtypes = [P, I]
         lib.ar_workspace_last_regime.restype = I
         lib.ar_workspace_last_regime.argtypes = [P, ctypes.POINTER(I)]
+        lib.ar_workspace_last_grid.restype = I
+        lib.ar_workspace_last_grid.argtypes = [P]
         lib.ar_status_string.restype = ctypes.c_char_p
         lib.ar_status_string.argtypes = [I]
         _lib = lib
@@ -249,6 +251,11 @@ def ar_workspace_last_regime(ws: Workspace):
     n = ctypes.c_int(0)
     r = load_library().ar_workspace_last_regime(ctypes.c_void_p(ws.handle), ctypes.byref(n))
     return int(r), int(n.value)
+
+
+def ar_workspace_last_grid(ws: Workspace) -> int:
+    """CTAs launched by the last call (0 before the first)."""
+    return int(load_library().ar_workspace_last_grid(ctypes.c_void_p(ws.handle)))
 
 
 def ar_workspace_device_error(ws: Workspace) -> int:

@@ -39,6 +39,7 @@ struct ar_workspace {
     int split_groups;        // column groups per row of the split kernel; 0: automatic
     int last_regime;
     int last_ctas;
+    int last_grid;
     unsigned long long stall_wait_ns;  // failure injection (whole-row streaming), 0 = off
     int table_n;  // rules in `table` (0: heuristic only)
     ar_regime_rule table[AR_MAX_REGIME_RULES];
@@ -411,10 +412,14 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
                      : regime == AR_REGIME_SPLIT ? pl.x.geo.C
                      : regime == AR_REGIME_CLUSTER ? pl.s.geo.C
                                                    : pl.s.grid;
+    const int grid = regime == AR_REGIME_ONESHOT ? (int)(T * pl.c.C)
+                     : regime == AR_REGIME_SPLIT ? pl.x.grid
+                                                 : pl.s.grid;
 
     if (ws->flags & AR_WS_DRY_RUN) {
         ws->last_regime = regime;
         ws->last_ctas = ctas;
+        ws->last_grid = grid;
         return AR_VALIDATED;
     }
 
@@ -466,6 +471,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     }
     ws->last_regime = regime;
     ws->last_ctas = ctas;
+    ws->last_grid = grid;
     return AR_OK;
 }
 
@@ -503,6 +509,7 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
     ws->producer_warps = 0;
     ws->last_regime = 0;
     ws->last_ctas = 0;
+    ws->last_grid = 0;
     install_builtin_table(ws);
 
     if (flags & AR_WS_DRY_RUN) {
@@ -755,6 +762,8 @@ ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps) {
     ws->producer_warps = warps;
     return AR_OK;
 }
+
+int ar_workspace_last_grid(const ar_workspace* ws) { return ws ? ws->last_grid : 0; }
 
 int ar_workspace_last_regime(const ar_workspace* ws, int* ctas) {
     if (!ws) return 0;
