@@ -529,7 +529,7 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
 
 # Token counts swept beyond each workload's configured ones: the mid-range decode
 # T where the regime tables switch kernels and ring variants.
-SWEEP_EXTRA_T = {"dsv3_decode": (24, 32, 48, 96, 192, 256)}
+SWEEP_EXTRA_T = {"dsv3_decode": (24, 32, 36, 48, 72, 96, 112, 160, 192, 256)}
 
 
 def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate",

@@ -157,7 +157,8 @@ def test_k0_table_selects_oneshot_then_stream():
     try:
         assert s.plan(8) == (arf.AR_REGIME_ONESHOT, 8)
         assert s.plan(128) == (arf.AR_REGIME_ONESHOT, 8)
-        assert s.plan(200) == (arf.AR_REGIME_ONESHOT, 4)
+        assert s.plan(160) == (arf.AR_REGIME_ONESHOT, 4)
+        assert s.plan(200) == (arf.AR_REGIME_ONESHOT, 2)
         assert s.plan(256) == (arf.AR_REGIME_ONESHOT, 4)
         assert s.plan(300)[0] == arf.AR_REGIME_STREAM
     finally:
@@ -234,9 +235,12 @@ def test_one_shot_cluster_size_from_a_rule_or_the_workspace():
 def test_eight_partial_allreduce_table_runs_the_one_shot_kernel():
     s = Shape(8, 0, 7168)
     try:
-        assert arf.ar_workspace_get_regime_table(s.ws) == [(256, arf.AR_REGIME_ONESHOT, 8, 0, 0)]
+        assert arf.ar_workspace_get_regime_table(s.ws) == [(96, arf.AR_REGIME_ONESHOT, 8, 0, 0),
+                                                          (112, arf.AR_REGIME_ONESHOT, 2, 0, 0),
+                                                          (256, arf.AR_REGIME_ONESHOT, 8, 0, 0)]
         for T in (1, 64, 128, 256):
             assert s.plan(T) == (arf.AR_REGIME_ONESHOT, 8)
+        assert s.plan(100) == (arf.AR_REGIME_ONESHOT, 2)
         assert s.plan(300)[0] == arf.AR_REGIME_STREAM   # past the table: the heuristic
     finally:
         s.ws.destroy()

@@ -72,55 +72,62 @@ Range range_of(const void* p, int64_t bytes) {
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
 // Regime tables measured on GB300 (tp_reduce_moe_gb300.tune: every regime,
-// cluster size and ring variant, L2-cold, T = 1..256; ties within noise merged
-// into the neighbouring rule), installed for these shapes at create.
+// cluster size and ring variant, L2-cold, at 28 token counts from 1 to 256; a
+// faster plan replaces the running rule only when it is more than 1.5 %
+// ahead), installed for these shapes at create.
 struct BuiltinTable {
     int R, K, H, n;
-    ar_regime_rule rules[10];
+    ar_regime_rule rules[16];
 };
-// Rules: {max_tokens, regime, ctas_per_row, stage_bytes, producer_warps}.  A
-// clustered rule with 24 KB slots and two producer warps holds more CTAs per
-// SM than the default plan (64 KB slots), which the tuner found faster at
-// T = 48 and 96-192 for these shapes (dsv3 T = 96 22.9 -> 20.5 us with eight-CTA
-// tiles, H = 8192 K = 10 T = 192 54.2 us whole rows -> 48.0 us); 32 KB slots
-// with two warps and 48 KB slots with three sit between the two (TP4 T = 96
-// 12.99 -> 12.39 us, H = 8192 K = 10 T = 64 20.4 -> 18.8 us).  Twelve-CTA
-// split clusters (four groups of three CTAs, 1/4-row copies) win where
-// sixteen-CTA ones would leave most SMs with two CTAs: dsv3 T = 16 7.96 ->
-// 7.54 us, H = 8192 K = 10 T = 8 7.14 -> 6.70 us.
+// Rules: {max_tokens, regime, ctas_per_row, stage_bytes, producer_warps}.
+// Clustered rules with smaller ring slots (24 KB and two producer warps,
+// 32 KB and two, 48 KB and three) hold more CTAs per SM than the default plan
+// (64 KB slots) and win where that plan would run more rows per cluster than
+// needed (dsv3 T = 96 22.9 -> 20.5 us with eight-CTA tiles; H = 8192 K = 10
+// T = 64 20.4 -> 18.8 us with four-CTA tiles and 48 KB slots).  Twelve-CTA
+// split clusters (four groups of three CTAs) win where sixteen-CTA ones would
+// leave most SMs with two CTAs.  The crossovers fall between powers of two:
+// four-CTA tiles at T = 72 are 11-15 % ahead of the plan that wins at T = 96.
 const BuiltinTable kBuiltinTables[] = {
     // DeepSeek-V3 decode, TP8 (H = 7168, top-8)
-    {8, 8, 7168, 9,
-     {{12, AR_REGIME_SPLIT, 16, 0, 0}, {16, AR_REGIME_SPLIT, 12, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0},
-      {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
-      {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_CLUSTER, 4, 0, 0}}},
+    {8, 8, 7168, 10,
+     {{14, AR_REGIME_SPLIT, 16, 0, 0}, {20, AR_REGIME_SPLIT, 12, 0, 0}, {36, AR_REGIME_CLUSTER, 8, 0, 0},
+      {48, AR_REGIME_CLUSTER, 8, 24576, 2}, {72, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {128, AR_REGIME_STREAM, 0, 0, 2}, {160, AR_REGIME_CLUSTER, 4, 24576, 2},
+      {224, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
     // DeepSeek-V3 decode, TP4
-    {4, 8, 7168, 8,
-     {{4, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_SPLIT, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 32768, 2},
-      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 32768, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
-      {192, AR_REGIME_CLUSTER, 4, 32768, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
+    {4, 8, 7168, 9,
+     {{6, AR_REGIME_SPLIT, 16, 0, 0}, {28, AR_REGIME_SPLIT, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 49152, 3},
+      {72, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 4, 32768, 2}, {128, AR_REGIME_STREAM, 0, 0, 0},
+      {192, AR_REGIME_CLUSTER, 4, 32768, 2}, {224, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {256, AR_REGIME_CLUSTER, 4, 0, 0}}},
     // GLM-style decode, TP8 (H = 6144, top-8)
-    {8, 8, 6144, 8,
-     {{16, AR_REGIME_SPLIT, 16, 0, 0}, {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 4, 0, 0}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
-      {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
-    // H = 8192, top-10, TP8 (eight- and sixteen-CTA tiles within noise at T = 13-16)
-    {8, 10, 8192, 10,
-     {{4, AR_REGIME_SPLIT, 16, 0, 0}, {8, AR_REGIME_SPLIT, 12, 0, 0}, {12, AR_REGIME_SPLIT, 16, 0, 0},
-      {32, AR_REGIME_CLUSTER, 8, 0, 0}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {64, AR_REGIME_CLUSTER, 4, 49152, 3}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
-      {192, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_STREAM, 0, 0, 2}}},
-    // trailing all-reduce + RMSNorm, two partials (K = 0): the one-shot kernel
-    // in eight-CTA clusters to T = 128, four-CTA ones beyond (smaller clusters
-    // than its plan's coverage rule picks: T = 1 2.77 -> 2.70 us, T = 256
-    // 7.43 -> 7.14 us)
-    {2, 0, 7168, 2, {{128, AR_REGIME_ONESHOT, 8, 0, 0}, {256, AR_REGIME_ONESHOT, 4, 0, 0}}},
+    {8, 8, 6144, 11,
+     {{20, AR_REGIME_SPLIT, 16, 0, 0}, {36, AR_REGIME_CLUSTER, 8, 0, 0}, {44, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {48, AR_REGIME_CLUSTER, 8, 32768, 2}, {72, AR_REGIME_CLUSTER, 4, 0, 0}, {80, AR_REGIME_CLUSTER, 4, 24576, 2},
+      {96, AR_REGIME_CLUSTER, 8, 32768, 2}, {128, AR_REGIME_STREAM, 0, 0, 2},
+      {160, AR_REGIME_CLUSTER, 4, 24576, 2}, {224, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {256, AR_REGIME_STREAM, 0, 0, 2}}},
+    // H = 8192, top-10, TP8
+    {8, 10, 8192, 13,
+     {{6, AR_REGIME_SPLIT, 16, 0, 0}, {8, AR_REGIME_SPLIT, 12, 0, 0}, {14, AR_REGIME_SPLIT, 16, 0, 0},
+      {20, AR_REGIME_CLUSTER, 16, 24576, 2}, {36, AR_REGIME_CLUSTER, 8, 0, 0},
+      {48, AR_REGIME_CLUSTER, 8, 24576, 2}, {72, AR_REGIME_CLUSTER, 4, 49152, 3},
+      {80, AR_REGIME_CLUSTER, 8, 24576, 2}, {96, AR_REGIME_CLUSTER, 8, 32768, 2},
+      {128, AR_REGIME_CLUSTER, 4, 49152, 3}, {160, AR_REGIME_CLUSTER, 16, 0, 0},
+      {224, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_CLUSTER, 4, 49152, 3}}},
+    // trailing all-reduce + RMSNorm, two partials (K = 0): the one-shot kernel in
+    // smaller clusters than its plan's coverage rule picks (T = 160-256: wave
+    // quantisation of the grid decides between four- and two-CTA clusters)
+    {2, 0, 7168, 4,
+     {{128, AR_REGIME_ONESHOT, 8, 0, 0}, {192, AR_REGIME_ONESHOT, 4, 0, 0}, {224, AR_REGIME_ONESHOT, 2, 0, 0},
+      {256, AR_REGIME_ONESHOT, 4, 0, 0}}},
     // trailing all-reduce + RMSNorm, eight partials (K = 0, TP8): the one-shot
-    // kernel in eight-CTA clusters, its 64-register form once a launch no
-    // longer fits one wave of the 80-register form (T = 128 6.7 us, T = 256
-    // 10.7 us against 8.2 and 12.2 us whole-row streaming)
-    {8, 0, 7168, 1, {{256, AR_REGIME_ONESHOT, 8, 0, 0}}},
+    // kernel in eight-CTA clusters, its 64-register form once a launch no longer
+    // fits one wave of the 80-register form (T = 128 6.6 us, T = 256 10.8 us
+    // against 8.1 and 11.0 us for the best streaming plans)
+    {8, 0, 7168, 3,
+     {{96, AR_REGIME_ONESHOT, 8, 0, 0}, {112, AR_REGIME_ONESHOT, 2, 0, 0}, {256, AR_REGIME_ONESHOT, 8, 0, 0}}},
 };
 
 bool valid_regime(int r) {
