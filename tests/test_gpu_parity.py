@@ -60,9 +60,14 @@ def run_gpu(ws, d, fp32=False, regime=arf.AR_REGIME_AUTO, **kw):
                                    residual_out_fp32=fp32, rows_e=d["rows_e"], **kw)
 
 
-def check_all(ws, d, ref, what, regimes=REGIMES, fp32s=(False, True)):
+def check_all(ws, d, ref, what, regimes=REGIMES, fp32s=(False, True), declines=()):
     for regime in regimes:
         for fp32 in fp32s:
+            if regime in declines:   # no launch plan for this shape: a clean decline
+                with pytest.raises(arf.ArfuseError) as e:
+                    run_gpu(ws, d, fp32=fp32, regime=regime)
+                assert e.value.status == arf.AR_ERR_UNSUPPORTED
+                continue
             if regime in SPLITTING and d["H"] // 8 < 2:
                 with pytest.raises(arf.ArfuseError) as e:   # one chunk cannot be split
                     run_gpu(ws, d, fp32=fp32, regime=regime)
@@ -168,7 +173,12 @@ EDGE = [
     (2, 3, 16384, 20, True),    # maximum hidden (4 chunks per stream consumer)
     (4, 2, 12296, 7, True),     # ragged: 1537 chunks, last consumer warp partial
     (8, 8, 7168, 333, True),    # T not a multiple of the SM count, both kernels
+    (16, 16, 16384, 3, True),   # the heaviest row the library takes: 273 segments of 32 KB
 ]
+# Forced regimes with no launch plan for a shape, which must decline cleanly: at the heaviest row
+# the one-shot kernel would need more than 768 threads per CTA, and the split kernel more than 32
+# segments per CTA or more shared memory than an SM has.
+EDGE_DECLINES = {(16, 16, 16384, 3, True): (arf.AR_REGIME_ONESHOT, arf.AR_REGIME_SPLIT)}
 
 
 @pytest.mark.parametrize("R,K,H,T,shared", EDGE, ids=[f"R{a}K{b}H{c}T{d}S{int(e)}" for a, b, c, d, e in EDGE])
@@ -180,7 +190,8 @@ def test_edge_shapes(R, K, H, T, shared):
     ref = run_oracle(inp, want_abs=True)
     ws = make_ws(inp, max_tokens=T + 5)
     try:
-        check_all(ws, to_dev(inp), ref, f"edge R={R} K={K} H={H} T={T}")
+        check_all(ws, to_dev(inp), ref, f"edge R={R} K={K} H={H} T={T}",
+                  declines=EDGE_DECLINES.get((R, K, H, T, shared), ()))
     finally:
         ws.destroy()
 
