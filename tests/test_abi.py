@@ -16,7 +16,8 @@ import pytest
 import tp_reduce_moe_gb300 as arf
 from tp_reduce_moe_gb300 import binding
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "arfuse.h")
+HERE = os.path.dirname(os.path.abspath(__file__))
+HEADER = os.path.join(os.path.dirname(HERE), "include", "arfuse.h")
 
 
 @pytest.fixture(scope="module")
@@ -420,3 +421,22 @@ def test_wait_timeout_injection_setter(lib):
     finally:
         w.destroy()
     assert lib.ar_workspace_inject_wait_timeout(None, 1) == arf.AR_ERR_INVALID_ARG
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
+    """include/arfuse.h compiles as C11 with warnings as errors, and a C
+    program linked to libarfuse.so drives a dry-run workspace through the
+    ABI (tests/host/abi_check.c)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if not gcc:
+        pytest.skip("gcc not available")
+    lib_dir = os.path.dirname(arf.LIB_PATH)
+    exe = tmp_path / "abi_check"
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
+                    os.path.join(HERE, "host", "abi_check.c"), "-L", lib_dir, "-larfuse",
+                    "-Wl,-rpath," + lib_dir, "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "c abi ok" in r.stdout
