@@ -349,8 +349,9 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
     return r;
 }
 
-// Programmatic dependent launch.  Every kernel lets the next kernel in the
-// stream start launching as soon as it starts (launch_dependents), and waits
+// Programmatic dependent launch.  The decode kernels let the next kernel in
+// the stream start launching as soon as they start (launch_dependents), the
+// streaming kernel as each of its CTAs finishes; every kernel waits
 // (griddepcontrol.wait) for the previous kernel to complete and flush its
 // memory before its first global memory access: with the launch attribute,
 // launch latency and prologue overlap the previous kernel's tail; without
