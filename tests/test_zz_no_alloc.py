@@ -86,11 +86,15 @@ def _check(out, r_out, ref, fp32, tag):
         check_bf16(r_out, ref["h"], tag + " residual_out")
 
 
-# dsv3 T = 16 / 24 / 48 / 64: 16-, 8-, 8- and 4-CTA tiles of the built-in table; tiny and
-# glm T = 1: the split kernel; ar_only T = 16: the one-shot kernel (K = 0); prefill T = 200:
-# whole rows with a ragged last wave
+# The plans the automatic choice makes: dsv3 T = 16 the split kernel in twelve-CTA clusters,
+# T = 24 / 48 / 72 eight-CTA tiles (64 KB and 24 KB ring slots) and four-CTA tiles; prefill
+# shape T = 64 four-CTA tiles with 48 KB slots and three producer warps, T = 200 eight-CTA tiles
+# with 24 KB slots, T = 300 (past the table) whole rows with a ragged last wave (300 mod 152);
+# glm T = 1 the split kernel in sixteen-CTA clusters; tiny T = 4 (six summands) and ar_only
+# T = 16 / 200 the one-shot kernel in sixteen-, eight- and two-CTA clusters
 CASES = [("tiny", 4), ("dsv3_decode", 16), ("dsv3_decode", 24), ("dsv3_decode", 48),
-         ("dsv3_decode", 64), ("glm_gemma", 1), ("ar_only", 16), ("prefill", 200)]
+         ("dsv3_decode", 72), ("prefill", 64), ("glm_gemma", 1), ("ar_only", 16), ("ar_only", 200),
+         ("prefill", 200), ("prefill", 300)]
 
 
 @pytest.mark.parametrize("cfg,T", CASES, ids=[f"{c}-T{t}" for c, t in CASES])
