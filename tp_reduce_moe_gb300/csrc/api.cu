@@ -413,6 +413,13 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
     // cluster): a plan the device cannot co-schedule is declined here, before
     // anything is launched.
     if (plan_fits && !plan_fits(fits_ctx, regime, pl, res_f32 != 0)) return AR_ERR_UNSUPPORTED;
+    // The occupancy queries below run on the current device and are cached
+    // under the workspace's: the two must be the same device.
+    if (!(ws->flags & AR_WS_DRY_RUN)) {
+        int cur = -1;
+        if (cudaGetDevice(&cur) != cudaSuccess) return AR_ERR_CUDA;
+        if (cur != ws->device) return AR_ERR_INVALID_ARG;
+    }
     if (regime == AR_REGIME_ONESHOT) oneshot_wave_fit(ws, &pl.c, T, res_f32 != 0);
     if (regime == AR_REGIME_CLUSTER) stream_wave_fit(ws, &pl.s, res_f32 != 0);
     const int ctas = regime == AR_REGIME_ONESHOT ? pl.c.C
@@ -429,10 +436,6 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
         ws->last_grid = grid;
         return AR_VALIDATED;
     }
-
-    int cur = -1;
-    if (cudaGetDevice(&cur) != cudaSuccess) return AR_ERR_CUDA;
-    if (cur != ws->device) return AR_ERR_INVALID_ARG;
 
     arf::RowArgs a;
     std::memset(&a, 0, sizeof a);
