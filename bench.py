@@ -518,9 +518,24 @@ def run_e2e(args, arf, torch, d, ws, dev, stream, bytes_step, barrier, rank_max,
     torch.cuda.synchronize()
     barrier()
     ms = rank_max(a.elapsed_time(b)) / n
+    # The host link on its own (after the timed region): the largest input's
+    # pinned host->device copy, best of three -- the bound the e2e step meets.
+    big = max(range(len(host)), key=lambda j: host[j].numel() * host[j].element_size())
+    nbytes = host[big].numel() * host[big].element_size()
+    link = 0.0
+    for _ in range(3):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        with torch.cuda.stream(stream):
+            sets[0][big].copy_(host[big], non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        link = max(link, nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9)
     del host, sets
     return {"value": round(world * bytes_step / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "h2d_gbs": round(h2d / (ms * 1e-3) / 1e9, 2), "host_link_gbs": round(link, 2),
             "steps": n, "copy_streams": len(copy_streams),
             "overlap": "inputs double-buffered: a step's host->device copies overlap the previous "
                        "step's kernel and read-back",
