@@ -431,6 +431,13 @@ def main_ours(args):
                           gated=args.gated,
                           pdls={"off": (False,), "on": (True,), "both": (False, True)}[args.sweep_pdl],
                           perm_kind=args.sweep_perm)
+    # The L2-hot numbers beside the cold ones: the decode workloads at their
+    # configured T with one input set replayed (inputs that fit the L2 stay
+    # there).
+    sweep_warm = None
+    if not args.no_sweep and rank == 0 and args.sweep_mode == "rotate" and not args.sweep_only:
+        sweep_warm = run_sweep(arf, torch, dev, stream, peak, ("auto",), ("ar_only", "dsv3_decode", "glm_gemma"),
+                               "warm", gated=args.gated, pdls=(False,), perm_kind=args.sweep_perm, extra=False)
 
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
@@ -449,7 +456,8 @@ def main_ours(args):
                 "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas, "gated": bool(args.gated),
                 "pdl": bool(args.pdl),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps, "clocks": clocks.summary(), "sweep": sweep}
+                "gpu_launches": args.steps, "clocks": clocks.summary(), "sweep": sweep,
+                "sweep_warm": sweep_warm}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -548,7 +556,7 @@ SWEEP_EXTRA_T = {"dsv3_decode": (24, 32, 36, 48, 72, 96, 112, 160, 192, 256)}
 
 
 def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="rotate",
-              gated=False, pdls=(False,), perm_kind="random"):
+              gated=False, pdls=(False,), perm_kind="random", extra=True):
     """µs/call vs T for every workload: L2-cold by rotating through disjoint
     input sets (>= 3x L2 in total; each set gathers only within its own block
     of expert rows, like successive layers), timed by replaying a CUDA graph
@@ -560,7 +568,7 @@ def run_sweep(arf, torch, dev, stream, peak, regimes=("auto",), only=(), mode="r
         if only and name not in only:
             continue
         cfg = CONFIGS[name]
-        for T in sorted(set(cfg.Ts) | set(SWEEP_EXTRA_T.get(name, ()))):
+        for T in sorted(set(cfg.Ts) | set(SWEEP_EXTRA_T.get(name, ()) if extra else ())):
             if name == "prefill" and T == HEADLINE[1]:
                 continue
             for regime_name in regimes:
