@@ -51,3 +51,17 @@ def test_binding_refuses_to_run_without_its_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0
     assert "RuntimeError" in r.stderr and "not found" in r.stderr
+
+
+def test_recorded_dram_traffic_is_within_five_percent_of_the_algorithmic_bytes():
+    """The ncu capture behind the headline's roofline.traffic: DRAM reads +
+    writes per token row of the prefill shape within 5 % of the algorithmic
+    bytes per row (R = 8, K = 10, H = 8192, bf16 residual_out), reads alone
+    equal to the algorithmic reads to 0.1 % (every input byte read once)."""
+    import json
+    rec = json.load(open(os.path.join(ROOT, "profiles", "stream_rows_prefill_traffic.json")))
+    R, K, H = 8, 10, 8192
+    per_row = 2 * H * (R * K + R + 3)
+    reads_per_row = 2 * H * (R * K + R + 1)
+    assert abs(rec["dram_bytes_per_row"] / per_row - 1.0) < 0.05
+    assert abs(rec["dram_bytes_read"] / (rec["captured_rows"] * reads_per_row) - 1.0) < 1e-3
