@@ -112,6 +112,7 @@ def load_library(path: str | None = None):
 
 
 def ar_status_string(status: int) -> str:
+    """Text of an ar_status code (\"unknown status\" for other values)."""
     return load_library().ar_status_string(int(status)).decode()
 
 
@@ -146,6 +147,11 @@ def _destroy_handle(handle):
 
 def ar_workspace_create(ranks: int, top_k: int, hidden: int, max_tokens: int, eps: float,
                         device: int | None = None, flags: int = 0) -> Workspace:
+    """Workspace for one model shape (R rank partials, top_k, hidden, eps),
+    shared by its layers; `device` defaults to the current CUDA device,
+    `flags` takes AR_WS_* (AR_WS_DRY_RUN: no GPU state, calls only validate).
+    Installs the built-in regime table when the library has one for the
+    shape."""
     lib = load_library()
     dry = bool(flags & AR_WS_DRY_RUN)
     if device is None:
@@ -158,10 +164,14 @@ def ar_workspace_create(ranks: int, top_k: int, hidden: int, max_tokens: int, ep
 
 
 def ar_workspace_destroy(ws: Workspace) -> None:
+    """Free the workspace (no call on it may still be running)."""
     ws.destroy()
 
 
 def ar_workspace_set_regime(ws: Workspace, regime: int) -> None:
+    """Force AR_REGIME_CLUSTER / _STREAM / _ONESHOT / _SPLIT for later calls
+    (a call it cannot plan raises AR_ERR_UNSUPPORTED); AR_REGIME_AUTO restores
+    the regime table and the heuristic."""
     _check(load_library().ar_workspace_set_regime(ctypes.c_void_p(ws.handle), int(regime)),
            "ar_workspace_set_regime")
 
@@ -248,6 +258,8 @@ def ar_workspace_inject_wait_timeout(ws: Workspace, limit_ns: int) -> None:
 
 
 def ar_workspace_last_regime(ws: Workspace):
+    """(regime, CTAs per row -- or the grid for whole-row streaming) of the
+    last launched (dry run: validated) call; (0, 0) before the first."""
     n = ctypes.c_int(0)
     r = load_library().ar_workspace_last_regime(ctypes.c_void_p(ws.handle), ctypes.byref(n))
     return int(r), int(n.value)
