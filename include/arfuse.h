@@ -121,15 +121,19 @@ typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
  *   max_tokens  largest T any call may pass (>= 1)
  *   eps         RMSNorm epsilon every call must repeat
  *   flags       0, or any of AR_WS_DRY_RUN, AR_WS_NORM_BF16_H, AR_WS_PDL.
- *               AR_WS_PDL launches every kernel with programmatic dependent
+ *               AR_WS_PDL launches the kernels with programmatic dependent
  *               launch (cudaLaunchAttributeProgrammaticStreamSerialization):
  *               the launch may begin while the previous kernel in the stream
  *               is still running, and the kernel waits (griddepcontrol.wait)
  *               for that kernel to complete and flush its memory before its
  *               first global memory access, so results and stream order are
- *               unchanged; launch latency overlaps the previous kernel.  Every
- *               kernel also signals its own dependents as soon as it starts
- *               (kernels launched without the attribute are not affected).
+ *               unchanged; launch latency overlaps the previous kernel.  The
+ *               decode kernels signal their own dependents as soon as they
+ *               start, the streaming kernel as each of its CTAs finishes
+ *               (kernels launched without the attribute are not affected).  A
+ *               clustered launch whose clusters fill every co-resident slot
+ *               goes out without the attribute (the next kernel could not be
+ *               placed before it drains).
  *   out         host pointer that receives the handle (set to NULL on error)
  * Errors: AR_ERR_INVALID_ARG (out NULL, max_tokens < 1, eps < 0 or not
  * finite), AR_ERR_ALIGNMENT (hidden % 8), AR_ERR_UNSUPPORTED (limits above,

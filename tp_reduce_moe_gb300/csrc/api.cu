@@ -213,10 +213,13 @@ int stream_active_clusters(int device, const arf::StreamPlan& p, bool res_f32) {
 // would only start once others finish (measured: dsv3 T = 192, four-CTA
 // tiles with 24 KB slots, 114 planned clusters, the last ones starting
 // 19 us into the launch); the grid is capped at the co-resident count.
-void stream_wave_fit(const ar_workspace* ws, arf::StreamPlan* p, bool res_f32) {
-    if ((ws->flags & AR_WS_DRY_RUN) || p->geo.C < 2) return;
+// Returns whether the grid fills every co-resident cluster slot.
+bool stream_wave_fit(const ar_workspace* ws, arf::StreamPlan* p, bool res_f32) {
+    if ((ws->flags & AR_WS_DRY_RUN) || p->geo.C < 2) return false;
     const int n = stream_active_clusters(ws->device, *p, res_f32);
-    if (n >= 1 && (int64_t)n * p->geo.C < p->grid) p->grid = n * p->geo.C;
+    if (n < 1) return false;
+    if ((int64_t)n * p->geo.C < p->grid) p->grid = n * p->geo.C;
+    return p->grid / p->geo.C >= n;
 }
 
 // A one-shot launch of eight loads per thread that does not fit one wave of
@@ -421,7 +424,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
         if (cur != ws->device) return AR_ERR_INVALID_ARG;
     }
     if (regime == AR_REGIME_ONESHOT) oneshot_wave_fit(ws, &pl.c, T, res_f32 != 0);
-    if (regime == AR_REGIME_CLUSTER) stream_wave_fit(ws, &pl.s, res_f32 != 0);
+    const bool fills_device = regime == AR_REGIME_CLUSTER && stream_wave_fit(ws, &pl.s, res_f32 != 0);
     const int ctas = regime == AR_REGIME_ONESHOT ? pl.c.C
                      : regime == AR_REGIME_SPLIT ? pl.x.geo.C
                      : regime == AR_REGIME_CLUSTER ? pl.s.geo.C
@@ -468,7 +471,12 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    const bool pdl = (ws->flags & AR_WS_PDL) != 0;
+    // A clustered streaming launch that fills every co-resident cluster slot
+    // runs without programmatic dependent launch: the next call's clusters
+    // cannot be placed before it drains anyway, and placed early they left
+    // an eight-CTA cluster waiting (measured, dsv3 T = 36, 36 clusters of 8
+    // on 36 slots: +1.7-2.0 us per call with the attribute, none without).
+    const bool pdl = (ws->flags & AR_WS_PDL) != 0 && !fills_device;
     if (regime == AR_REGIME_ONESHOT)
         e = arf::launch_cluster_rows(a, pl.c, res_f32 != 0, s, pdl);
     else if (regime == AR_REGIME_SPLIT)
