@@ -902,3 +902,21 @@ def test_split_any_cluster_size_and_groups(cfg, T, combos):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+# --------------------- the TP16 routing profile (R = 16, K = 10, H = 8192) through its table
+@pytest.mark.parametrize("T", [3, 12, 32, 72])
+def test_tp16_table_plans_meet_the_oracle(T):
+    """Sixteen rank partials of top-10 rows at H = 8192 (177 segments per
+    row): the built-in table's plan at decode and mid-range T -- split, tiles
+    with default and smaller ring slots -- against the oracle."""
+    from gen import Config
+    cfg = Config("tp16", 97, R=16, K=10, H=8192, Ts=(T,), eps=1e-6, weights="softmax", has_shared=True)
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        assert arf.ar_workspace_get_regime_table(ws), "a built-in table for this shape"
+        check_all(ws, to_dev(inp), ref, f"tp16 T={T}", regimes=(arf.AR_REGIME_AUTO,))
+    finally:
+        ws.destroy()

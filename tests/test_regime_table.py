@@ -259,8 +259,8 @@ def test_rule_slot_size_and_producers_reach_the_plan(dsv3):
     assert dsv3.plan(48) == with_rule == (arf.AR_REGIME_CLUSTER, 4)
 
 
-@pytest.mark.parametrize("shape", [(8, 8, 7168), (4, 8, 7168), (8, 8, 6144), (8, 10, 8192), (2, 0, 7168),
-                                   (8, 0, 7168)])
+@pytest.mark.parametrize("shape", [(8, 8, 7168), (4, 8, 7168), (8, 8, 6144), (8, 10, 8192), (16, 10, 8192),
+                                   (2, 0, 7168), (8, 0, 7168)])
 def test_every_builtin_rule_has_its_own_plan(shape):
     """Every rule of every built-in table plans its own regime (and cluster
     size, where it names one) at both ends of its token range on a GB300-sized

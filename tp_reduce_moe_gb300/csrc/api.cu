@@ -116,6 +116,14 @@ const BuiltinTable kBuiltinTables[] = {
       {80, AR_REGIME_CLUSTER, 8, 24576, 2}, {96, AR_REGIME_CLUSTER, 8, 32768, 2},
       {128, AR_REGIME_CLUSTER, 4, 49152, 3}, {160, AR_REGIME_CLUSTER, 16, 0, 0},
       {224, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_CLUSTER, 4, 49152, 3}}},
+    // H = 8192, top-10, TP16 (with TP8 above, the GB300 routing profiles of sglang PR
+    // #37196, Known gaps)
+    {16, 10, 8192, 11,
+     {{6, AR_REGIME_SPLIT, 16, 0, 0}, {14, AR_REGIME_CLUSTER, 8, 0, 0}, {20, AR_REGIME_CLUSTER, 16, 0, 0},
+      {36, AR_REGIME_CLUSTER, 8, 49152, 3}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {72, AR_REGIME_CLUSTER, 4, 24576, 2}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 0},
+      {160, AR_REGIME_CLUSTER, 8, 49152, 3}, {192, AR_REGIME_CLUSTER, 8, 24576, 2},
+      {256, AR_REGIME_STREAM, 0, 0, 0}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0): the one-shot kernel in
     // smaller clusters than its plan's coverage rule picks (T = 160-256: wave
     // quantisation of the grid decides between four- and two-CTA clusters)
