@@ -687,7 +687,8 @@ def test_split_rows_of_the_last_wave(cfg, T):
         ws.destroy()
 
 
-@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 4), ("dsv3_decode", 64), ("ar_only", 16), ("prefill", 3)])
+@pytest.mark.parametrize("cfg,T", [("dsv3_decode", 4), ("dsv3_decode", 64), ("ar_only", 16), ("prefill", 3),
+                                   ("dsv3_decode", 200)])
 def test_pdl_chain_reads_the_previous_calls_output(cfg, T):
     """With AR_WS_PDL, calls launched back to back without a host sync, each
     reading the previous call's residual_out as its residual: every call must
