@@ -101,7 +101,8 @@ typedef enum ar_status {
 #define AR_REGIME_SPLIT 4    /* small T: one cluster per row, the row's segments dealt    */
                              /* to its C CTAs (in column groups), partial rows            */
                              /* reduce-scattered through distributed shared memory        */
-                             /* (fewest copies per CTA)                                   */
+                             /* (fewest copies per CTA); heavy rows in two copy rounds    */
+                             /* through half the buffers when that fits more clusters     */
 
 typedef struct ar_workspace ar_workspace;  /* opaque, library-owned */
 
@@ -284,9 +285,9 @@ ARFUSE_API ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps
  * segments among themselves (bulk copies of 1/G of a row each) and
  * reduce-scatter only their group's columns, which cuts the distributed-
  * shared-memory exchange G-fold for G-fold more, smaller copies.  A forced
- * value that does not split the cluster into groups of at least two CTAs
- * leaves the split regime without a plan (AR_ERR_UNSUPPORTED when the regime
- * is forced).  Other values are AR_ERR_INVALID_ARG.  A tuning control:
+ * value that does not split the cluster into groups of at least two CTAs,
+ * or deals a CTA more than 64 segments (32 per copy round), leaves the split
+ * regime without a plan (AR_ERR_UNSUPPORTED when the regime is forced).  Other values are AR_ERR_INVALID_ARG.  A tuning control:
  * residual_out equals, bit for bit, that of a split over C/G CTAs without
  * groups (the same segments per CTA, the same slice order); out differs from
  * it only through the summation order of the tile sums of squares.

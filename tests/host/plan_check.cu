@@ -82,11 +82,11 @@ int main() {
   // split plans (one row per cluster, segments dealt round-robin within a
   // column group)
   for (int H : Hs) for (int R : Rs) for (int K : Ks) for (int sh = 0; sh < 2; ++sh) for (long T : Ts)
-  for (int G = 1; G <= 8; ++G) {
+  for (int G = 1; G <= 8; ++G) for (int rounds = 1; rounds <= 2; ++rounds) {
     if (K == 0 && !sh) continue;
     for (int Cf = 0; Cf <= 16; Cf = Cf ? Cf + 1 : 2) {
       SplitPlan p;
-      if (!plan_split_rows(R, K, H, sh, T, 152, 232448, 16, Cf, &p, G)) continue;
+      if (!plan_split_rows(R, K, H, sh, T, 152, 232448, 16, Cf, &p, G, rounds)) continue;
       ++checks;
       const auto& g = p.geo;
       const int chunks = H / 8, nseg = (sh ? R : 0) + 1 + R * K, C = g.C, Cs = g.Cs;
@@ -98,13 +98,26 @@ int main() {
       if (2 * g.tile_chunks > p.cpt * consumers) bad = true;     // <= CPT float4 items per thread
       if (g.seg_stride < g.group_chunks * 16 || g.seg_stride % 128 || g.part_bytes < Cs * g.tile_chunks * 32) bad = true;
       if (g.row_f32_bytes < g.group_chunks * 32) bad = true;
+      if (g.rounds != rounds) bad = true;
+      const int nsr = (sh ? R : 0) + 1;
+      bool second = false;
       long covered = 0;
       for (int c = 0; c < C; ++c) {
         const int grp = c / Cs, cs = c % Cs;
         const int g0 = grp * g.group_chunks, gchunks = std::min(g.group_chunks, chunks - g0);
         const int ns = (nseg - cs + Cs - 1) / Cs;
-        if (gchunks < 1 || ns < 1 || ns > 32) bad = true;
-        if (1024 + g.part_bytes + std::max<long>(g.row_f32_bytes, (long)ns * g.seg_stride) > p.smem) bad = true;
+        // the kernel's own split of the CTA's segments: [0, nsr_c) shared
+        // partials and residual, [nsr_c, nmid) the first routed half
+        const int nsr_c = nsr > cs ? (nsr - 1 - cs) / Cs + 1 : 0;
+        const int nmid = nsr_c + (ns - nsr_c + 1) / 2;
+        if (gchunks < 1 || ns < 1 || ns > 64) bad = true;       // coefficient table of 64
+        // buffers the CTA touches: every segment's, or with two rounds the
+        // first nmid (segment i >= nmid lands in buffer i - nmid < ns - nmid)
+        const int nbuf = rounds == 1 ? ns : nmid;
+        if (rounds == 1 && ns > 32) bad = true;                 // one producer lane per segment
+        if (rounds == 2 && (nmid > 32 || ns - nmid > 32 || ns - nmid > nmid)) bad = true;
+        if (rounds == 2 && ns > nmid) second = true;
+        if (1024 + g.part_bytes + std::max<long>(g.row_f32_bytes, (long)nbuf * g.seg_stride) > p.smem) bad = true;
         if ((long)ns * gchunks * 16 >= (1 << 20)) bad = true;   // mbarrier transaction count
         const int ntile = std::min(g.tile_chunks, gchunks - cs * g.tile_chunks);
         if (ntile < 1) bad = true;                               // every CTA owns a tile
@@ -112,7 +125,8 @@ int main() {
         covered += ntile;
       }
       if (covered != chunks) bad = true;                         // tiles partition the row
-      if (bad) { ++fails; if (fails < 20) printf("BAD split H=%d R=%d K=%d sh=%d T=%ld Cf=%d G=%d\n", H, R, K, sh, T, Cf, G); }
+      if (rounds == 2 && !second) bad = true;                    // a second round exists
+      if (bad) { ++fails; if (fails < 20) printf("BAD split H=%d R=%d K=%d sh=%d T=%ld Cf=%d G=%d rounds=%d\n", H, R, K, sh, T, Cf, G, rounds); }
     }
   }
   // one-shot plans (one cluster per row, every load of a thread in flight)
@@ -167,6 +181,27 @@ int main() {
       printf("oneshot R=8 K=0 H=7168 T=%ld C=%d threads=%d -> %s\n", T, p.C, p.threads, use64 ? "64-register form" : "80-register form");
       if (use64 != (T >= 128)) { ++fails; printf("unexpected form at T=%ld\n", T); }
     }
+  }
+  // the two-round switch: only when one-round clusters are fewer than the
+  // rows and the two-round form holds more
+  {
+    struct Case { long T; int n1, n2; bool want; };
+    const Case cases[] = {{8, 7, 14, true}, {7, 7, 14, false}, {8, 7, 7, false}, {8, 7, 6, false},
+                          {16, 7, 14, true}, {1, 7, 14, false}, {8, 0, 14, false}};
+    for (const Case& c : cases)
+      if (split_prefer_two_rounds(c.T, c.n1, c.n2) != c.want) {
+        ++fails;
+        printf("two-round switch T=%ld n1=%d n2=%d: expected %d\n", c.T, c.n1, c.n2, (int)c.want);
+      }
+    // the heavy-row shape that needs it: R = 16, K = 10, H = 8192
+    SplitPlan p1, p2;
+    const bool ok1 = plan_split_rows(16, 10, 8192, true, 8, 152, 232448, 16, 16, &p1, 0, 1);
+    const bool ok2 = plan_split_rows(16, 10, 8192, true, 8, 152, 232448, 16, 16, &p2, 0, 2);
+    printf("split R=16 K=10 H=8192 C=16: one round %s (groups %d, %d B), two rounds %s (groups %d, %d B)\n",
+           ok1 ? "ok" : "none", ok1 ? p1.geo.C / p1.geo.Cs : 0, ok1 ? p1.smem : 0, ok2 ? "ok" : "none",
+           ok2 ? p2.geo.C / p2.geo.Cs : 0, ok2 ? p2.smem : 0);
+    // two rounds must fit two CTAs per SM there (1 KB reserved per CTA)
+    if (!ok1 || !ok2 || 2 * (p2.smem + 1024) > 233472) { ++fails; printf("unexpected heavy-row split plans\n"); }
   }
   printf("checked %ld plans, %ld bad\n", checks, fails);
   return fails != 0;

@@ -721,10 +721,11 @@ def test_pdl_chain_reads_the_previous_calls_output(cfg, T):
 # ------------------------------- split kernel with more rows than resident clusters
 @pytest.mark.parametrize("cfg,T,csize", [("dsv3_decode", 64, 16), ("dsv3_decode", 100, 8), ("glm_gemma", 40, 16),
                                          ("prefill", 30, 16), ("tiny", 1000, 4)])
-def test_split_clusters_loop_over_rows(cfg, T, csize):
-    """When T exceeds the clusters the device runs at once, each cluster of the
-    split kernel loops over rows k, k + n, ... (every barrier one phase per row,
-    the producer reusing the buffers once the row's exchange is done)."""
+def test_split_launch_of_more_rows_than_resident_clusters(cfg, T, csize):
+    """When T exceeds the clusters the device runs at once, the split kernel's
+    clusters (one row each) run in several waves -- or, for rows whose
+    segments leave one CTA per SM, in the two-copy-round form when the device
+    holds more of its clusters."""
     inp = make_inputs(cfg, T)
     ref = run_oracle(inp, want_abs=True)
     ws = make_ws(inp)
@@ -919,5 +920,48 @@ def test_tp16_table_plans_meet_the_oracle(T):
     try:
         assert arf.ar_workspace_get_regime_table(ws), "a built-in table for this shape"
         check_all(ws, to_dev(inp), ref, f"tp16 T={T}", regimes=(arf.AR_REGIME_AUTO,))
+    finally:
+        ws.destroy()
+
+
+# --------------------- split kernel in two copy rounds (half the segment buffers)
+TWO_ROUND_CASES = [
+    # (R, K, H, T, cluster size, column groups): two rounds because one round
+    # has no plan (more than 32 segments for a CTA), or -- groups 0 at T >= 8 --
+    # because the device holds more of the two-round form's clusters
+    (16, 10, 8192, 1, 16, 4),
+    (16, 10, 8192, 9, 16, 4),
+    (16, 10, 8192, 8, 16, 0),
+    (16, 10, 8192, 13, 16, 0),
+    (8, 8, 7168, 1, 16, 8),
+    (8, 8, 7168, 5, 16, 8),
+    (8, 8, 7168, 3, 4, 2),
+]
+
+
+@pytest.mark.parametrize("R,K,H,T,csize,groups", TWO_ROUND_CASES,
+                         ids=[f"R{c[0]}K{c[1]}H{c[2]}T{c[3]}C{c[4]}G{c[5]}" for c in TWO_ROUND_CASES])
+def test_split_two_rounds_meets_the_oracle(R, K, H, T, csize, groups):
+    """The split kernel with buffers for the first half of a CTA's segments:
+    the second routed half is fetched into them once every consumer warp has
+    folded the first.  Both residual_out types against the oracle, the error
+    word clean, and the same bits on a second call."""
+    from gen import Config
+    cfg = Config("two_rounds", 98, R=R, K=K, H=H, Ts=(T,), eps=1e-6, weights="softmax", has_shared=True)
+    inp = make_inputs(cfg, T)
+    ref = run_oracle(inp, want_abs=True)
+    ws = make_ws(inp)
+    try:
+        arf.ar_workspace_set_cluster_size(ws, csize)
+        arf.ar_workspace_set_split_column_groups(ws, groups)
+        d = to_dev(inp)
+        check_all(ws, d, ref, f"two rounds R={R} K={K} H={H} T={T} C={csize} G={groups}",
+                  regimes=(arf.AR_REGIME_SPLIT,))
+        assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_SPLIT, csize)
+        a1 = run_gpu(ws, d, fp32=True, regime=arf.AR_REGIME_SPLIT)
+        a2 = run_gpu(ws, d, fp32=True, regime=arf.AR_REGIME_SPLIT)
+        torch.cuda.synchronize()
+        assert torch.equal(a1[0], a2[0]) and torch.equal(a1[1], a2[1])
+        assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()

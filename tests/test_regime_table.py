@@ -83,7 +83,8 @@ def test_rule_without_a_plan_falls_back(dsv3):
     arf.ar_workspace_set_regime_table(dsv3.ws, [])
     h1 = dsv3.plan(1)
     # 73 segments over a 2-CTA split cluster is 37 per CTA: beyond the split
-    # kernel's 32 producer lanes, so the rule has no plan
+    # kernel's 32 producer lanes in one round, and two rounds would buffer 21
+    # whole 14 KB rows (301 KB of shared memory), so the rule has no plan
     arf.ar_workspace_set_regime_table(dsv3.ws, [(4, arf.AR_REGIME_SPLIT, 2)])
     assert dsv3.plan(1) == h1
 
@@ -191,22 +192,35 @@ def test_light_rows_are_never_split():
 
 
 def test_split_column_groups_need_two_ctas_per_group(dsv3):
-    """Forced column groups must leave groups of at least two CTAs whose share
-    of the row's 73 segments fits the producer's 32 lanes; otherwise the
-    forced split regime has no plan."""
+    """Forced column groups must leave groups of at least two CTAs.  A
+    group's share of the row's segments beyond the producer's 32 lanes is
+    fetched in two copy rounds of at most 32 segments each (dsv3, 2 CTAs per
+    group: 37 segments, 21 + 16); past that the forced split regime has no
+    plan (R = 16, K = 10: 89 segments for each of 2 CTAs per group)."""
     arf.ar_workspace_set_regime(dsv3.ws, arf.AR_REGIME_SPLIT)
     arf.ar_workspace_set_cluster_size(dsv3.ws, 16)
-    for groups in (0, 1, 2, 4):
+    for groups in (0, 1, 2, 4, 8):
         arf.ar_workspace_set_split_column_groups(dsv3.ws, groups)
         assert dsv3.plan(4) == (arf.AR_REGIME_SPLIT, 16)
-    arf.ar_workspace_set_split_column_groups(dsv3.ws, 8)    # 2 CTAs per group: 37 segments each
-    with pytest.raises(arf.ArfuseError) as e:
-        dsv3.plan(4)
-    assert e.value.status == arf.AR_ERR_UNSUPPORTED
+        assert arf.ar_workspace_last_grid(dsv3.ws) == 4 * 16
     arf.ar_workspace_set_cluster_size(dsv3.ws, 4)
     arf.ar_workspace_set_split_column_groups(dsv3.ws, 4)    # one CTA per group
-    with pytest.raises(arf.ArfuseError):
+    with pytest.raises(arf.ArfuseError) as e:
         dsv3.plan(1)
+    assert e.value.status == arf.AR_ERR_UNSUPPORTED
+    heavy = Shape(16, 10, 8192)
+    try:
+        arf.ar_workspace_set_regime(heavy.ws, arf.AR_REGIME_SPLIT)
+        arf.ar_workspace_set_cluster_size(heavy.ws, 16)
+        for groups in (0, 2, 4):        # one round (two groups) or two rounds (four)
+            arf.ar_workspace_set_split_column_groups(heavy.ws, groups)
+            assert heavy.plan(1) == (arf.AR_REGIME_SPLIT, 16)
+        arf.ar_workspace_set_split_column_groups(heavy.ws, 8)
+        with pytest.raises(arf.ArfuseError) as e:
+            heavy.plan(1)
+        assert e.value.status == arf.AR_ERR_UNSUPPORTED
+    finally:
+        heavy.ws.destroy()
 
 
 def test_one_shot_cluster_size_from_a_rule_or_the_workspace():

@@ -117,12 +117,12 @@ const BuiltinTable kBuiltinTables[] = {
       {128, AR_REGIME_CLUSTER, 4, 49152, 3}, {160, AR_REGIME_CLUSTER, 16, 0, 0},
       {224, AR_REGIME_CLUSTER, 8, 24576, 2}, {256, AR_REGIME_CLUSTER, 4, 49152, 3}}},
     // H = 8192, top-10, TP16 (with TP8 above, the GB300 routing profiles of sglang PR
-    // #37196, Known gaps)
-    {16, 10, 8192, 11,
-     {{6, AR_REGIME_SPLIT, 16, 0, 0}, {14, AR_REGIME_CLUSTER, 8, 0, 0}, {20, AR_REGIME_CLUSTER, 16, 0, 0},
-      {36, AR_REGIME_CLUSTER, 8, 49152, 3}, {48, AR_REGIME_CLUSTER, 8, 24576, 2},
-      {72, AR_REGIME_CLUSTER, 4, 24576, 2}, {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 0},
-      {160, AR_REGIME_CLUSTER, 8, 49152, 3}, {192, AR_REGIME_CLUSTER, 8, 24576, 2},
+    // #37196, Known gaps); from T = 8 the split kernel runs in two copy rounds
+    {16, 10, 8192, 10,
+     {{12, AR_REGIME_SPLIT, 16, 0, 0}, {20, AR_REGIME_CLUSTER, 16, 0, 0}, {36, AR_REGIME_CLUSTER, 8, 49152, 3},
+      {48, AR_REGIME_CLUSTER, 8, 24576, 2}, {72, AR_REGIME_CLUSTER, 4, 24576, 2},
+      {96, AR_REGIME_CLUSTER, 8, 24576, 2}, {128, AR_REGIME_STREAM, 0, 0, 0},
+      {160, AR_REGIME_CLUSTER, 8, 49152, 3}, {224, AR_REGIME_CLUSTER, 8, 24576, 2},
       {256, AR_REGIME_STREAM, 0, 0, 0}}},
     // trailing all-reduce + RMSNorm, two partials (K = 0): the one-shot kernel in
     // smaller clusters than its plan's coverage rule picks (T = 160-256: wave
@@ -182,7 +182,8 @@ struct Plans {
 // Host-side occupancy queries, cached per (device, query kind, kernel
 // instantiation, block, shared memory, cluster) in a fixed-size table (no
 // allocation): resident blocks per SM of a one-shot plan (kind 0) and
-// co-resident clusters of a clustered streaming plan (kind 1).
+// co-resident clusters of a clustered streaming plan (kind 1) or of a split
+// plan (kind 2).
 struct OccEntry {
     int key[7];  // device + 1, kind, then the kind's fields; key[0] == 0: empty
     int n;
@@ -212,6 +213,11 @@ int oneshot_blocks_per_sm(int device, const arf::ClusterPlan& p, bool res_f32) {
 int stream_active_clusters(int device, const arf::StreamPlan& p, bool res_f32) {
     const int key[7] = {device + 1, 1, p.cpt, res_f32 ? 1 : 0, p.threads, p.smem, p.geo.C};
     return occ_cached(key, [&] { return arf::stream_rows_active_clusters(p, res_f32); });
+}
+
+int split_active_clusters(int device, const arf::SplitPlan& p, bool res_f32) {
+    const int key[7] = {device + 1, 2, p.cpt, res_f32 ? 1 : 0, p.threads, p.smem, p.geo.C};
+    return occ_cached(key, [&] { return arf::split_rows_active_clusters(p, res_f32); });
 }
 
 // A clustered streaming plan sizes its grid from shared memory per SM; the
@@ -248,6 +254,23 @@ void oneshot_wave_fit(const ar_workspace* ws, arf::ClusterPlan* p, int64_t T, bo
 // Column groups of a split plan (0: the planner's choice).
 int split_groups(const ar_workspace* ws) { return ws->split_groups; }
 
+// A split plan of one round buffers all of a CTA's segments; for heavy rows
+// that can leave one CTA per SM and fewer co-resident clusters than rows, so
+// the last rows would run in a second wave.  Then the same cluster size with
+// two copy rounds (half the buffers) runs instead when the device holds more
+// of its clusters (measured at R = 16, K = 10, H = 8192).
+void split_wave_fit(const ar_workspace* ws, arf::SplitPlan* p, int R, int K, int H, bool shared, int64_t T,
+                    bool res_f32) {
+    if ((ws->flags & AR_WS_DRY_RUN) || p->geo.rounds != 1) return;
+    const int n1 = split_active_clusters(ws->device, *p, res_f32);
+    if (n1 < 1 || n1 >= T) return;
+    arf::SplitPlan q{};
+    if (!arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin, ws->max_cluster_split,
+                              p->geo.C, &q, split_groups(ws), 2))
+        return;
+    if (arf::split_prefer_two_rounds(T, n1, split_active_clusters(ws->device, q, res_f32))) *p = q;
+}
+
 // Plan `regime` with `ctas` CTAs per row (0: the regime's own choice).
 // Returns the regime that will run (a streaming plan reports CLUSTER when its
 // rows are split over a cluster, STREAM otherwise), 0 when there is no plan.
@@ -261,11 +284,13 @@ int plan_regime(const ar_workspace* ws, int regime, int ctas, int R, int K, int 
                        ? AR_REGIME_ONESHOT
                        : 0;
         case AR_REGIME_SPLIT:
-            // the given cluster size, else the largest that fits
-            for (int c = ctas ? ctas : 16; c >= 2; c = ctas ? 0 : c >> 1)
-                if (arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
-                                         ws->max_cluster_split, c, &p->x, split_groups(ws)))
-                    return AR_REGIME_SPLIT;
+            // the given cluster size, else the largest that fits; with every
+            // segment buffered at once, else in two copy rounds
+            for (int rounds = 1; rounds <= 2; ++rounds)
+                for (int c = ctas ? ctas : 16; c >= 2; c = ctas ? 0 : c >> 1)
+                    if (arf::plan_split_rows(R, K, H, shared, T, ws->num_sms, ws->smem_optin,
+                                             ws->max_cluster_split, c, &p->x, split_groups(ws), rounds))
+                        return AR_REGIME_SPLIT;
             return 0;
         case AR_REGIME_STREAM:
         case AR_REGIME_CLUSTER: {
@@ -432,6 +457,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
         if (cur != ws->device) return AR_ERR_INVALID_ARG;
     }
     if (regime == AR_REGIME_ONESHOT) oneshot_wave_fit(ws, &pl.c, T, res_f32 != 0);
+    if (regime == AR_REGIME_SPLIT) split_wave_fit(ws, &pl.x, R, K, H, shared, T, res_f32 != 0);
     const bool fills_device = regime == AR_REGIME_CLUSTER && stream_wave_fit(ws, &pl.s, res_f32 != 0);
     const int ctas = regime == AR_REGIME_ONESHOT ? pl.c.C
                      : regime == AR_REGIME_SPLIT ? pl.x.geo.C

@@ -402,6 +402,8 @@ struct SplitGeom {
     int part_bytes;   // bytes of the fp32 receive buffer (Cs slices of a column tile)
     int row_f32_bytes;  // bytes of the CTA's fp32 partial row (over the segment buffers)
     int tile_chunks;  // 16-byte chunks of the column tile each CTA finishes
+    int rounds;       // 1: every segment buffered at once; 2: the second routed half
+                      // reuses the first buffers once they are folded
 };
 
 // Arguments of the all-reduce + mHC write-back (mhc_post.cu).

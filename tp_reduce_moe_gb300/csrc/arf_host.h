@@ -74,13 +74,23 @@ struct SplitPlan {
 
 // Plan a split_rows launch (one row per cluster); C = 0 picks the largest
 // cluster that fits; `groups` column groups per row (they must divide C; 0
-// picks the most that fit).  Returns false if no plan fits.
+// picks the most that fit); `rounds` 1 buffers all of a CTA's segments at
+// once, 2 fetches the second routed half into the first half's buffers once
+// those are folded (half the shared memory, one more round trip).  Returns
+// false if no plan fits.
 bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
-                     int max_cluster, int C, SplitPlan* p, int groups = 1);
+                     int max_cluster, int C, SplitPlan* p, int groups = 1, int rounds = 1);
 cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32,
                               cudaStream_t stream, bool pdl = false);
 cudaError_t split_rows_set_attributes(int smem_optin);
 int split_rows_max_cluster(int threads, int smem, int cpt);
 bool split_rows_plan_fits(const SplitPlan& p, bool res_f32);
+// Clusters of a split plan the device holds at once (0 if the query fails).
+int split_rows_active_clusters(const SplitPlan& p, bool res_f32);
+// Whether T rows should run the two-round form of a split plan, given the
+// co-resident clusters of its one-round form (n1) and two-round form (n2):
+// only when the one-round launch does not fit one wave and the two-round
+// form holds more clusters.
+bool split_prefer_two_rounds(int64_t T, int n1, int n2);
 
 }  // namespace arf

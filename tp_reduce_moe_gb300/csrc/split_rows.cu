@@ -35,6 +35,11 @@
 //     C sums; normalise; store.
 //   producer warp, afterwards: sends the partial row's slices to the group
 //     peers and the tile's sum of squares to every CTA of the cluster.
+//   two rounds (heavy rows, e.g. 177 segments at R = 16, K = 10): the CTA
+//     has buffers for the first half of its segments only; the producer warp
+//     issues the second routed half into them once every consumer warp has
+//     folded the first (one more memory round trip, half the shared memory,
+//     so two CTAs fit on an SM where one did).
 //
 // One cluster barrier (arrived on right after the mbarriers are initialised,
 // waited on just before the first send) keeps peers from signalling a
@@ -55,7 +60,7 @@
 
 namespace arf {
 
-constexpr int kSplitMaxSegs = 32;       // segments per CTA (one producer lane each)
+constexpr int kSplitMaxSegs = 32;       // segments per CTA and copy round (one producer lane each)
 constexpr int kSplitMaxConsumers = 512;
 constexpr int kSplitMaxThreads = 32 + kSplitMaxConsumers;
 constexpr int kSplitHeader = 1024;      // barriers, coefficient table, partial sums, flags
@@ -63,11 +68,15 @@ constexpr int kSplitMinGroupChunks = 128;  // automatic column groups: at least 
 
 // Header layout (bytes): 0 bar[3] (segment loads: shared partials and
 // residual, first and second half of the routed rows), 24 rbar (slices
-// received), 32 ssbar (sums of squares received); 64 coef[32] f32; 192
-// red[32] f32; 320 ss slots [16] f32 (one per source CTA); 384 abort flag;
-// 1024 receive buffer [Cs][tile_chunks*8] f32 (slice of every source CTA's
-// partial row); then the segment buffers at seg_stride, which the partial row
-// [group_chunks*8] f32 reuses once the segments are folded in.
+// received), 32 ssbar (sums of squares received), 40 relbar (two rounds: the
+// first round's buffers are folded, one arrival per consumer warp); 64
+// coef[64] f32; 320 red[32] f32; 448 ss slots [16] f32 (one per source CTA);
+// 512 abort flag; 516 second-round flag; 1024 receive buffer
+// [Cs][tile_chunks*8] f32 (slice of every source CTA's partial row); then the
+// segment buffers at seg_stride, which the partial row [group_chunks*8] f32
+// reuses once the segments are folded in.  With two rounds there are buffers
+// for the first nmid segments only: segment i >= nmid lands in buffer
+// i - nmid.
 template <int CPT, bool RES_F32>
 __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     split_rows_kernel(const __grid_constant__ RowArgs a, const SplitGeom geo) {
@@ -76,10 +85,12 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     uint64_t* rbar = bar + 3;
     uint64_t* ssbar = bar + 4;
+    uint64_t* relbar = bar + 5;
     float* coef = reinterpret_cast<float*>(smem + 64);
-    float* red = reinterpret_cast<float*>(smem + 192);
-    float* ss_slots = reinterpret_cast<float*>(smem + 320);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 384);
+    float* red = reinterpret_cast<float*>(smem + 320);
+    float* ss_slots = reinterpret_cast<float*>(smem + 448);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 512);
+    int* round2 = reinterpret_cast<int*>(smem + 516);
     float* recv = reinterpret_cast<float*>(smem + kSplitHeader);
     uint8_t* segbuf = smem + kSplitHeader + geo.part_bytes;
     // the CTA's fp32 partial row reuses the segment buffers once every
@@ -110,6 +121,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     const int ns = (nseg - cs + Cs - 1) / Cs;
     const int nsr_c = (nsr > cs) ? (nsr - 1 - cs) / Cs + 1 : 0;
     const int nmid = nsr_c + (ns - nsr_c + 1) / 2;
+    // Two rounds: the routed rows [nmid, ns) go out only once the consumers
+    // have folded [0, nmid), into the buffers of segments [0, ns - nmid).
+    const bool two = geo.rounds == 2;
 
     const int tile = geo.tile_chunks;
     const int ntile_c = min(tile, chunks - cs * tile);  // chunks of this CTA's tile
@@ -145,7 +159,9 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         mbar_init(smem_addr(&bar[2]), 1);
         mbar_init(smem_addr(rbar), 1);
         mbar_init(smem_addr(ssbar), 1);
+        mbar_init(smem_addr(relbar), (uint32_t)ncw);
         *abort_flag = 0;
+        *round2 = 0;
         fence_mbar_init();
         // every CTA of the group sends this tile's slice of its partial row,
         // and every CTA of the cluster its tile's sum of squares (4 bytes)
@@ -180,7 +196,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             __syncwarp();
             if (lane == 0 && nsr_c > 0) mbar_arrive_expect_tx(smem_addr(&bar[0]), (uint32_t)nsr_c * row_bytes);
         } else {
-            const bool routed = i >= nsr_c && i < ns;
+            const bool routed = i >= nsr_c && i < (two ? nmid : ns);
             const int64_t rowv = lane < a.K ? checked_row(raw, a.rows_e, a.err) : 0;
             const int e = s - nsr;
             const int k = routed ? e / a.R : 0;
@@ -193,7 +209,40 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if (nmid > nsr_c) mbar_arrive_expect_tx(smem_addr(&bar[1]), (uint32_t)(nmid - nsr_c) * row_bytes);
-                if (ns > nmid) mbar_arrive_expect_tx(smem_addr(&bar[2]), (uint32_t)(ns - nmid) * row_bytes);
+                if (!two && ns > nmid) mbar_arrive_expect_tx(smem_addr(&bar[2]), (uint32_t)(ns - nmid) * row_bytes);
+            }
+            if (two && ns > nmid) {
+                // Second round: once every consumer warp has folded the first
+                // (relbar), the routed rows [nmid, ns) into buffers
+                // [0, ns - nmid), lane l taking segment nmid + l.
+                int go = 0;
+                if (lane == 0) {
+                    if (mbar_wait_bounded(smem_addr(relbar), 0u, abort_flag)) {
+                        go = *abort_flag ? 0 : 1;
+                    } else {
+                        if (!*abort_flag) atomicOr(a.err, kErrTimeout);
+                        *abort_flag = 1;
+                    }
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (go) {
+                    const int i2 = nmid + lane;
+                    const bool routed2 = i2 < ns;
+                    const int e2 = cs + i2 * Cs - nsr;
+                    const int k2 = routed2 ? e2 / a.R : 0;
+                    const int64_t row_k2 = __shfl_sync(0xffffffffu, rowv, k2);
+                    const float w_k2 = __shfl_sync(0xffffffffu, wv, k2);
+                    if (routed2) {
+                        bulk_g2s(smem_addr(segbuf + (size_t)lane * geo.seg_stride),
+                                 a.E[e2 % a.R] + row_k2 * H + col0, row_bytes, smem_addr(&bar[2]), pol);
+                        coef[i2] = w_k2;
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        *round2 = 1;
+                        mbar_arrive_expect_tx(smem_addr(&bar[2]), (uint32_t)(ns - nmid) * row_bytes);
+                    }
+                }
             }
         }
     }
@@ -213,6 +262,13 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         for (int phase_set = 0; phase_set < 3; ++phase_set) {
             const int i_begin = phase_set == 0 ? 0 : phase_set == 1 ? nsr_c : nmid;
             const int i_end = phase_set == 0 ? nsr_c : phase_set == 1 ? nmid : ns;
+            if (phase_set == 2 && two) {
+                // this warp is done with the first round's buffers
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(relbar));
+            }
+            // buffer of segment i: i, or i - nmid in the second round
+            const int boff = (phase_set == 2 && two) ? nmid : 0;
             if (i_begin >= i_end) continue;
             if (ok && !mbar_wait_bounded(smem_addr(&bar[phase_set]), 0u, abort_flag)) {
                 ok = false;
@@ -235,7 +291,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                 for (int u = 0; u < SU; ++u)
 #pragma unroll
                     for (int m = 0; m < CPT; ++m)
-                        if (valid[m]) v[u][m] = *reinterpret_cast<const uint4*>(src[m] + (size_t)(i0 + u) * stride);
+                        if (valid[m])
+                            v[u][m] = *reinterpret_cast<const uint4*>(src[m] + (size_t)(i0 + u - boff) * stride);
 #pragma unroll
                 for (int u = 0; u < SU; ++u)
 #pragma unroll
@@ -246,7 +303,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
                 const float cf = coef[i0];
 #pragma unroll
                 for (int m = 0; m < CPT; ++m)
-                    if (valid[m]) fma_bf16x8(acc[m], cf, *reinterpret_cast<const uint4*>(src[m] + (size_t)i0 * stride));
+                    if (valid[m])
+                        fma_bf16x8(acc[m], cf, *reinterpret_cast<const uint4*>(src[m] + (size_t)(i0 - boff) * stride));
             }
         }
         // The partial row, locally (over the spent segment buffers); made
@@ -367,7 +425,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) {
         if (nsr_c > 0) (void)mbar_wait_bounded(smem_addr(&bar[0]), 0u, nullptr, 10000000ull);
         if (nmid > nsr_c) (void)mbar_wait_bounded(smem_addr(&bar[1]), 0u, nullptr, 10000000ull);
-        if (ns > nmid) (void)mbar_wait_bounded(smem_addr(&bar[2]), 0u, nullptr, 10000000ull);
+        if (ns > nmid && (!two || *round2)) (void)mbar_wait_bounded(smem_addr(&bar[2]), 0u, nullptr, 10000000ull);
         (void)mbar_wait_bounded(smem_addr(rbar), 0u, nullptr, 10000000ull);
         (void)mbar_wait_bounded<true>(smem_addr(ssbar), 0u, nullptr, 10000000ull);
         grace_period(1000000ull);
@@ -378,10 +436,11 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
 static int ceil_div_s(int a, int b) { return (a + b - 1) / b; }
 
 bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, int smem_optin,
-                     int max_cluster, int C, SplitPlan* p, int groups) {
+                     int max_cluster, int C, SplitPlan* p, int groups, int rounds) {
     const int chunks = H / 8;
-    const int nseg = (shared ? R : 0) + 1 + R * K;
-    if (chunks < 2 || T < 1 || groups < 0) return false;
+    const int nsr = (shared ? R : 0) + 1;  // shared partials + residual
+    const int nseg = nsr + R * K;
+    if (chunks < 2 || T < 1 || groups < 0 || rounds < 1 || rounds > 2) return false;
     if (groups == 0) {
         // Automatic: the most column groups (of at least kSplitMinGroupChunks
         // chunks) that leave a plan -- fewer bytes through the cluster
@@ -389,7 +448,7 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
         // 16-CTA cluster beat one group by 1.1 us at T = 1.
         for (int g = 8; g > 1; g >>= 1)
             if (ceil_div_s(chunks, g) >= kSplitMinGroupChunks &&
-                plan_split_rows(R, K, H, shared, T, num_sms, smem_optin, max_cluster, C, p, g))
+                plan_split_rows(R, K, H, shared, T, num_sms, smem_optin, max_cluster, C, p, g, rounds))
                 return true;
         groups = 1;
     }
@@ -402,8 +461,26 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
         if (c < 2 || c > 16 || c > max_cluster || c % groups || last < 1) return false;
         const int cs = c / groups;
         if (cs < 2 || cs > nseg) return false;
-        const int ns = ceil_div_s(nseg, cs);
-        if (ns > kSplitMaxSegs) return false;
+        // Segment buffers: every segment of the busiest CTA (rank 0 of a
+        // group deals the most), or with two rounds its first nmid, the
+        // second half reusing them.  A copy round is one producer lane per
+        // segment.
+        int nbuf = 0;
+        bool second = false;
+        for (int r = 0; r < cs; ++r) {
+            const int ns_r = (nseg - r + cs - 1) / cs;
+            const int nsr_r = nsr > r ? (nsr - 1 - r) / cs + 1 : 0;
+            const int nmid_r = nsr_r + (ns_r - nsr_r + 1) / 2;
+            if (rounds == 1) {
+                if (ns_r > kSplitMaxSegs) return false;
+                nbuf = std::max(nbuf, ns_r);
+            } else {
+                if (nmid_r > kSplitMaxSegs || ns_r - nmid_r > kSplitMaxSegs) return false;
+                nbuf = std::max(nbuf, nmid_r);
+                second = second || ns_r > nmid_r;
+            }
+        }
+        if (rounds == 2 && !second) return false;  // nothing for a second round
         const int tile = ceil_div_s(gch, cs);
         if ((cs - 1) * tile >= last) return false;  // every CTA owns a tile, the shortest group too
         int cpt = 1;
@@ -414,7 +491,7 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
         const int seg_stride = ceil_div_s(gch * 16, 128) * 128;
         const int recv = ceil_div_s(cs * tile * 32, 128) * 128;
         const int row_f32 = ceil_div_s(gch * 32, 128) * 128;
-        const int smem = kSplitHeader + recv + std::max(row_f32, ns * seg_stride);
+        const int smem = kSplitHeader + recv + std::max(row_f32, nbuf * seg_stride);
         if (smem > smem_optin) return false;
         q->geo.C = c;
         q->geo.Cs = cs;
@@ -423,6 +500,7 @@ bool plan_split_rows(int R, int K, int H, bool shared, int64_t T, int num_sms, i
         q->geo.part_bytes = recv;
         q->geo.row_f32_bytes = row_f32;
         q->geo.tile_chunks = tile;
+        q->geo.rounds = rounds;
         q->cpt = cpt;
         q->threads = 32 + consumers;
         q->smem = smem;
@@ -511,6 +589,30 @@ bool split_rows_plan_fits(const SplitPlan& p, bool res_f32) {
     const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
     if (e != cudaSuccess) (void)cudaGetLastError();
     return e == cudaSuccess && n > 0;
+}
+
+bool split_prefer_two_rounds(int64_t T, int n1, int n2) { return n1 >= 1 && n1 < T && n2 > n1; }
+
+int split_rows_active_clusters(const SplitPlan& p, bool res_f32) {
+    const void* k = split_kernel_for(p.cpt, res_f32);
+    if (!k) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)p.geo.C);
+    cfg.blockDim = dim3((unsigned)p.threads);
+    cfg.dynamicSmemBytes = (size_t)p.smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.geo.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 cudaError_t launch_split_rows(const RowArgs& a, const SplitPlan& p, bool res_f32, cudaStream_t stream,
