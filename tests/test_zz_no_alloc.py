@@ -22,7 +22,7 @@ import pytest
 import torch
 
 import tp_reduce_moe_gb300 as arf
-from gen import make_inputs
+from gen import Config, make_inputs
 from tests._util import check_bf16, check_f32, run_oracle, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -91,16 +91,18 @@ def _check(out, r_out, ref, fp32, tag):
 # shape T = 64 four-CTA tiles with 48 KB slots and three producer warps, T = 200 eight-CTA tiles
 # with 24 KB slots, T = 300 (past the table) whole rows with a ragged last wave (300 mod 152);
 # glm T = 1 the split kernel in sixteen-CTA clusters; tiny T = 4 (six summands) and ar_only
-# T = 16 / 200 the one-shot kernel in sixteen-, eight- and two-CTA clusters
+# T = 16 / 200 the one-shot kernel in sixteen-, eight- and two-CTA clusters; the TP16 routing
+# profile (R = 16, K = 10, H = 8192) at T = 9 the split kernel in two copy rounds
 CASES = [("tiny", 4), ("dsv3_decode", 16), ("dsv3_decode", 24), ("dsv3_decode", 48),
          ("dsv3_decode", 72), ("prefill", 64), ("glm_gemma", 1), ("ar_only", 16), ("ar_only", 200),
-         ("prefill", 200), ("prefill", 300)]
+         ("prefill", 200), ("prefill", 300), ("tp16", 9)]
+TP16 = Config("tp16", 97, R=16, K=10, H=8192, Ts=(9,), eps=1e-6, weights="softmax", has_shared=True)
 
 
 @pytest.mark.parametrize("cfg,T", CASES, ids=[f"{c}-T{t}" for c, t in CASES])
 @pytest.mark.parametrize("fp32", [False, True])
 def test_noalloc_matches_the_oracle(noalloc, cfg, T, fp32):
-    inp = make_inputs(cfg, T)
+    inp = make_inputs(TP16 if cfg == "tp16" else cfg, T)
     ref = run_oracle(inp, want_abs=True)
     d = _to_dev(inp)
     for call in range(2):  # two calls in a row share the library's array
