@@ -339,6 +339,27 @@ ARFUSE_API int ar_workspace_last_regime(const ar_workspace* ws, int* ctas);
  * clusters the device co-schedules (a multiple of the CTAs per row). */
 ARFUSE_API int ar_workspace_last_grid(const ar_workspace* ws);
 
+/* The launch plan of the last launched call (on a dry-run workspace: of the
+ * last validated call, planned without the device's occupancy queries, so
+ * without their grid cap and form switches).  All zero before the first
+ * call.  Fields a regime does not use are 0. */
+typedef struct ar_plan_info {
+    int32_t regime;          /* AR_REGIME_CLUSTER / _STREAM / _ONESHOT / _SPLIT            */
+    int32_t ctas_per_row;    /* as ar_workspace_last_regime                                */
+    int32_t grid;            /* CTAs launched (as ar_workspace_last_grid)                  */
+    int32_t block;           /* threads per CTA                                           */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA                             */
+    int32_t column_groups;   /* split: column groups per row                              */
+    int32_t copy_rounds;     /* split: 1, or 2 (second routed half into reused buffers)   */
+    int32_t ring_slots;      /* cluster / stream: bulk-copy ring slots per CTA            */
+    int32_t ring_slot_bytes; /* cluster / stream: bytes per ring slot                     */
+    int32_t producer_warps;  /* cluster / stream: producer warps; split: 1                */
+    int32_t loads_per_thread; /* one-shot: register loads a thread holds (2 or 8)         */
+} ar_plan_info;
+
+/* Copy the last call's plan into *info.  AR_ERR_INVALID_ARG for NULL. */
+ARFUSE_API ar_status ar_workspace_last_plan(const ar_workspace* ws, ar_plan_info* info);
+
 /*
  * Regime table: the kernel regime (and CTAs per row) that AR_REGIME_AUTO runs
  * at each token count.  The fastest regime depends on T and on the shape, and

@@ -49,6 +49,11 @@ int main(void) {
     const int regime = ar_workspace_last_regime(ws, &ctas);
     expect(regime == AR_REGIME_SPLIT && ctas == 16, "the built-in table's plan for T = 4");
     expect(ar_workspace_last_grid(ws) == (int)(T * 16), "its grid");
+    ar_plan_info info;
+    expect(ar_workspace_last_plan(ws, &info) == AR_OK && info.regime == AR_REGIME_SPLIT &&
+               info.grid == (int)(T * 16) && info.column_groups == 4 && info.copy_rounds == 1,
+           "its plan");
+    expect(ar_workspace_last_plan(ws, NULL) == AR_ERR_INVALID_ARG, "plan into NULL");
 
     st = ar_finalize_rmsnorm(ws, E, T * K, perm, w, S, NULL, gamma, 0.0f, 1e-6f, T, R, K, H, out,
                              residual_out, 0, NULL);

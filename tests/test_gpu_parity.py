@@ -907,7 +907,7 @@ def test_split_any_cluster_size_and_groups(cfg, T, combos):
 
 
 # --------------------- the TP16 routing profile (R = 16, K = 10, H = 8192) through its table
-@pytest.mark.parametrize("T", [3, 12, 32, 72])
+@pytest.mark.parametrize("T", [3, 9, 12, 32, 72])
 def test_tp16_table_plans_meet_the_oracle(T):
     """Sixteen rank partials of top-10 rows at H = 8192 (177 segments per
     row): the built-in table's plan at decode and mid-range T -- split, tiles
@@ -920,6 +920,10 @@ def test_tp16_table_plans_meet_the_oracle(T):
     try:
         assert arf.ar_workspace_get_regime_table(ws), "a built-in table for this shape"
         check_all(ws, to_dev(inp), ref, f"tp16 T={T}", regimes=(arf.AR_REGIME_AUTO,))
+        plan = arf.ar_workspace_last_plan(ws)
+        if T <= 12:   # the split kernel: one copy round while its clusters fit one wave, else two
+            assert plan["regime"] == arf.AR_REGIME_SPLIT
+            assert plan["copy_rounds"] == (1 if T <= 6 else 2)
     finally:
         ws.destroy()
 
@@ -958,6 +962,7 @@ def test_split_two_rounds_meets_the_oracle(R, K, H, T, csize, groups):
         check_all(ws, d, ref, f"two rounds R={R} K={K} H={H} T={T} C={csize} G={groups}",
                   regimes=(arf.AR_REGIME_SPLIT,))
         assert arf.ar_workspace_last_regime(ws) == (arf.AR_REGIME_SPLIT, csize)
+        assert arf.ar_workspace_last_plan(ws)["copy_rounds"] == 2
         a1 = run_gpu(ws, d, fp32=True, regime=arf.AR_REGIME_SPLIT)
         a2 = run_gpu(ws, d, fp32=True, regime=arf.AR_REGIME_SPLIT)
         torch.cuda.synchronize()

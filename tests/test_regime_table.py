@@ -311,3 +311,43 @@ def test_last_grid_reports_the_planned_ctas(dsv3):
     regime, ctas = dsv3.plan(24)
     assert (regime, ctas) == (arf.AR_REGIME_CLUSTER, 4)
     assert arf.ar_workspace_last_grid(dsv3.ws) == 24 * 4      # one cluster per row when that fits
+
+
+def test_last_plan_reports_the_launch_shape():
+    """ar_workspace_last_plan: the plan of the last validated call -- split
+    column groups and copy rounds, streaming ring slots and producer warps,
+    one-shot loads per thread -- all zero before the first call."""
+    d = Shape(8, 8, 7168)
+    heavy = Shape(16, 10, 8192)
+    k0 = Shape(2, 0, 7168)
+    try:
+        assert set(arf.ar_workspace_last_plan(d.ws).values()) == {0}
+        d.plan(4)                                    # table: split, 16 CTAs, four groups
+        p = arf.ar_workspace_last_plan(d.ws)
+        assert (p["regime"], p["ctas_per_row"], p["grid"]) == (arf.AR_REGIME_SPLIT, 16, 64)
+        assert (p["column_groups"], p["copy_rounds"], p["producer_warps"]) == (4, 1, 1)
+        assert p["ring_slots"] == 0 and p["loads_per_thread"] == 0 and p["smem_bytes"] > 0
+        d.plan(64)                                   # table: four-CTA tiles
+        p = arf.ar_workspace_last_plan(d.ws)
+        assert (p["regime"], p["ctas_per_row"], p["grid"]) == (arf.AR_REGIME_CLUSTER, 4, 256)
+        assert p["ring_slots"] >= 2 and p["ring_slot_bytes"] > 0 and p["producer_warps"] >= 1
+        assert p["column_groups"] == 0 and p["copy_rounds"] == 0
+        assert p["grid"] == arf.ar_workspace_last_grid(d.ws)
+        k0.plan(16)                                  # one-shot, two loads per thread
+        p = arf.ar_workspace_last_plan(k0.ws)
+        assert p["regime"] == arf.AR_REGIME_ONESHOT and p["loads_per_thread"] == 2
+        assert p["block"] * p["ctas_per_row"] >= 7168 // 8
+        # heavy rows: one round in two column groups, two rounds in four
+        arf.ar_workspace_set_regime(heavy.ws, arf.AR_REGIME_SPLIT)
+        arf.ar_workspace_set_cluster_size(heavy.ws, 16)
+        heavy.plan(1)
+        one = arf.ar_workspace_last_plan(heavy.ws)
+        arf.ar_workspace_set_split_column_groups(heavy.ws, 4)
+        heavy.plan(1)
+        two = arf.ar_workspace_last_plan(heavy.ws)
+        assert (one["column_groups"], one["copy_rounds"]) == (2, 1)
+        assert (two["column_groups"], two["copy_rounds"]) == (4, 2)
+        assert 2 * (two["smem_bytes"] + 1024) <= 233472 < 2 * (one["smem_bytes"] + 1024)  # two CTAs per SM
+    finally:
+        for x in (d, heavy, k0):
+            x.ws.destroy()

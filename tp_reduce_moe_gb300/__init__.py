@@ -13,7 +13,8 @@ from .binding import (  # noqa: F401
     AR_VALIDATED,
     AR_WS_DRY_RUN, AR_WS_NORM_BF16_H, AR_WS_PDL, LIB_PATH, ArfuseError, Workspace, ar_finalize_rmsnorm, ar_rmsnorm,
     ar_status_string, ar_workspace_create, ar_workspace_destroy, ar_workspace_device_error,
-    ar_workspace_last_regime, ar_workspace_last_grid, ar_workspace_set_cluster_size, ar_workspace_set_regime,
+    ar_workspace_last_regime, ar_workspace_last_grid, ar_workspace_last_plan, PlanInfo,
+    ar_workspace_set_cluster_size, ar_workspace_set_regime,
     ar_workspace_set_producer_warps, ar_workspace_set_stage_bytes, load_library,
     AR_MAX_REGIME_RULES, RegimeRule, ar_workspace_get_regime_table, ar_workspace_set_regime_table,
     AR_MAX_HC_STREAMS, ar_mhc_post, AR_MAX_SPLIT_PARTS, ar_workspace_set_split_rows,

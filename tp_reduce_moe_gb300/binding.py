@@ -105,6 +105,8 @@ def load_library(path: str | None = None):
         lib.ar_workspace_last_regime.argtypes = [P, ctypes.POINTER(I)]
         lib.ar_workspace_last_grid.restype = I
         lib.ar_workspace_last_grid.argtypes = [P]
+        lib.ar_workspace_last_plan.restype = I
+        lib.ar_workspace_last_plan.argtypes = [P, P]
         lib.ar_status_string.restype = ctypes.c_char_p
         lib.ar_status_string.argtypes = [I]
         _lib = lib
@@ -268,6 +270,24 @@ def ar_workspace_last_regime(ws: Workspace):
 def ar_workspace_last_grid(ws: Workspace) -> int:
     """CTAs launched by the last call (0 before the first)."""
     return int(load_library().ar_workspace_last_grid(ctypes.c_void_p(ws.handle)))
+
+
+class PlanInfo(ctypes.Structure):
+    """The launch plan of a call (``ar_plan_info``)."""
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "regime", "ctas_per_row", "grid", "block", "smem_bytes", "column_groups", "copy_rounds",
+        "ring_slots", "ring_slot_bytes", "producer_warps", "loads_per_thread")]
+
+
+def ar_workspace_last_plan(ws: Workspace) -> dict:
+    """The last launched (dry run: validated) call's launch plan as a dict of
+    the ``ar_plan_info`` fields (regime, CTAs per row, grid, block, shared
+    memory, split column groups and copy rounds, ring slots and slot bytes,
+    producer warps, one-shot loads per thread); all zero before the first."""
+    info = PlanInfo()
+    _check(load_library().ar_workspace_last_plan(ctypes.c_void_p(ws.handle), ctypes.byref(info)),
+           "ar_workspace_last_plan")
+    return {name: int(getattr(info, name)) for name, _ in PlanInfo._fields_}
 
 
 def ar_workspace_device_error(ws: Workspace) -> int:

@@ -40,6 +40,7 @@ struct ar_workspace {
     int last_regime;
     int last_ctas;
     int last_grid;
+    ar_plan_info last_plan;
     unsigned long long stall_wait_ns;  // failure injection (whole-row streaming), 0 = off
     int table_n;  // rules in `table` (0: heuristic only)
     ar_regime_rule table[AR_MAX_REGIME_RULES];
@@ -358,6 +359,35 @@ void cluster_limits(int R, int K, int H, int num_sms, int smem_optin, int* max_c
             *max_cluster_split = arf::split_rows_max_cluster(xp.threads, xp.smem, xp.cpt);
 }
 
+// What the last call launched (or, on a dry-run workspace, planned).
+void record_plan(ar_workspace* ws, int regime, int ctas, int grid, const Plans& pl) {
+    ws->last_regime = regime;
+    ws->last_ctas = ctas;
+    ws->last_grid = grid;
+    ar_plan_info& i = ws->last_plan;
+    std::memset(&i, 0, sizeof i);
+    i.regime = regime;
+    i.ctas_per_row = ctas;
+    i.grid = grid;
+    if (regime == AR_REGIME_ONESHOT) {
+        i.block = pl.c.threads;
+        i.smem_bytes = pl.c.smem;
+        i.loads_per_thread = pl.c.maxt == arf::kClusterMaxTerms64 ? 8 : pl.c.maxt;
+    } else if (regime == AR_REGIME_SPLIT) {
+        i.block = pl.x.threads;
+        i.smem_bytes = pl.x.smem;
+        i.column_groups = pl.x.geo.C / pl.x.geo.Cs;
+        i.copy_rounds = pl.x.geo.rounds;
+        i.producer_warps = 1;
+    } else {
+        i.block = pl.s.threads;
+        i.smem_bytes = pl.s.smem;
+        i.ring_slots = pl.s.geo.nstages;
+        i.ring_slot_bytes = pl.s.geo.slot_bytes;
+        i.producer_warps = pl.s.geo.producers;
+    }
+}
+
 ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int32_t* perm,
               const float* w, const void* const* S, const void* residual, const void* gamma,
               float weight_bias, float eps, int64_t T, int R, int K, int H, void* out,
@@ -468,9 +498,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
                                                  : pl.s.grid;
 
     if (ws->flags & AR_WS_DRY_RUN) {
-        ws->last_regime = regime;
-        ws->last_ctas = ctas;
-        ws->last_grid = grid;
+        record_plan(ws, regime, ctas, grid, pl);
         return AR_VALIDATED;
     }
 
@@ -521,9 +549,7 @@ ar_status run(ar_workspace* ws, const void* const* E, int64_t rows_e, const int3
         (void)cudaGetLastError();
         return AR_ERR_CUDA;
     }
-    ws->last_regime = regime;
-    ws->last_ctas = ctas;
-    ws->last_grid = grid;
+    record_plan(ws, regime, ctas, grid, pl);
     return AR_OK;
 }
 
@@ -562,6 +588,7 @@ ar_status ar_workspace_create(int device, int ranks, int top_k, int hidden, int6
     ws->last_regime = 0;
     ws->last_ctas = 0;
     ws->last_grid = 0;
+    std::memset(&ws->last_plan, 0, sizeof ws->last_plan);
     install_builtin_table(ws);
 
     if (flags & AR_WS_DRY_RUN) {
@@ -816,6 +843,12 @@ ar_status ar_workspace_set_producer_warps(ar_workspace* ws, int warps) {
 }
 
 int ar_workspace_last_grid(const ar_workspace* ws) { return ws ? ws->last_grid : 0; }
+
+ar_status ar_workspace_last_plan(const ar_workspace* ws, ar_plan_info* info) {
+    if (!ws || !info) return AR_ERR_INVALID_ARG;
+    *info = ws->last_plan;
+    return AR_OK;
+}
 
 int ar_workspace_last_regime(const ar_workspace* ws, int* ctas) {
     if (!ws) return 0;
