@@ -373,6 +373,7 @@ def main_ours(args):
         step()
     torch.cuda.synchronize()
     regime, ctas = arf.ar_workspace_last_regime(ws)
+    plan = {k: v for k, v in arf.ar_workspace_last_plan(ws).items() if v and k not in ("regime", "ctas_per_row")}
 
     clocks = ClockSampler(smi_device_id(torch, local))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -453,7 +454,7 @@ def main_ours(args):
                 "data": "synthetic",
                 "config": headline_config(args.workload, T, world),
                 "us_per_call": round(1e3 * ms_per_step, 3),
-                "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas, "gated": bool(args.gated),
+                "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas, "plan": plan, "gated": bool(args.gated),
                 "pdl": bool(args.pdl),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps, "clocks": clocks.summary(), "sweep": sweep,
@@ -681,6 +682,7 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
     torch.cuda.current_stream(dev).wait_stream(side)
     torch.cuda.synchronize()
     regime, ctas = arf.ar_workspace_last_regime(ws)
+    plan = {k: v for k, v in arf.ar_workspace_last_plan(ws).items() if v and k not in ("regime", "ctas_per_row")}
     calls = WARM_CALLS if mode == "warm" else n_sets
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
@@ -709,7 +711,7 @@ def sweep_point(arf, torch, dev, stream, peak, l2, cfg, name, T, force, csize=0,
     return {"workload": name, "R": cfg.R, "K": cfg.K, "H": cfg.H, "T": T,
             "us_per_call": round(us, 3), "GBps": round(gbs, 1),
             "frac_of_hbm_peak": round(gbs / peak, 4),
-            "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas,
+            "regime": REGIME_NAMES.get(regime, "?"), "ctas": ctas, "plan": plan,
             "forced": force != 0, "calls_per_graph": calls, "mode": mode, "perm": perm_kind,
             "gated": gated,
             "pdl": pdl, "device_error": err}
