@@ -105,7 +105,8 @@ def time_regime(ws, inp: _Inputs, eps: float, regime: int, ctas: int, dev, reps:
                 stage_bytes: int = 0, producer_warps: int = 0):
     """Median µs per call of one forced (regime, ctas_per_row, stage_bytes,
     producer_warps), or None when the library has no plan for it.  Returns
-    (us, regime_run, ctas_run)."""
+    (us, regime_run, ctas_run, plan_run) -- plan_run the nonzero fields of
+    the launch plan (ar_workspace_last_plan)."""
     arf.ar_workspace_set_regime(ws, regime)
     arf.ar_workspace_set_cluster_size(ws, ctas)
     arf.ar_workspace_set_stage_bytes(ws, stage_bytes)
@@ -118,11 +119,12 @@ def time_regime(ws, inp: _Inputs, eps: float, regime: int, ctas: int, dev, reps:
                 inp.call(ws, i, eps, side)
     except arf.ArfuseError as e:
         if e.status == arf.AR_ERR_UNSUPPORTED:
-            return None, regime, ctas
+            return None, regime, ctas, {}
         raise
     torch.cuda.current_stream(dev).wait_stream(side)
     torch.cuda.synchronize(dev)
     ran = arf.ar_workspace_last_regime(ws)
+    plan = {k: v for k, v in arf.ar_workspace_last_plan(ws).items() if v and k not in ("regime", "ctas_per_row")}
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         cs = torch.cuda.current_stream(dev)
@@ -141,7 +143,7 @@ def time_regime(ws, inp: _Inputs, eps: float, regime: int, ctas: int, dev, reps:
         torch.cuda.synchronize(dev)
         per.append(a.elapsed_time(b) * 1e3 / inp.n)
     del g
-    return statistics.median(per), ran[0], ran[1]
+    return statistics.median(per), ran[0], ran[1], plan
 
 
 def arf_regime(name: str) -> int:
@@ -168,10 +170,11 @@ def tune(R: int, K: int, H: int, tokens=DEFAULT_TOKENS, shared: bool = True, eps
         ws = arf.ar_workspace_create(R, K, H, T, eps, device=device)
         best = None
         for regime, ctas, sb, pw in cands:
-            us, ran_regime, ran_ctas = time_regime(ws, inp, eps, regime, ctas, dev, stage_bytes=sb,
-                                                   producer_warps=pw)
+            us, ran_regime, ran_ctas, plan = time_regime(ws, inp, eps, regime, ctas, dev, stage_bytes=sb,
+                                                         producer_warps=pw)
             pt = {"T": T, "regime": REGIME_NAME[regime], "ctas_per_row": ctas, "stage_bytes": sb,
-                  "producer_warps": pw, "us": us, "ran": [REGIME_NAME.get(ran_regime, "?"), ran_ctas]}
+                  "producer_warps": pw, "us": us, "ran": [REGIME_NAME.get(ran_regime, "?"), ran_ctas],
+                  "plan": plan}
             points.append(pt)
             if log:
                 log(pt)
