@@ -151,13 +151,15 @@ def arf_regime(name: str) -> int:
 
 
 def tune(R: int, K: int, H: int, tokens=DEFAULT_TOKENS, shared: bool = True, eps: float = 1e-6,
-         device: int = 0, cands=None, log=None, margin: float = SWITCH_MARGIN):
+         device: int = 0, cands=None, log=None, margin: float = SWITCH_MARGIN, pdl: bool = False):
     """Time every candidate at every T; returns (rules, points).
 
     rules: [(max_tokens, regime, ctas_per_row, stage_bytes, producer_warps)]:
     the fastest candidate at each T, except that the running rule is kept
     while it is within `margin` of the fastest, consecutive equal choices
     merged; points: one dict per (T, candidate) with the measured µs.
+    pdl: the calls launch with programmatic dependent launch (back to back in
+    the timed graph, so a call's start-up overlaps the previous call).
     """
     dev = torch.device("cuda", device)
     torch.cuda.set_device(dev)
@@ -167,7 +169,7 @@ def tune(R: int, K: int, H: int, tokens=DEFAULT_TOKENS, shared: bool = True, eps
     for T in sorted(set(int(t) for t in tokens)):
         n_sets = int(min(4096, max(2, math.ceil(3 * l2 / problem_bytes(R, K, H, T, shared)))))
         inp = _Inputs(R, K, H, T, shared, n_sets, dev)
-        ws = arf.ar_workspace_create(R, K, H, T, eps, device=device)
+        ws = arf.ar_workspace_create(R, K, H, T, eps, device=device, flags=arf.AR_WS_PDL if pdl else 0)
         best = None
         for regime, ctas, sb, pw in cands:
             us, ran_regime, ran_ctas, plan = time_regime(ws, inp, eps, regime, ctas, dev, stage_bytes=sb,
@@ -212,11 +214,14 @@ def main(argv=None):
     p.add_argument("--device", type=int, default=0)
     p.add_argument("--margin", type=float, default=SWITCH_MARGIN,
                    help="keep the running rule while within this fraction of the fastest")
+    p.add_argument("--pdl", action="store_true",
+                   help="time calls launched with programmatic dependent launch (AR_WS_PDL), for a "
+                        "table that such workspaces use")
     args = p.parse_args(argv)
     shared = not args.no_shared or args.K == 0
     rules, points = tune(args.R, args.K, args.H, [int(t) for t in args.tokens.split(",")],
-                         shared=shared, eps=args.eps, device=args.device, margin=args.margin)
-    print(json.dumps({"R": args.R, "K": args.K, "H": args.H, "shared": shared,
+                         shared=shared, eps=args.eps, device=args.device, margin=args.margin, pdl=args.pdl)
+    print(json.dumps({"R": args.R, "K": args.K, "H": args.H, "shared": shared, "pdl": args.pdl,
                       "device": torch.cuda.get_device_name(args.device),
                       "rules": [[t, REGIME_NAME[r], c, sb, pw] for t, r, c, sb, pw in rules],
                       "points": points}))
