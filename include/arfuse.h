@@ -341,8 +341,10 @@ ARFUSE_API int ar_workspace_last_grid(const ar_workspace* ws);
 
 /* The launch plan of the last launched call (on a dry-run workspace: of the
  * last validated call, planned without the device's occupancy queries, so
- * without their grid cap and form switches).  All zero before the first
- * call.  Fields a regime does not use are 0. */
+ * without their grid cap and form switches): which of the kernel forms the
+ * per-shape choice picked (the crossovers between the fused operator's
+ * algorithms move with the shape: sglang PR #37196, Known gaps).  All zero
+ * before the first call.  Fields a regime does not use are 0. */
 typedef struct ar_plan_info {
     int32_t regime;          /* AR_REGIME_CLUSTER / _STREAM / _ONESHOT / _SPLIT            */
     int32_t ctas_per_row;    /* as ar_workspace_last_regime                                */
