@@ -41,8 +41,14 @@ __global__ void __launch_bounds__(kMhcThreads)
     const int per_token = (chunks + kMhcThreads - 1) / kMhcThreads;
     const int64_t t = blockIdx.x / per_token;
     const int chunk = (int)(blockIdx.x % per_token) * kMhcThreads + threadIdx.x;
-    for (int q = threadIdx.x; q < hc * hc; q += blockDim.x) s_comb[q] = __ldg(a.comb + t * hc * hc + q);
-    for (int q = threadIdx.x; q < hc; q += blockDim.x) s_post[q] = __ldg(a.post + t * hc + q);
+    // The token's coefficients go to registers first and to shared memory
+    // only after the data loads are out: a warp issues in order, so storing
+    // a load's value stalls it until the value arrives, and would hold back
+    // the loads behind it by a memory round trip.
+    const int nq = hc * hc;  // <= 64 < kMhcThreads
+    float comb_v = 0.0f, post_v = 0.0f;
+    if ((int)threadIdx.x < nq) comb_v = __ldg(a.comb + t * nq + threadIdx.x);
+    if ((int)threadIdx.x < hc) post_v = __ldg(a.post + t * hc + threadIdx.x);
 
     float y[8];
     uint4 xv[kMhcMaxStreams];
@@ -74,6 +80,8 @@ __global__ void __launch_bounds__(kMhcThreads)
                 }
         }
     }
+    if ((int)threadIdx.x < nq) s_comb[threadIdx.x] = comb_v;
+    if ((int)threadIdx.x < hc) s_post[threadIdx.x] = post_v;
     __syncthreads();  // coefficients staged
     if (!active) return;
     const int64_t col = (int64_t)chunk * 8;
