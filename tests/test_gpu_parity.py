@@ -940,6 +940,8 @@ TWO_ROUND_CASES = [
     (8, 8, 7168, 1, 16, 8),
     (8, 8, 7168, 5, 16, 8),
     (8, 8, 7168, 3, 4, 2),
+    (12, 12, 6144, 2, 12, 3),      # twelve-CTA clusters in three groups, 40 segments per CTA
+    (10, 14, 6152, 3, 12, 3),      # ragged column groups (769 chunks), 38 segments per CTA
 ]
 
 
