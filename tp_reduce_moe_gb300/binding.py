@@ -307,19 +307,24 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
-def _need(t, dtype, shape, name):
+def _need(t, dtype, shape, name, index=None):
     if isinstance(t, int):       # raw device address: the caller vouches for it
         return
+    # one combined test on the common path (a call checks ~20 tensors); the
+    # name is formatted only for the error
+    if t.dtype is dtype and t.shape == shape and t.is_contiguous():
+        return
+    if index is not None:
+        name = f"{name}[{index}]"
     if t.dtype != dtype:
         raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name}: must be contiguous")
+    raise ValueError(f"{name}: must be contiguous")
 
 
 def _ptr_array(ts):
-    return (ctypes.c_void_p * len(ts))(*[_ptr(t) for t in ts])
+    return (ctypes.c_void_p * len(ts))(*[t if isinstance(t, int) else t.data_ptr() for t in ts])
 
 
 def _stream_handle(stream, device) -> int:
@@ -353,7 +358,7 @@ def ar_finalize_rmsnorm(ws: Workspace, expert_out, perm, topk_w, shared_out, res
     if rows_e is None:
         rows_e = expert_out[0].shape[0] if K > 0 else 0
     for r, e in enumerate(expert_out):
-        _need(e, torch.bfloat16, (rows_e, H), f"expert_out[{r}]")
+        _need(e, torch.bfloat16, (rows_e, H), "expert_out", r)
     if K > 0:
         _need(perm, torch.int32, (T, K), "perm")
         _need(topk_w, torch.float32, (T, K), "topk_w")
@@ -361,7 +366,7 @@ def ar_finalize_rmsnorm(ws: Workspace, expert_out, perm, topk_w, shared_out, res
         if len(shared_out) != R:
             raise ValueError("shared_out must have R entries")
         for r, s in enumerate(shared_out):
-            _need(s, torch.bfloat16, (T, H), f"shared_out[{r}]")
+            _need(s, torch.bfloat16, (T, H), "shared_out", r)
     _need(residual, torch.bfloat16, (T, H), "residual")
     _need(gamma, torch.bfloat16, (H,), "gamma")
     if shared_gate is not None:
@@ -378,9 +383,9 @@ def ar_finalize_rmsnorm(ws: Workspace, expert_out, perm, topk_w, shared_out, res
     e_arr = _ptr_array(expert_out) if K > 0 else None
     s_arr = _ptr_array(shared_out) if shared_out is not None else None
     head = (ctypes.c_void_p(ws.handle),
-            ctypes.cast(e_arr, ctypes.c_void_p) if e_arr is not None else None,
+            ctypes.addressof(e_arr) if e_arr is not None else None,
             int(rows_e), _ptr(perm) if K > 0 else None, _ptr(topk_w) if K > 0 else None,
-            ctypes.cast(s_arr, ctypes.c_void_p) if s_arr is not None else None)
+            ctypes.addressof(s_arr) if s_arr is not None else None)
     tail = (_ptr(residual), _ptr(gamma), float(weight_bias), float(eps), int(T), int(R), int(K),
             int(H), _ptr(out), _ptr(residual_out), 1 if residual_out_fp32 else 0,
             _stream_handle(stream, dev) if not ws.dry_run else None)
@@ -406,7 +411,7 @@ def ar_rmsnorm(ws: Workspace, partials, residual, gamma, weight_bias: float, eps
     if len(partials) != R:
         raise ValueError(f"partials has {len(partials)} entries, workspace has R={R}")
     for r, s in enumerate(partials):
-        _need(s, torch.bfloat16, (T, H), f"partials[{r}]")
+        _need(s, torch.bfloat16, (T, H), "partials", r)
     _need(residual, torch.bfloat16, (T, H), "residual")
     _need(gamma, torch.bfloat16, (H,), "gamma")
     dev = residual.device if not isinstance(residual, int) else None
@@ -420,7 +425,7 @@ def ar_rmsnorm(ws: Workspace, partials, residual, gamma, weight_bias: float, eps
           "residual_out")
     p_arr = _ptr_array(partials)
     st = load_library().ar_rmsnorm(
-        ctypes.c_void_p(ws.handle), ctypes.cast(p_arr, ctypes.c_void_p), int(R), _ptr(residual),
+        ctypes.c_void_p(ws.handle), ctypes.addressof(p_arr), int(R), _ptr(residual),
         _ptr(gamma), float(weight_bias), float(eps), int(T), int(H), _ptr(out), _ptr(residual_out),
         1 if residual_out_fp32 else 0, _stream_handle(stream, dev) if not ws.dry_run else None)
     _check(st, "ar_rmsnorm", ok=(AR_OK, AR_VALIDATED) if ws.dry_run else (AR_OK,))
@@ -444,7 +449,7 @@ def ar_mhc_post(ws: Workspace, partials, streams, post, comb, out=None, stream=N
     if hc is None:
         hc = streams.shape[1] if not isinstance(streams, int) else post.shape[1]
     for r, p in enumerate(partials):
-        _need(p, torch.bfloat16, (T, H), f"partials[{r}]")
+        _need(p, torch.bfloat16, (T, H), "partials", r)
     _need(streams, torch.bfloat16, (T, hc, H), "streams")
     _need(post, torch.float32, (T, hc), "post")
     _need(comb, torch.float32, (T, hc, hc), "comb")
