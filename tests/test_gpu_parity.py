@@ -972,3 +972,40 @@ def test_split_two_rounds_meets_the_oracle(R, K, H, T, csize, groups):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+@pytest.mark.parametrize("bf16_h", [False, True])
+def test_split_two_rounds_gated_and_bf16_h(bf16_h):
+    """Two copy rounds combined with the variants that change the first
+    round's coefficients (a gated shared expert: the shared partials scaled by
+    sigmoid(gate[t])) and the epilogue (the norm reading h rounded to bf16),
+    both residual_out types, against the oracle."""
+    from gen import make_gate_logits
+    R, K, H, T = 16, 10, 8192, 9
+    cfg = Config("two_rounds_gated", 99, R=R, K=K, H=H, Ts=(T,), eps=1e-6, weights="softmax", has_shared=True)
+    inp = make_inputs(cfg, T)
+    gate = make_gate_logits(T)
+    a = oracle_args(inp)
+    ref = oracle.ar_finalize_rmsnorm_ref(a["E"], a["perm"], a["w"], a["S"], a["residual"], a["gamma"],
+                                         a["weight_bias"], a["eps"], want_abs=True, shared_gate=gate.numpy(),
+                                         h_bf16_before_norm=bf16_h)
+    ws = arf.ar_workspace_create(R, K, H, T, inp["eps"], device=0,
+                                 flags=arf.AR_WS_NORM_BF16_H if bf16_h else 0)
+    try:
+        arf.ar_workspace_set_cluster_size(ws, 16)
+        arf.ar_workspace_set_split_column_groups(ws, 4)
+        d = to_dev(inp)
+        g = gate.to(DEV)
+        for fp32 in (False, True):
+            out, r_out = run_gpu(ws, d, fp32=fp32, regime=arf.AR_REGIME_SPLIT, shared_gate=g)
+            torch.cuda.synchronize()
+            assert arf.ar_workspace_last_plan(ws)["copy_rounds"] == 2
+            tag = f"two rounds gated bf16_h={bf16_h} fp32={fp32}"
+            check_bf16(out, ref["out"], tag + " out")
+            if fp32:
+                check_f32(r_out, ref["h"], ref["abs"], tag + " residual_out")
+            else:
+                check_bf16(r_out, ref["h"], tag + " residual_out")
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
