@@ -1009,3 +1009,62 @@ def test_split_two_rounds_gated_and_bf16_h(bf16_h):
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+# ------------------------- independent callers: a workspace each, own streams and threads
+def test_two_workspaces_on_two_streams_and_threads():
+    """Two callers, each with its own workspace and stream -- whole rows whose
+    last wave splits rows over CTAs (the workspace's scratch and counters)
+    and column tiles over clusters -- launched interleaved without host syncs,
+    first from one host thread, then from two threads at once (the library's
+    shared host state: plan caches, occupancy queries).  Every output against
+    the oracle; the error words stay clean."""
+    import threading
+    cases = [("prefill", 300), ("dsv3_decode", 64)]
+    inps = [make_inputs(c, T) for c, T in cases]
+    refs = [run_oracle(x) for x in inps]
+    wss = [make_ws(x) for x in inps]
+    streams = [torch.cuda.Stream() for _ in cases]
+    try:
+        devs = [to_dev(x) for x in inps]
+        outs = [(torch.empty_like(d["residual"]), torch.empty_like(d["residual"])) for d in devs]
+
+        def call(i):
+            with torch.cuda.stream(streams[i]):
+                run_gpu(wss[i], devs[i], out=outs[i][0], residual_out=outs[i][1], stream=streams[i])
+
+        torch.cuda.synchronize()
+        for _ in range(10):           # one host thread, interleaved on two streams
+            call(0)
+            call(1)
+        torch.cuda.synchronize()
+        for i, (c, T) in enumerate(cases):
+            check_bf16(outs[i][0], refs[i]["out"], f"interleaved {c} T={T} out")
+            check_bf16(outs[i][1], refs[i]["h"], f"interleaved {c} T={T} residual_out")
+            outs[i][0].zero_()
+            outs[i][1].zero_()
+        torch.cuda.synchronize()
+        errors = []
+
+        def worker(i):
+            try:
+                for _ in range(25):
+                    call(i)
+                streams[i].synchronize()
+            except Exception as e:  # noqa: BLE001 -- reported by the main thread
+                errors.append(e)
+
+        threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(cases))]
+        for th in threads:
+            th.start()
+        for th in threads:
+            th.join()
+        assert not errors, errors
+        torch.cuda.synchronize()
+        for i, (c, T) in enumerate(cases):
+            check_bf16(outs[i][0], refs[i]["out"], f"threads {c} T={T} out")
+            check_bf16(outs[i][1], refs[i]["h"], f"threads {c} T={T} residual_out")
+            assert arf.ar_workspace_device_error(wss[i]) == 0
+    finally:
+        for ws in wss:
+            ws.destroy()
