@@ -1068,3 +1068,41 @@ def test_two_workspaces_on_two_streams_and_threads():
     finally:
         for ws in wss:
             ws.destroy()
+
+
+def test_cuda_graph_capture_of_a_first_call_with_plan_switch():
+    """The first call of a fresh shape captured straight into a CUDA graph,
+    no warm-up call: its plan needs the device's occupancy queries (here the
+    split kernel's switch to two copy rounds, R = 15, K = 10, H = 8192 -- a
+    shape no other test plans), which must be legal during stream capture.
+    Replays after overwriting the inputs meet the oracle."""
+    R, K, H, T = 15, 10, 8192, 9
+    cfg = Config("capture_first", 100, R=R, K=K, H=H, Ts=(T,), eps=1e-6, weights="softmax", has_shared=True)
+    inp = make_inputs(cfg, T, seed=1)
+    ws = arf.ar_workspace_create(R, K, H, T, 1e-6, device=0)
+    try:
+        arf.ar_workspace_set_cluster_size(ws, 16)
+        d = to_dev(inp)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+        r_out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run_gpu(ws, d, regime=arf.AR_REGIME_SPLIT, out=out, residual_out=r_out)
+        assert arf.ar_workspace_last_plan(ws)["copy_rounds"] == 2
+        for seed in (2, 3):
+            new = make_inputs(cfg, T, seed=seed)
+            for key in ("E", "S"):
+                for dst, src in zip(d[key], new[key]):
+                    dst.copy_(src)
+            for key in ("perm", "w", "residual", "gamma"):
+                d[key].copy_(new[key])
+            g.replay()
+            torch.cuda.synchronize()
+            ref = run_oracle(new)
+            check_bf16(out, ref["out"], f"captured first call seed={seed} out")
+            check_bf16(r_out, ref["h"], f"captured first call seed={seed} residual_out")
+        del g
+        assert arf.ar_workspace_device_error(ws) == 0
+    finally:
+        ws.destroy()
