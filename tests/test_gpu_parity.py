@@ -1106,3 +1106,34 @@ def test_cuda_graph_capture_of_a_first_call_with_plan_switch():
         assert arf.ar_workspace_device_error(ws) == 0
     finally:
         ws.destroy()
+
+
+def test_pdl_chain_through_two_round_split_plans():
+    """AR_WS_PDL with the split kernel in two copy rounds (the TP16 table at
+    T = 9): calls launched back to back, each reading the previous call's
+    residual_out, every step against the oracle."""
+    R, K, H, T = 16, 10, 8192, 9
+    cfg = Config("tp16", 97, R=R, K=K, H=H, Ts=(T,), eps=1e-6, weights="softmax", has_shared=True)
+    inp = make_inputs(cfg, T)
+    ws = arf.ar_workspace_create(R, K, H, T, inp["eps"], device=0, flags=arf.AR_WS_PDL)
+    try:
+        d = to_dev(inp)
+        steps = 4
+        res = [d["residual"].clone()] + [torch.empty_like(d["residual"]) for _ in range(steps)]
+        outs = [torch.empty_like(d["residual"]) for _ in range(steps)]
+        for n in range(steps):
+            dn = dict(d)
+            dn["residual"] = res[n]
+            run_gpu(ws, dn, out=outs[n], residual_out=res[n + 1])
+        torch.cuda.synchronize()
+        plan = arf.ar_workspace_last_plan(ws)
+        assert plan["regime"] == arf.AR_REGIME_SPLIT and plan["copy_rounds"] == 2
+        assert arf.ar_workspace_device_error(ws) == 0
+        for n in range(steps):
+            step = dict(inp)
+            step["residual"] = res[n].cpu()
+            ref = run_oracle(step)
+            check_bf16(outs[n], ref["out"], f"pdl two-round chain step {n} out")
+            check_bf16(res[n + 1], ref["h"], f"pdl two-round chain step {n} residual_out")
+    finally:
+        ws.destroy()
