@@ -152,6 +152,10 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
         hv[m] = warp > 0 && q < 2 * ntile_c;
         gpre[m] = hv[m] ? ld_early8(a.gamma + (int64_t)tile0 * 8 + (int64_t)q * 4) : make_uint2(0, 0);
     }
+    // a gated shared expert's gate logit, for the warp that writes the shared
+    // partials' coefficients (requested with the metadata, read after its
+    // copies are out)
+    const uint32_t gate_bits = (warp == 1 && a.shared_gate) ? ld_early4(a.shared_gate + t) : 0u;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&bar[0]), 1);
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads, 1)
             if (i < nsr_c) {
                 const uint16_t* src = (s < nS ? a.S[s] + t * H : a.residual + t * H) + col0;
                 bulk_g2s(dst, src, row_bytes, smem_addr(&bar[0]), pol);
-                coef[i] = s < nS ? shared_coef(a, t) : 1.0f;
+                coef[i] = s < nS && a.shared_gate ? 1.0f / (1.0f + expf(-__uint_as_float(gate_bits))) : 1.0f;
             }
             __syncwarp();
             if (lane == 0 && nsr_c > 0) mbar_arrive_expect_tx(smem_addr(&bar[0]), (uint32_t)nsr_c * row_bytes);
