@@ -58,8 +58,12 @@ def _profiler_ready():
     ("prefill", 200, arf.AR_REGIME_STREAM),      # whole rows, last wave split over CTAs
     ("dsv3_decode", 4, arf.AR_REGIME_ONESHOT),   # one-shot kernel
     ("ar_only", 16, arf.AR_REGIME_AUTO),         # K = 0 entry point
+    ("tp16", 9, arf.AR_REGIME_AUTO),             # split kernel in two copy rounds
 ])
 def test_one_call_is_one_kernel_launch(cfg, T, regime):
+    if cfg == "tp16":
+        from gen import Config
+        cfg = Config("tp16", 97, R=16, K=10, H=8192, Ts=(T,), eps=1e-6, weights="softmax", has_shared=True)
     inp = make_inputs(cfg, T)
     d = _to_dev(inp)
     ws = arf.ar_workspace_create(inp["R"], inp["K"], inp["H"], T, inp["eps"], device=0)
