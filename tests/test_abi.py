@@ -298,6 +298,14 @@ def test_binding_checks_shapes(lib, ws):
     with pytest.raises(TypeError):
         arf.ar_finalize_rmsnorm(ws, E, torch.zeros(4, 2, dtype=torch.int64), x(4, 2, dt=torch.float32),
                                 None, x(4, H), x(H), 0.0, EPS)
+    # the message names the tensor, with its index in a list
+    perm, w = torch.zeros(4, 2, dtype=torch.int32), x(4, 2, dt=torch.float32)
+    with pytest.raises(TypeError, match=r"expert_out\[1\]: dtype"):
+        arf.ar_finalize_rmsnorm(ws, [E[0], x(8, H, dt=torch.float16)], perm, w, None, x(4, H), x(H), 0.0, EPS)
+    with pytest.raises(ValueError, match=r"expert_out\[0\]: must be contiguous"):
+        arf.ar_finalize_rmsnorm(ws, [x(H, 8).t(), E[1]], perm, w, None, x(4, H), x(H), 0.0, EPS)
+    with pytest.raises(ValueError, match=r"shared_out\[1\]: shape"):
+        arf.ar_finalize_rmsnorm(ws, E, perm, w, [x(4, H), x(3, H)], x(4, H), x(H), 0.0, EPS)
 
 
 # ------------------------------------------------------------ gated shared expert
